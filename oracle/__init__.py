@@ -1,0 +1,144 @@
+"""Plain fp64 CPU oracle for one-pass tree verification.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg call it; the product path never does. It shares
+no code with the CUDA library. The arithmetic lives in ``oracle.c`` (plain C,
+fp64, optional OpenMP); this module only builds it with gcc and marshals numpy
+arrays.
+
+Functions (the C file cites the passage each one follows):
+  tree_mask(parent)                      -> anc [B,N,W] uint64, depth [B,N], status [B]
+  tree_attn(q, k, v, seq_lens, parent, scale, rows=None) -> out [R,D] f64, lse [R] f64
+  spec_accept(target, draft, tokens, parent, u_accept, u_bonus) -> dict
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc into _build/liboracle.so (IEEE fp64, no FMA contraction)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.oracle_tree_mask.argtypes = [P, I, I, P, P, P]
+            lib.oracle_tree_mask.restype = I
+            lib.oracle_tree_attn.argtypes = [P, P, P, I, P, P, I, I, I, I, I, ctypes.c_double,
+                                             P, I, P, P]
+            lib.oracle_tree_attn.restype = I
+            lib.oracle_spec_accept.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P, P, P]
+            lib.oracle_spec_accept.restype = I
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = I
+            lib.oracle_set_threads.argtypes = [I]
+            lib.oracle_set_threads.restype = None
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+def tree_mask(parent):
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    if parent.ndim == 1:
+        parent = parent[None]
+    B, N = parent.shape
+    W = max(1, (N + 63) // 64)
+    anc = np.zeros((B, N, W), dtype=np.uint64)
+    depth = np.zeros((B, N), dtype=np.int32)
+    status = np.zeros((B,), dtype=np.int32)
+    rc = _load().oracle_tree_mask(_p(parent), B, N, _p(anc), _p(depth), _p(status))
+    assert rc == 0
+    return anc, depth, status
+
+
+def tree_attn(q, k, v, seq_lens, parent, scale=None, rows=None):
+    """q [B,N,Hq,D]; k, v [B,Tcap,Hkv,D] logical order (all float32 values)."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    B, N, Hq, D = q.shape
+    Tcap, Hkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    if rows is None:
+        R = B * N * Hq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
+        R = rows_arr.shape[0]
+    out = np.zeros((R, D), dtype=np.float64)
+    lse = np.zeros((R,), dtype=np.float64)
+    rc = _load().oracle_tree_attn(_p(q), _p(k), _p(v), Tcap, _p(seq_lens), _p(parent), B, N, Hq,
+                                  Hkv, D, float(scale), _p(rows_arr), R, _p(out), _p(lse))
+    if rc != 0:
+        raise ValueError("oracle_tree_attn: bad arguments")
+    return out, lse
+
+
+def spec_accept(target, draft, tokens, parent, u_accept, u_bonus):
+    target = np.ascontiguousarray(target, dtype=np.float32)
+    draft = np.ascontiguousarray(draft, dtype=np.float32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32)
+    u_bonus = np.ascontiguousarray(u_bonus, dtype=np.float32)
+    B, N, V = target.shape
+    assert draft.shape == (B, N, V) and tokens.shape == (B, N) and parent.shape == (B, N)
+    assert u_accept.shape == (B, N) and u_bonus.shape == (B,)
+    out = {
+        "accept_len": np.zeros((B,), np.int32),
+        "path": np.zeros((B, N), np.int32),
+        "out_tokens": np.zeros((B, N), np.int32),
+        "ratio": np.zeros((B, N), np.float64),
+        "accept_margin": np.zeros((B, N), np.float64),
+        "bonus_margin": np.zeros((B,), np.float64),
+        "n_rejects": np.zeros((B,), np.int32),
+        "status": np.zeros((B,), np.int32),
+    }
+    rc = _load().oracle_spec_accept(
+        _p(target), _p(draft), _p(tokens), _p(parent), _p(u_accept), _p(u_bonus), B, N, V,
+        _p(out["accept_len"]), _p(out["path"]), _p(out["out_tokens"]), _p(out["ratio"]),
+        _p(out["accept_margin"]), _p(out["bonus_margin"]), _p(out["n_rejects"]), _p(out["status"]))
+    assert rc == 0
+    return out

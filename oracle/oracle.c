@@ -1,0 +1,322 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for one-pass tree verification.
+ *
+ * TEST INFRASTRUCTURE ONLY. Tests, the smoke check and the benchmark's CPU
+ * baseline call it; the product path never does. It shares no code, header,
+ * table or helper with the CUDA library, and it follows the definitions on the
+ * pages literally, with no blocking, fusion or reordering:
+ *
+ *   oracle_tree_mask   "EAGLE 演化史 (1 → 2 → 3) 与 DFlash 的回答", § Tree
+ *                      Verification 详解, B (the tree is flattened in BFS
+ *                      order; a node sees only its ancestors, never siblings or
+ *                      cousins) and G step 3 (the 7-node worked tree).
+ *   oracle_tree_attn   same page, § A and § B (one target pass over prefix +
+ *                      tree; each node attends to the prefix, its ancestors and
+ *                      itself; its output equals running prompt + root->node
+ *                      path as an ordinary causal sequence).
+ *   oracle_spec_accept "Eagle vs DFlash", speculative sampling rule (accept
+ *                      x with probability min(1, p(x)/q(x)); on rejection
+ *                      sample from normalize(max(0, p - q))); "EAGLE 演化史"
+ *                      § C (walk from the root, children in order, residual
+ *                      after each rejected sibling, sample from the residual
+ *                      when every child is rejected, longest accepted path)
+ *                      and § G steps 5-6 (worked walk with a bonus token).
+ *
+ * Readings where the pages are silent (all listed in the design notes):
+ *   - N counts nodes including the root; node 0 is the root, whose KV is at
+ *     logical position L_b, and node j's KV is at L_b + j.
+ *   - head h reads KV head h / (Hq / Hkv); the softmax scale is given.
+ *   - a sequence with an invalid parent[] gets status bit 1; its masks hold
+ *     only each node's own bit (depth 0), and the acceptance outputs are "no
+ *     result" (-1 everywhere, accept_len 0).
+ *   - siblings are tried in ascending node index; the draft distribution for
+ *     a child is the draft softmax at its parent, and only the target side is
+ *     replaced by the residual after a rejection.
+ *   - accept iff u * q(x) < p~(x); a residual with zero mass leaves p~ as it
+ *     was; the bonus token is the smallest k whose cumulative p~ exceeds
+ *     u * sum(p~), else the last k with p~(k) > 0.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_BAD_PARENT 1
+#define ORACLE_BAD_TOKEN 2
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* A parent array is a BFS-flattened tree: node 0 is the root (parent -1) and
+ * every other node's parent comes before it. */
+static int tree_is_valid(const int32_t *parent, int N) {
+    if (N < 1 || parent[0] != -1) return 0;
+    for (int i = 1; i < N; ++i)
+        if (parent[i] < 0 || parent[i] >= i) return 0;
+    return 1;
+}
+
+/* is node j on the root->i path (j == i included)?  Walks parent links up. */
+static int is_ancestor_or_self(const int32_t *parent, int j, int i) {
+    for (int a = i; a != -1; a = parent[a])
+        if (a == j) return 1;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O1: ancestor bitmasks and depths.                                         */
+/* anc is [B, N, W] with W = ceil(N / 64); bit j of anc[b, i] is set iff node */
+/* j is an ancestor of node i or i itself.                                    */
+/* ------------------------------------------------------------------------ */
+int oracle_tree_mask(const int32_t *parent, int B, int N, uint64_t *anc,
+                     int32_t *depth, int32_t *status) {
+    if (B < 0 || N < 0) return -1;
+    const int W = (N + 63) / 64;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parent + (size_t)b * N;
+        const int ok = tree_is_valid(par, N);
+        status[b] = ok ? 0 : ORACLE_BAD_PARENT;
+        for (int i = 0; i < N; ++i) {
+            uint64_t *row = anc + ((size_t)b * N + i) * W;
+            for (int w = 0; w < W; ++w) row[w] = 0;
+            if (!ok) {
+                row[i / 64] |= (uint64_t)1 << (i % 64);
+                if (depth) depth[(size_t)b * N + i] = 0;
+                continue;
+            }
+            int d = -1;
+            for (int a = i; a != -1; a = par[a]) {
+                row[a / 64] |= (uint64_t)1 << (a % 64);
+                ++d;
+            }
+            if (depth) depth[(size_t)b * N + i] = d;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O2: tree attention, fp64.                                                 */
+/*   q   [B, N, Hq, D]    (float32 values; bf16 inputs arrive widened)       */
+/*   k,v [B, Tcap, Hkv, D] logical token order: token t of sequence b is at   */
+/*                         [b, t]; the prefix is t < L_b, node j is L_b + j   */
+/*   rows: nrows triples (b, i, h) to compute, or NULL for every (b, i, h) in */
+/*         that order; out [nrows, D], lse [nrows].                           */
+/* For row (b, i, h) with g = h / (Hq / Hkv) the visible tokens are           */
+/* t < L_b and L_b + j for j an ancestor of i or i itself:                    */
+/*   s_t = scale * <q, k_t>,  o = sum_t softmax(s)_t v_t,  lse = log sum e^s. */
+/* ------------------------------------------------------------------------ */
+int oracle_tree_attn(const float *q, const float *k, const float *v, int Tcap,
+                     const int32_t *seq_lens, const int32_t *parent,
+                     int B, int N, int Hq, int Hkv, int D, double scale,
+                     const int32_t *rows, int nrows, double *out, double *lse) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0) return -1;
+    const int G = Hq / Hkv;
+    const long total = rows ? nrows : (long)B * N * Hq;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long r = 0; r < total; ++r) {
+        int b, i, h;
+        if (rows) {
+            b = rows[3 * r]; i = rows[3 * r + 1]; h = rows[3 * r + 2];
+        } else {
+            b = (int)(r / ((long)N * Hq)); i = (int)((r / Hq) % N); h = (int)(r % Hq);
+        }
+        if (b < 0 || b >= B || i < 0 || i >= N || h < 0 || h >= Hq) { err = 1; continue; }
+        const int g = h / G;
+        const int L = seq_lens[b];
+        const int32_t *par = parent + (size_t)b * N;
+        const int valid = tree_is_valid(par, N);
+        const int T = L + N;
+        if (T > Tcap) { err = 1; continue; }
+        const float *qv = q + (((size_t)b * N + i) * Hq + h) * D;
+        double *s = (double *)malloc(sizeof(double) * T);
+        char *vis = (char *)malloc(T);
+        for (int t = 0; t < T; ++t) {
+            if (t < L) vis[t] = 1;
+            else {
+                int j = t - L;
+                vis[t] = valid ? (char)is_ancestor_or_self(par, j, i) : (char)(j == i);
+            }
+        }
+        double m = -INFINITY;
+        for (int t = 0; t < T; ++t) {
+            if (!vis[t]) continue;
+            const float *kt = k + (((size_t)b * Tcap + t) * Hkv + g) * D;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += (double)qv[d] * (double)kt[d];
+            s[t] = scale * acc;
+            if (s[t] > m) m = s[t];
+        }
+        double Z = 0.0;
+        for (int t = 0; t < T; ++t)
+            if (vis[t]) Z += exp(s[t] - m);
+        double *o = out + (size_t)r * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int t = 0; t < T; ++t) {
+            if (!vis[t]) continue;
+            const double w = exp(s[t] - m) / Z;
+            const float *vt = v + (((size_t)b * Tcap + t) * Hkv + g) * D;
+            for (int d = 0; d < D; ++d) o[d] += w * (double)vt[d];
+        }
+        if (lse) lse[r] = m + log(Z);
+        free(s);
+        free(vis);
+    }
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O3: acceptance walk over the tree, fp64.                                  */
+/* ------------------------------------------------------------------------ */
+
+/* p = softmax(row): m = max, e = exp(l - m), p = e / sum(e). */
+static void softmax64(const float *row, int V, double *p) {
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v)
+        if ((double)row[v] > m) m = (double)row[v];
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) {
+        p[v] = exp((double)row[v] - m);
+        Z += p[v];
+    }
+    for (int v = 0; v < V; ++v) p[v] /= Z;
+}
+
+/*
+ * Inputs:  target, draft [B, N, V] logits (softmax at temperature 1);
+ *          tokens [B, N] (tokens[b][c] is node c's draft token; the root's is
+ *          not tested); parent [B, N]; u_accept [B, N] (u of node c tests c);
+ *          u_bonus [B].
+ * Outputs: accept_len [B]   accepted draft tokens (root excluded);
+ *          path [B, N]      root first, then the accepted nodes, -1 padded;
+ *          out_tokens [B,N] accepted draft tokens then the bonus, -1 padded;
+ *          ratio [B, N]     p~(x)/q(x) for every tested node, NaN otherwise;
+ *          accept_margin [B,N]  |u q(x) - p~(x)| / max(u q(x), p~(x)) for
+ *                           tested nodes, NaN otherwise (how near a tie the
+ *                           decision was);
+ *          bonus_margin [B] distance of u*sum(p~) to the nearer edge of the
+ *                           chosen token's CDF interval, divided by sum(p~);
+ *          n_rejects [B]    rejected children of the node the bonus is drawn
+ *                           at (0: drawn from that node's target softmax);
+ *          status [B]       bit 1 bad parent[], bit 2 token outside [0, V).
+ * Any of ratio / accept_margin / bonus_margin / n_rejects may be NULL.
+ */
+int oracle_spec_accept(const float *target, const float *draft, const int32_t *tokens,
+                       const int32_t *parent, const float *u_accept, const float *u_bonus,
+                       int B, int N, int V, int32_t *accept_len, int32_t *path,
+                       int32_t *out_tokens, double *ratio, double *accept_margin,
+                       double *bonus_margin, int32_t *n_rejects, int32_t *status) {
+    if (B < 0 || N < 0 || V <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parent + (size_t)b * N;
+        const int32_t *tok = tokens + (size_t)b * N;
+        int st = 0;
+        if (!tree_is_valid(par, N)) st |= ORACLE_BAD_PARENT;
+        for (int c = 1; c < N; ++c)
+            if (tok[c] < 0 || tok[c] >= V) st |= ORACLE_BAD_TOKEN;
+        status[b] = st;
+        for (int c = 0; c < N; ++c) {
+            path[(size_t)b * N + c] = -1;
+            out_tokens[(size_t)b * N + c] = -1;
+            if (ratio) ratio[(size_t)b * N + c] = NAN;
+            if (accept_margin) accept_margin[(size_t)b * N + c] = NAN;
+        }
+        accept_len[b] = 0;
+        if (bonus_margin) bonus_margin[b] = NAN;
+        if (n_rejects) n_rejects[b] = 0;
+        if (st != 0 || N == 0) continue;
+
+        double *pt = (double *)malloc(sizeof(double) * V); /* p~ at the current node */
+        double *qd = (double *)malloc(sizeof(double) * V); /* draft softmax at the current node */
+        double *res = (double *)malloc(sizeof(double) * V);
+
+        int cur = 0, len = 0, rejects = 0;
+        path[(size_t)b * N] = 0;
+        softmax64(target + ((size_t)b * N + cur) * V, V, pt);
+        for (;;) {
+            int has_child = 0, moved = 0;
+            rejects = 0;
+            for (int c = cur + 1; c < N && !moved; ++c) {
+                if (par[c] != cur) continue;
+                if (!has_child) {
+                    softmax64(draft + ((size_t)b * N + cur) * V, V, qd);
+                    has_child = 1;
+                }
+                const int x = tok[c];
+                const double u = (double)u_accept[(size_t)b * N + c];
+                const double qx = qd[x], px = pt[x];
+                if (ratio) ratio[(size_t)b * N + c] = px / qx;
+                if (accept_margin) {
+                    double hi = u * qx > px ? u * qx : px;
+                    accept_margin[(size_t)b * N + c] = hi > 0 ? fabs(u * qx - px) / hi : 0.0;
+                }
+                if (u * qx < px) {
+                    /* accepted: move to c; its target softmax is the new p~ */
+                    ++len;
+                    path[(size_t)b * N + len] = c;
+                    out_tokens[(size_t)b * N + len - 1] = x;
+                    cur = c;
+                    softmax64(target + ((size_t)b * N + cur) * V, V, pt);
+                    moved = 1;
+                } else {
+                    /* rejected: p~ <- normalize(max(0, p~ - q)), try the next sibling */
+                    double S = 0.0;
+                    for (int v = 0; v < V; ++v) {
+                        res[v] = pt[v] - qd[v] > 0.0 ? pt[v] - qd[v] : 0.0;
+                        S += res[v];
+                    }
+                    if (S > 0.0)
+                        for (int v = 0; v < V; ++v) pt[v] = res[v] / S;
+                    ++rejects;
+                }
+            }
+            if (!moved) break;
+        }
+        /* bonus: inverse CDF of p~ at u_bonus */
+        double tot = 0.0;
+        for (int v = 0; v < V; ++v) tot += pt[v];
+        const double thr = (double)u_bonus[b] * tot;
+        double cum = 0.0, prev = 0.0;
+        int pick = -1;
+        for (int v = 0; v < V; ++v) {
+            prev = cum;
+            cum += pt[v];
+            if (cum > thr) { pick = v; break; }
+        }
+        double margin;
+        if (pick < 0) {
+            for (int v = V - 1; v >= 0; --v)
+                if (pt[v] > 0.0) { pick = v; break; }
+            margin = 0.0;
+        } else {
+            double a = thr - prev, c2 = cum - thr;
+            margin = (a < c2 ? a : c2) / tot;
+        }
+        out_tokens[(size_t)b * N + len] = pick;
+        accept_len[b] = len;
+        if (bonus_margin) bonus_margin[b] = margin;
+        if (n_rejects) n_rejects[b] = rejects;
+        free(pt);
+        free(qd);
+        free(res);
+    }
+    return 0;
+}
