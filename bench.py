@@ -1,0 +1,451 @@
+"""Benchmark of one verify step: ancestor masks -> tree attention (one layer) ->
+acceptance walk, on synthetic inputs shaped like the workloads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+Prints ONE JSON line on rank 0. ``value`` is verified tree nodes per second
+(per attention layer) over all ranks, with inputs resident in HBM; ``e2e``
+repeats the measurement through the public API from pinned host buffers with
+the copies inside the timed region. Between timed steps the inputs rotate over
+enough copies that the working set exceeds L2. ``--impl reference`` times the
+fp64 CPU oracle on the host cores instead (the reference arm).
+
+Multi-GPU: the path does not shard; each rank runs an independent replica of
+the workload (weak scaling) and the step time is the maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import WORKLOADS, make_inputs  # noqa: E402
+from synth.gen import algorithmic_bytes  # noqa: E402
+
+DEFAULT_WORKLOAD = "binary_tree_8b"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload_by_name(name):
+    for i, w in enumerate(WORKLOADS):
+        if w.name == name:
+            return i, w
+    raise SystemExit(f"unknown workload {name}; choose from {[w.name for w in WORKLOADS]}")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(workload, kernel_src):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    has not changed since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload]
+        if e.get("source_hash") == source_hash(kernel_src):
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def aggregate(local_ms: float, local_units: float, world: int, reduce_max, reduce_sum):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    ms = reduce_max(local_ms)
+    units = reduce_sum(local_units)
+    return ms, units / (ms / 1e3)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm / CPU baseline: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def _oracle_inputs(inp):
+    """Logical float32 K/V, q for the oracle (regenerated from the generator)."""
+    from synth.gen import logical_kv, bf16_bits_to_f32
+    w = inp.w
+    T = inp.seq_lens.astype(np.int64) + w.N
+    Tcap = int(T.max())
+    K = np.zeros((w.B, Tcap, w.Hkv, w.D), np.float32)
+    V = np.zeros_like(K)
+    cvt = (lambda x: bf16_bits_to_f32(x)) if w.dtype == "bf16" else (lambda x: x)
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            k, v = logical_kv(w, inp.seed, b, g, int(T[b]))
+            K[b, : T[b], g] = cvt(k)
+            V[b, : T[b], g] = cvt(v)
+    return cvt(inp.q), K, V
+
+
+def time_oracle(inp, budget_s=15.0, max_steps=20):
+    import oracle
+    w = inp.w
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    q, K, V = _oracle_inputs(inp)
+    rows_all = w.B * w.N * w.Hq
+    # time one row first to size the sample
+    t0 = time.perf_counter()
+    oracle.tree_attn(q, K, V, inp.seq_lens, inp.parent, rows=np.array([[0, 0, 0]]))
+    one = max(time.perf_counter() - t0, 1e-6)
+    frac = 1.0
+    rows = None
+    if one * rows_all / cores > budget_s / 2:
+        nsel = max(cores, int(budget_s / 2 * cores / one))
+        sel = np.linspace(0, rows_all - 1, nsel).astype(np.int64)
+        rows = np.stack([sel // (w.N * w.Hq), (sel // w.Hq) % w.N, sel % w.Hq], 1)
+        frac = nsel / rows_all
+    steps = 0
+    t_attn = t_acc = 0.0
+    start = time.perf_counter()
+    while steps < max_steps and (steps == 0 or time.perf_counter() - start < budget_s):
+        t0 = time.perf_counter()
+        oracle.tree_attn(q, K, V, inp.seq_lens, inp.parent, rows=rows)
+        t1 = time.perf_counter()
+        oracle.tree_mask(inp.parent)
+        oracle.spec_accept(inp.target, inp.draft, inp.tokens, inp.parent, inp.u_accept,
+                           inp.u_bonus)
+        t2 = time.perf_counter()
+        t_attn += (t1 - t0) / frac
+        t_acc += t2 - t1
+        steps += 1
+    per_step = (t_attn + t_acc) / steps
+    sample = (f"{steps} full verify step(s) of {w.name}; attention "
+              + ("all rows" if rows is None else f"{len(rows)} of {rows_all} rows, scaled")
+              + "; fp64 oracle, OpenMP")
+    return per_step, sample, cores
+
+
+def run_reference(args, w, idx):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = make_inputs(w, 1000 + idx)
+    per_step, sample, cores = time_oracle(inp, budget_s=max(5.0, 2.0 * args.steps))
+    value = w.B * w.N / per_step
+    line = {
+        "impl": "reference", "metric": "verified tree-nodes/s per attn layer", "value": value,
+        "unit": "nodes/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "context": w.L, "Hq": w.Hq,
+                   "Hkv": w.Hkv, "head_dim": w.D, "vocab": w.V},
+        "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w, idx):
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from speculative_decoding_tree_03_gb300 import build as _build
+    _build.build()
+    import speculative_decoding_tree_03_gb300 as sv
+
+    seed = 1000 + idx
+    inp = make_inputs(w, seed)
+    nb = algorithmic_bytes(w, inp.seq_lens, inp.parent)
+    dev = torch.device("cuda", local)
+
+    def to_dev(x, bf16=False):
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if bf16 else x).to(dev)
+        return t.view(torch.bfloat16) if bf16 else t
+
+    bf = w.dtype == "bf16"
+    base = {
+        "q": to_dev(inp.q, bf), "k": to_dev(inp.k_cache, bf), "v": to_dev(inp.v_cache, bf),
+        "page_table": to_dev(inp.page_table), "seq_lens": to_dev(inp.seq_lens),
+        "parent": to_dev(inp.parent), "tokens": to_dev(inp.tokens),
+        "target": to_dev(inp.target), "draft": to_dev(inp.draft),
+        "u_accept": to_dev(inp.u_accept), "u_bonus": to_dev(inp.u_bonus),
+    }
+    step_bytes = sum(t.numel() * t.element_size() for t in base.values())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(1, math.ceil(3 * l2 / step_bytes))
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
+
+    B, N, Hq, D = w.B, w.N, w.Hq, w.D
+    stream = torch.cuda.current_stream(dev)
+    anc = torch.empty((B, N, 1), dtype=torch.int64, device=dev)
+    depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    mstat = torch.empty((B,), dtype=torch.int32, device=dev)
+    out = torch.empty_like(base["q"])
+    lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    astat = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws_need = sv.tree_verify_attn_workspace_size(B, N, Hq, w.Hkv, D, base["q"].dtype,
+                                                 inp.page_table.shape[1], inp.page_size)
+    attn_ws = torch.empty((max(ws_need, 1),), dtype=torch.uint8, device=dev)
+    acc_ws = torch.empty((sv.spec_accept_workspace_size(B, N, w.V),), dtype=torch.uint8,
+                         device=dev)
+    acc_out = {}
+
+    def step(s, ev=None):
+        sv.tree_mask_build(s["parent"], anc, depth, mstat)
+        if ev is not None:
+            ev[0].record(stream)
+        sv.tree_verify_attn(s["q"], s["k"], s["v"], s["page_table"], s["seq_lens"], anc,
+                            out=out, lse=lse, workspace=attn_ws, status=astat)
+        if ev is not None:
+            ev[1].record(stream)
+        sv.spec_accept(s["target"], s["draft"], s["tokens"], s["parent"], s["u_accept"],
+                       s["u_bonus"], workspace=acc_ws, outputs=acc_out)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        step(sets[i % nsets])
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(sets[i % nsets], evs[i])
+        t_end.record(stream)
+        barrier()
+    ms_local = t_start.elapsed_time(t_end) / args.steps
+    attn_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    acc_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+
+    def rmax(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def rsum(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    ms, value = aggregate(ms_local, B * N, world, rmax, rsum)
+
+    # ---- end to end through the public API from pinned host buffers
+    host = {k: v.cpu().pin_memory() for k, v in base.items()}
+    dsets = [{k: torch.empty_like(v) for k, v in base.items()} for _ in range(min(nsets, 4))]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    res_h = {k: torch.empty((B, N) if k in ("path", "out_tokens") else (B,),
+                            dtype=torch.int32).pin_memory()
+             for k in ("accept_len", "path", "out_tokens", "status")}
+    d2h = out_h.numel() * out_h.element_size() + sum(t.numel() * 4 for t in res_h.values())
+
+    def e2e_step(i):
+        d = dsets[i % len(dsets)]
+        for k in d:
+            d[k].copy_(host[k], non_blocking=True)
+        step(d)
+        out_h.copy_(out, non_blocking=True)
+        for k in res_h:
+            res_h[k].copy_(acc_out[k], non_blocking=True)
+
+    for i in range(min(args.warmup, 3)):
+        e2e_step(i)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    barrier()
+    e2e_ms = rmax(e0.elapsed_time(e1) / args.steps)
+    e2e_value = rsum(B * N) / (e2e_ms / 1e3)
+
+    # ---- checks that the timed work produced valid results
+    torch.cuda.synchronize(dev)
+    assert int(astat.abs().sum()) == 0 and int(acc_out["status"].abs().sum()) == 0
+    assert bool(torch.isfinite(out.float()).all())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    attn_gbs = nb["attn_bytes"] / (attn_ms / 1e3) / 1e9
+    acc_gbs = nb["accept_bytes"] / (acc_ms / 1e3) / 1e9
+    launches_per_step = 1 + 1 + (1 if ws_need > 0 else 0) + 2
+    line = {
+        "metric": "verified tree-nodes/s per attn layer",
+        "value": value,
+        "unit": "nodes/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if bf else "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "B": B, "N": N, "context": w.L if w.L_hi is None else
+            f"U[{w.L},{w.L_hi}]", "Hq": Hq, "Hkv": w.Hkv, "head_dim": D, "vocab": w.V,
+            "page_size": inp.page_size, "tree": w.tree,
+            "l2": f"inputs rotate over {nsets} copies ({nsets * step_bytes / 1e6:.0f} MB > "
+                  f"L2 {l2 / 1e6:.0f} MB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "accept_steps_per_s": rsum(B) / (ms / 1e3),
+        "kernels": {
+            "tree_verify_attn": {"ms": attn_ms, "bytes": nb["attn_bytes"], "gbs": attn_gbs,
+                                 "frac_of_hbm": attn_gbs / peak},
+            "spec_accept": {"ms": acc_ms, "bytes": nb["accept_bytes"], "gbs": acc_gbs,
+                            "frac_of_hbm": acc_gbs / peak},
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "tree_verify_attn",
+            "achieved": attn_gbs,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+            "unit": "GB/s",
+            "frac": attn_gbs / peak,
+            "traffic": committed_traffic(w.name, "speculative_decoding_tree_03_gb300/csrc/attn_tc.cu"),
+        },
+        "e2e": {"value": e2e_value, "unit": "nodes/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        per_step, sample, cores = time_oracle(inp)
+        line["cpu_baseline"] = {"value": B * N / per_step, "unit": "nodes/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    idx, w = workload_by_name(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w, idx)
+    else:
+        run_ours(args, w, idx)
+
+
+if __name__ == "__main__":
+    main()

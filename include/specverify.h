@@ -1,0 +1,190 @@
+/*
+ * specverify.h -- C ABI of the GB300 (sm_103a) one-pass tree-verification library.
+ *
+ * The library implements the target model's verification step of EAGLE-style
+ * speculative decoding, as stated on these pages:
+ *   - "EAGLE 演化史 (1 → 2 → 3) 与 DFlash 的回答", § Tree Verification 详解:
+ *       A  one target forward pass verifies a whole draft tree;
+ *       B  the tree is flattened in BFS order and given an attention mask in
+ *          which a node sees the cached prefix, its ancestors and itself;
+ *       C  the walk from the root: children in order, the rejection test,
+ *          the residual after each rejected sibling, sampling from the
+ *          residual when every child is rejected, the longest accepted path;
+ *       G  the worked 7-node example.
+ *   - "Eagle vs DFlash", § Target-model decoding is serial: accept x_i with
+ *       probability min(1, p_i(x_i)/q_i(x_i)); on rejection sample from the
+ *       normalised residual max(0, p_i - q_i); the bonus token.
+ *   - "EAGLE-4 Technical Deepdive", § EAGLE-4 verification trees and harness:
+ *       each token attends to the shared prefix, its ancestors and itself.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller; the
+ *     library allocates no memory and keeps no pointer after a call returns.
+ *   - Every call is asynchronous on the caller's CUDA stream (NULL = the
+ *     legacy default stream). Nothing synchronises with the host.
+ *   - Arrays are dense and row-major in the order their shapes are written.
+ *   - The tree of sequence b is given by parent[b][0..N): node 0 is the root
+ *     (parent -1) and 0 <= parent[i] < i for i >= 1 (BFS order). N counts the
+ *     root. Node i's K/V sits at logical token position seq_lens[b] + i.
+ *   - The host return code reports argument and launch errors only
+ *     (svf_status). Data errors found on the device (a bad parent[], a token
+ *     outside the vocabulary, a page id outside the cache) set bits in the
+ *     caller's int32 status[B] array (SVF_DEV_*); that sequence's outputs are
+ *     then written as defined "no result" values and the other sequences are
+ *     unaffected. Each call overwrites status[0..B).
+ *   - B == 0 is a valid empty call: nothing is launched and SVF_OK returned.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st *svf_stream_t;
+
+/* Element types of q, K, V and the attention output. */
+enum svf_dtype { SVF_F32 = 0, SVF_BF16 = 1 };
+
+/* Host return codes. */
+enum svf_status {
+    SVF_OK = 0,
+    SVF_ERR_ARG = -1,         /* null pointer, negative size, bad alignment */
+    SVF_ERR_UNSUPPORTED = -2, /* sizes outside the limits stated per call */
+    SVF_ERR_LAUNCH = -3,      /* a CUDA launch or driver call failed */
+    SVF_ERR_WORKSPACE = -4    /* workspace missing or smaller than required */
+};
+
+/* Device-side status bits, OR-ed into status[b]. */
+enum svf_device_status {
+    SVF_DEV_BAD_PARENT = 1, /* parent[b] is not a BFS-flattened tree */
+    SVF_DEV_BAD_TOKEN = 2,  /* a draft token (node >= 1) outside [0, V) */
+    SVF_DEV_BAD_PAGE = 4,   /* a needed page id outside [0, num_pages) */
+    SVF_DEV_BAD_LENGTH = 8, /* seq_lens[b] < 0 or the sequence overflows its page table */
+    SVF_DEV_TIMEOUT = 16    /* an internal wait gave up (the outputs of b are undefined) */
+};
+
+/* ------------------------------------------------------------------------
+ * svf_tree_mask_build -- ancestor bitmasks of BFS-flattened draft trees.
+ *
+ * Follows "EAGLE 演化史", § Tree Verification 详解, B: each node may attend
+ * only to its ancestors and itself. With W = ceil(N / 64):
+ *   anc[b][i][w] bit k  set  <=>  node 64*w + k is node i or an ancestor of i
+ *   depth[b][i]              =  number of edges from the root to node i
+ *
+ *   parent  [B, N] int32     in
+ *   anc     [B, N, W] uint64 out
+ *   depth   [B, N] int32     out, may be NULL
+ *   status  [B] int32        out; SVF_DEV_BAD_PARENT if parent[b][0] != -1 or
+ *                            some parent[b][i] is outside [0, i). Then every
+ *                            node of b gets only its own bit and depth 0.
+ * Limits: 1 <= N <= 1024.
+ * ---------------------------------------------------------------------- */
+int svf_tree_mask_build(const int32_t *parent, int B, int N, uint64_t *anc, int32_t *depth,
+                        int32_t *status, svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * svf_tree_verify_attn -- attention of a flattened draft tree against a
+ * cached KV prefix, one target layer, grouped-query heads.
+ *
+ * Follows "EAGLE 演化史", § Tree Verification 详解, A-B (one forward pass
+ * over prefix + tree; ancestor-only mask; the output of node i equals running
+ * prompt + root->i path as an ordinary causal sequence) and "EAGLE-4
+ * Technical Deepdive" (prefix, ancestors and self are visible). For sequence
+ * b, query head h, node i, with G = Hq / Hkv and KV head g = h / G, the
+ * visible tokens are t < L_b = seq_lens[b] and t = L_b + j for every j whose
+ * bit is set in anc[b][i]:
+ *   s_t = sm_scale * <q[b][i][h], K_b,g(t)>
+ *   out[b][i][h] = sum_t softmax(s)_t V_b,g(t),   lse[b][i][h] = log sum_t e^{s_t}
+ *
+ *   q          [B, N, Hq, D]                      dtype (post-RoPE)
+ *   k_cache,   [num_pages, page_size, Hkv, D]     dtype; token t of sequence
+ *   v_cache                                        b lives in page
+ *                                                  page_table[b][t / page_size],
+ *                                                  slot t % page_size. The
+ *                                                  tree's K/V must already be
+ *                                                  written at t = L_b .. L_b+N-1.
+ *   page_table [B, max_pages] int32               entries past the sequence's
+ *                                                  last page are not read
+ *   seq_lens   [B] int32                          L_b, the prefix length
+ *   anc        [B, N, 1] uint64                   from svf_tree_mask_build
+ *   sm_scale   <= 0 selects 1/sqrt(D)
+ *   out        [B, N, Hq, D] dtype                out
+ *   lse        [B, N, Hq] float32                 out, may be NULL (natural log)
+ *   workspace  device scratch of at least
+ *              svf_tree_verify_attn_workspace_size(...) bytes (NULL if that is 0)
+ *   status     [B] int32                          out; SVF_DEV_BAD_LENGTH,
+ *                                                  SVF_DEV_BAD_PAGE. A bad
+ *                                                  sequence's out and lse are 0.
+ * A contiguous cache is page_size = capacity, num_pages = B, page_table[b][0] = b.
+ * Limits: N <= 64; D in {64, 128} for SVF_F32, D == 128 for SVF_BF16;
+ * Hq % Hkv == 0; for SVF_BF16 page_size in {16, 32, 64} or a multiple of 128,
+ * q / k_cache / v_cache 16-byte aligned. Bytes past a sequence's last token
+ * inside its last page may hold anything.
+ * ---------------------------------------------------------------------- */
+size_t svf_tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int dtype,
+                                           int max_pages, int page_size);
+int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache, int num_pages,
+                         int page_size, const int32_t *page_table, int max_pages,
+                         const int32_t *seq_lens, const uint64_t *anc, int B, int N, int Hq,
+                         int Hkv, int D, int dtype, float sm_scale, void *out, float *lse,
+                         void *workspace, size_t workspace_bytes, int32_t *status,
+                         svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * svf_spec_accept -- lossless acceptance walk over the verified tree.
+ *
+ * Follows "Eagle vs DFlash" (accept x with probability min(1, p(x)/q(x));
+ * on rejection, sample from normalize(max(0, p - q))) and "EAGLE 演化史",
+ * § Tree Verification 详解, C and G (walk from the root; try children in
+ * order, after each rejected child replace the target side by the residual
+ * and test the next sibling; when all are rejected sample there; the bonus
+ * token is drawn at the last accepted node). With p_j = softmax(target[b][j])
+ * and q_j = softmax(draft[b][j]) (temperature 1):
+ *   - start at the root with p~ = p_0;
+ *   - for each child c of the current node j in ascending index order, with
+ *     x = tokens[b][c]: accept iff u_accept[b][c] * q_j(x) < p~(x). On accept
+ *     move to c with p~ = p_c. On reject set p~ = normalize(max(0, p~ - q_j))
+ *     (left unchanged if that has no mass) and try the next sibling;
+ *   - when the current node has no child left, the bonus token is the
+ *     smallest k with sum_{v<=k} p~(v) > u_bonus[b] * sum_v p~(v).
+ *
+ *   target_logits, draft_logits [B, N, V] float32   rows of leaves in draft
+ *                                                    are not read
+ *   tokens     [B, N] int32   node i's draft token (the root's is not read)
+ *   parent     [B, N] int32
+ *   u_accept   [B, N] float32 in [0, 1)   u_accept[b][c] tests node c
+ *   u_bonus    [B] float32 in [0, 1)
+ *   accept_len [B] int32      out: accepted draft tokens (root excluded)
+ *   path       [B, N] int32   out: 0, then the accepted nodes, then -1
+ *   out_tokens [B, N] int32   out: accepted draft tokens, the bonus, then -1
+ *   ratio      [B, N] float32 out, may be NULL: p~(x)/q_j(x) for every tested
+ *                             node, NaN for nodes never tested
+ *   workspace  at least svf_spec_accept_workspace_size(B, N, V) bytes
+ *   status     [B] int32      out: SVF_DEV_BAD_PARENT, SVF_DEV_BAD_TOKEN; a
+ *                             bad sequence gets accept_len 0 and -1 in path
+ *                             and out_tokens (ratio NaN).
+ * Limits: 1 <= N <= 1024, 1 <= V <= 786432.
+ * ---------------------------------------------------------------------- */
+size_t svf_spec_accept_workspace_size(int B, int N, int V);
+int svf_spec_accept(const float *target_logits, const float *draft_logits, const int32_t *tokens,
+                    const int32_t *parent, const float *u_accept, const float *u_bonus, int B,
+                    int N, int V, int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                    float *ratio, void *workspace, size_t workspace_bytes, int32_t *status,
+                    svf_stream_t stream);
+
+/* Human-readable name of a host return code or of one device status bit. */
+const char *svf_status_string(int code);
+
+/* Library version, 100 * major + minor. */
+int svf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

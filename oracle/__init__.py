@@ -54,7 +54,7 @@ def _load():
             lib.oracle_tree_attn.argtypes = [P, P, P, I, P, P, I, I, I, I, I, ctypes.c_double,
                                              P, I, P, P]
             lib.oracle_tree_attn.restype = I
-            lib.oracle_spec_accept.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P, P, P]
+            lib.oracle_spec_accept.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P, P, P, P, P]
             lib.oracle_spec_accept.restype = I
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = I
@@ -116,7 +116,10 @@ def tree_attn(q, k, v, seq_lens, parent, scale=None, rows=None):
     return out, lse
 
 
-def spec_accept(target, draft, tokens, parent, u_accept, u_bonus):
+def spec_accept(target, draft, tokens, parent, u_accept, u_bonus, probe_token=None):
+    """Acceptance walk in fp64. ``probe_token`` [B] (optional, -1 = none) asks for
+    the normalised CDF of the final distribution just before and through that
+    token (``probe_cdf`` [B, 3]: before, through, u_bonus)."""
     target = np.ascontiguousarray(target, dtype=np.float32)
     draft = np.ascontiguousarray(draft, dtype=np.float32)
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
@@ -135,10 +138,15 @@ def spec_accept(target, draft, tokens, parent, u_accept, u_bonus):
         "bonus_margin": np.zeros((B,), np.float64),
         "n_rejects": np.zeros((B,), np.int32),
         "status": np.zeros((B,), np.int32),
+        "probe_cdf": np.full((B, 3), np.nan, np.float64),
     }
+    if probe_token is not None:
+        probe_token = np.ascontiguousarray(probe_token, dtype=np.int32)
+        assert probe_token.shape == (B,)
     rc = _load().oracle_spec_accept(
         _p(target), _p(draft), _p(tokens), _p(parent), _p(u_accept), _p(u_bonus), B, N, V,
         _p(out["accept_len"]), _p(out["path"]), _p(out["out_tokens"]), _p(out["ratio"]),
-        _p(out["accept_margin"]), _p(out["bonus_margin"]), _p(out["n_rejects"]), _p(out["status"]))
+        _p(out["accept_margin"]), _p(out["bonus_margin"]), _p(out["n_rejects"]), _p(out["status"]),
+        _p(probe_token), _p(out["probe_cdf"]) if probe_token is not None else None)
     assert rc == 0
     return out

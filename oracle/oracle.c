@@ -216,13 +216,19 @@ static void softmax64(const float *row, int V, double *p) {
  *          n_rejects [B]    rejected children of the node the bonus is drawn
  *                           at (0: drawn from that node's target softmax);
  *          status [B]       bit 1 bad parent[], bit 2 token outside [0, V).
- * Any of ratio / accept_margin / bonus_margin / n_rejects may be NULL.
+ *          probe_cdf [B,3]  if probe_token is given: for k = probe_token[b]
+ *                           (skipped when -1), the normalised cumulative
+ *                           p~ before k and through k, and u_bonus[b] -- so a
+ *                           caller can check that a token k picked elsewhere
+ *                           lies on the inverse-CDF crossing.
+ * Any of ratio / accept_margin / bonus_margin / n_rejects / probe_* may be NULL.
  */
 int oracle_spec_accept(const float *target, const float *draft, const int32_t *tokens,
                        const int32_t *parent, const float *u_accept, const float *u_bonus,
                        int B, int N, int V, int32_t *accept_len, int32_t *path,
                        int32_t *out_tokens, double *ratio, double *accept_margin,
-                       double *bonus_margin, int32_t *n_rejects, int32_t *status) {
+                       double *bonus_margin, int32_t *n_rejects, int32_t *status,
+                       const int32_t *probe_token, double *probe_cdf) {
     if (B < 0 || N < 0 || V <= 0) return -1;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int b = 0; b < B; ++b) {
@@ -309,6 +315,13 @@ int oracle_spec_accept(const float *target, const float *draft, const int32_t *t
         } else {
             double a = thr - prev, c2 = cum - thr;
             margin = (a < c2 ? a : c2) / tot;
+        }
+        if (probe_token && probe_cdf && probe_token[b] >= 0 && probe_token[b] < V) {
+            double before = 0.0;
+            for (int v = 0; v < probe_token[b]; ++v) before += pt[v];
+            probe_cdf[3 * (size_t)b] = before / tot;
+            probe_cdf[3 * (size_t)b + 1] = (before + pt[probe_token[b]]) / tot;
+            probe_cdf[3 * (size_t)b + 2] = (double)u_bonus[b];
         }
         out_tokens[(size_t)b * N + len] = pick;
         accept_len[b] = len;

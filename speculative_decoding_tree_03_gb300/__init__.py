@@ -1,0 +1,282 @@
+"""GB300-native one-pass tree verification for EAGLE-style speculative decoding.
+
+A thin ctypes binding over ``libspecverify.so``, whose C ABI is declared in
+``include/specverify.h``. The functions here only check tensor shapes, dtypes,
+devices and contiguity and pass raw device pointers and the current CUDA
+stream; every step of the computation runs in the library's CUDA kernels.
+There is no CPU path: calling with a tensor that is not on a CUDA device, or
+without the built library, raises.
+
+    anc, depth, status = tree_mask_build(parent)
+    out, lse, status   = tree_verify_attn(q, k_cache, v_cache, page_table, seq_lens, anc)
+    res                = spec_accept(target_logits, draft_logits, tokens, parent,
+                                     u_accept, u_bonus)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libspecverify.so")
+
+SVF_F32, SVF_BF16 = 0, 1
+SVF_OK, SVF_ERR_ARG, SVF_ERR_UNSUPPORTED, SVF_ERR_LAUNCH, SVF_ERR_WORKSPACE = 0, -1, -2, -3, -4
+SVF_DEV_BAD_PARENT, SVF_DEV_BAD_TOKEN, SVF_DEV_BAD_PAGE, SVF_DEV_BAD_LENGTH, SVF_DEV_TIMEOUT = (
+    1, 2, 4, 8, 16)
+
+EXPORTED = [
+    "svf_tree_mask_build",
+    "svf_tree_verify_attn_workspace_size",
+    "svf_tree_verify_attn",
+    "svf_spec_accept_workspace_size",
+    "svf_spec_accept",
+    "svf_status_string",
+    "svf_version",
+]
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libspecverify.so and declare its signatures (no GPU needed)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise SpecVerifyError(
+            f"{path} is missing: build it with speculative_decoding_tree_03_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.svf_tree_mask_build.argtypes = [P, I, I, P, P, P, P]
+    lib.svf_tree_mask_build.restype = I
+    lib.svf_tree_verify_attn_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+    lib.svf_tree_verify_attn_workspace_size.restype = Z
+    lib.svf_tree_verify_attn.argtypes = [P, P, P, I, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P,
+                                         Z, P, P]
+    lib.svf_tree_verify_attn.restype = I
+    lib.svf_spec_accept_workspace_size.argtypes = [I, I, I]
+    lib.svf_spec_accept_workspace_size.restype = Z
+    lib.svf_spec_accept.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, Z, P, P]
+    lib.svf_spec_accept.restype = I
+    lib.svf_status_string.argtypes = [I]
+    lib.svf_status_string.restype = ctypes.c_char_p
+    lib.svf_version.argtypes = []
+    lib.svf_version.restype = I
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().svf_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != SVF_OK:
+        raise SpecVerifyError(f"{what}: {status_string(rc)} ({rc})")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise SpecVerifyError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise SpecVerifyError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise SpecVerifyError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise SpecVerifyError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return SVF_F32
+    if dt == torch.bfloat16:
+        return SVF_BF16
+    raise SpecVerifyError(f"unsupported dtype {dt}")
+
+
+# ---------------------------------------------------------------------------
+# tree_mask_build
+# ---------------------------------------------------------------------------
+
+def tree_mask_build(parent: torch.Tensor, anc: Optional[torch.Tensor] = None,
+                    depth: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                    stream=None):
+    """Ancestor bitmasks of BFS-flattened trees: parent [B, N] int32 ->
+    (anc [B, N, ceil(N/64)] int64 bit patterns, depth [B, N] int32, status [B] int32)."""
+    lib = load_library()
+    _dev(parent, "parent", torch.int32)
+    B, N = parent.shape
+    W = max(1, (N + 63) // 64)
+    dev = parent.device
+    if anc is None:
+        anc = torch.empty((B, N, W), dtype=torch.int64, device=dev)
+    if depth is None:
+        depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev(anc, "anc", torch.int64, (B, N, W))
+    _dev(depth, "depth", torch.int32, (B, N))
+    _dev(status, "status", torch.int32, (B,))
+    rc = lib.svf_tree_mask_build(_ptr(parent), B, N, _ptr(anc), _ptr(depth), _ptr(status),
+                                 _stream(stream))
+    _check(rc, "svf_tree_mask_build")
+    return anc, depth, status
+
+
+# ---------------------------------------------------------------------------
+# tree_verify_attn
+# ---------------------------------------------------------------------------
+
+def tree_verify_attn_workspace_size(B, N, Hq, Hkv, D, dtype, max_pages, page_size) -> int:
+    return int(load_library().svf_tree_verify_attn_workspace_size(
+        B, N, Hq, Hkv, D, _dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype),
+        max_pages, page_size))
+
+
+def tree_verify_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     page_table: torch.Tensor, seq_lens: torch.Tensor, anc: torch.Tensor,
+                     sm_scale: float = 0.0, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None, want_lse: bool = True, stream=None):
+    """Tree attention against a paged KV cache.
+
+    q [B, N, Hq, D]; k_cache, v_cache [num_pages, page_size, Hkv, D] (same dtype,
+    float32 or bfloat16); page_table [B, max_pages] int32; seq_lens [B] int32
+    (prefix length, tree excluded); anc [B, N, 1] int64 from tree_mask_build.
+    Returns (out [B, N, Hq, D], lse [B, N, Hq] float32 or None, status [B] int32).
+    """
+    lib = load_library()
+    _dev(q, "q")
+    B, N, Hq, D = q.shape
+    dt = q.dtype
+    _dev(k_cache, "k_cache", dt)
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D:
+        raise SpecVerifyError("k_cache head_dim differs from q")
+    _dev(v_cache, "v_cache", dt, k_cache.shape)
+    _dev(page_table, "page_table", torch.int32)
+    if page_table.dim() != 2 or page_table.shape[0] != B:
+        raise SpecVerifyError("page_table must be [B, max_pages]")
+    max_pages = page_table.shape[1]
+    _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    _dev(anc, "anc", torch.int64)
+    if anc.shape[0] != B or anc.shape[1] != N:
+        raise SpecVerifyError("anc must be [B, N, W]")
+    dev = q.device
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", dt, q.shape)
+    if lse is None and want_lse:
+        lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _dev(lse, "lse", torch.float32, (B, N, Hq))
+    if status is None:
+        status = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev(status, "status", torch.int32, (B,))
+    code = _dtype_code(dt)
+    need = int(lib.svf_tree_verify_attn_workspace_size(B, N, Hq, Hkv, D, code, max_pages,
+                                                       page_size))
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.svf_tree_verify_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages, page_size, _ptr(page_table), max_pages,
+        _ptr(seq_lens), _ptr(anc), B, N, Hq, Hkv, D, code, float(sm_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
+    _check(rc, "svf_tree_verify_attn")
+    return out, lse, status
+
+
+# ---------------------------------------------------------------------------
+# spec_accept
+# ---------------------------------------------------------------------------
+
+def spec_accept_workspace_size(B, N, V) -> int:
+    return int(load_library().svf_spec_accept_workspace_size(B, N, V))
+
+
+def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor, tokens: torch.Tensor,
+                parent: torch.Tensor, u_accept: torch.Tensor, u_bonus: torch.Tensor,
+                want_ratio: bool = True, workspace: Optional[torch.Tensor] = None,
+                outputs: Optional[dict] = None, stream=None) -> dict:
+    """Acceptance walk. Returns a dict of device tensors: accept_len [B], path [B, N],
+    out_tokens [B, N], ratio [B, N] (or None), status [B]."""
+    lib = load_library()
+    _dev(target_logits, "target_logits", torch.float32)
+    B, N, V = target_logits.shape
+    _dev(draft_logits, "draft_logits", torch.float32, (B, N, V))
+    _dev(tokens, "tokens", torch.int32, (B, N))
+    _dev(parent, "parent", torch.int32, (B, N))
+    _dev(u_accept, "u_accept", torch.float32, (B, N))
+    _dev(u_bonus, "u_bonus", torch.float32, (B,))
+    dev = target_logits.device
+    o = outputs if outputs is not None else {}
+    if "accept_len" not in o:
+        o["accept_len"] = torch.empty((B,), dtype=torch.int32, device=dev)
+        o["path"] = torch.empty((B, N), dtype=torch.int32, device=dev)
+        o["out_tokens"] = torch.empty((B, N), dtype=torch.int32, device=dev)
+        o["ratio"] = torch.empty((B, N), dtype=torch.float32, device=dev) if want_ratio else None
+        o["status"] = torch.empty((B,), dtype=torch.int32, device=dev)
+    need = int(lib.svf_spec_accept_workspace_size(B, N, V))
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib.svf_spec_accept(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parent), _ptr(u_accept),
+        _ptr(u_bonus), B, N, V, _ptr(o["accept_len"]), _ptr(o["path"]), _ptr(o["out_tokens"]),
+        _ptr(o.get("ratio")), _ptr(workspace), ws_bytes, _ptr(o["status"]), _stream(stream))
+    _check(rc, "svf_spec_accept")
+    return o
+
+
+# ---------------------------------------------------------------------------
+# One verify step: mask -> attention -> acceptance
+# ---------------------------------------------------------------------------
+
+def verify_step(parent, tokens, q, k_cache, v_cache, page_table, seq_lens, target_logits,
+                draft_logits, u_accept, u_bonus, stream=None, buffers: Optional[dict] = None):
+    """The whole hot path on device tensors: ancestor masks, tree attention of
+    one layer, acceptance walk. ``buffers`` (optional) holds preallocated
+    outputs and workspaces and is filled on the first call."""
+    bufs = buffers if buffers is not None else {}
+    anc, depth, mstatus = tree_mask_build(parent, bufs.get("anc"), bufs.get("depth"),
+                                          bufs.get("mask_status"), stream)
+    bufs["anc"], bufs["depth"], bufs["mask_status"] = anc, depth, mstatus
+    out, lse, astatus = tree_verify_attn(q, k_cache, v_cache, page_table, seq_lens, anc,
+                                         out=bufs.get("attn_out"), lse=bufs.get("lse"),
+                                         workspace=bufs.get("attn_ws"),
+                                         status=bufs.get("attn_status"), stream=stream)
+    bufs["attn_out"], bufs["lse"], bufs["attn_status"] = out, lse, astatus
+    if "attn_ws" not in bufs:
+        B, N, Hq, D = q.shape
+        need = tree_verify_attn_workspace_size(B, N, Hq, k_cache.shape[2], D, q.dtype,
+                                               page_table.shape[1], k_cache.shape[1])
+        bufs["attn_ws"] = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+    if "acc_ws" not in bufs:
+        B, N, V = target_logits.shape
+        bufs["acc_ws"] = torch.empty((spec_accept_workspace_size(B, N, V),), dtype=torch.uint8,
+                                     device=q.device)
+    res = spec_accept(target_logits, draft_logits, tokens, parent, u_accept, u_bonus,
+                      workspace=bufs["acc_ws"], outputs=bufs.get("accept"), stream=stream)
+    bufs["accept"] = res
+    return out, lse, res, bufs

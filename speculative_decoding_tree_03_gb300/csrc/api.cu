@@ -1,0 +1,140 @@
+// api.cu -- extern "C" entry points declared in include/specverify.h.
+//
+// Host-side argument checks, the per-call status reset, and the choice of
+// kernel: fp32 inputs take the CUDA-core attention kernel, bf16 inputs the
+// tensor-core kernel. All work is enqueued on the caller's stream.
+#include <limits.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace svf {
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    static int cached[64] = {0};
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool tc_page_size_ok(int ps) {
+    return ps == 16 || ps == 32 || ps == 64 || (ps > 0 && ps % 128 == 0);
+}
+
+}  // namespace svf
+
+using namespace svf;
+
+extern "C" {
+
+int svf_version(void) { return 100; }
+
+const char *svf_status_string(int code) {
+    switch (code) {
+        case SVF_OK: return "ok";
+        case SVF_ERR_ARG: return "invalid argument";
+        case SVF_ERR_UNSUPPORTED: return "unsupported size or dtype";
+        case SVF_ERR_LAUNCH: return "CUDA launch or driver call failed";
+        case SVF_ERR_WORKSPACE: return "workspace missing or too small";
+        case SVF_DEV_BAD_PARENT: return "device: parent[] is not a BFS-flattened tree";
+        case SVF_DEV_BAD_TOKEN: return "device: draft token outside the vocabulary";
+        case SVF_DEV_BAD_PAGE: return "device: page id outside the cache";
+        case SVF_DEV_BAD_LENGTH: return "device: sequence length outside its page table";
+        case SVF_DEV_TIMEOUT: return "device: an internal wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int svf_tree_mask_build(const int32_t *parent, int B, int N, uint64_t *anc, int32_t *depth,
+                        int32_t *status, svf_stream_t stream) {
+    if (B < 0 || N < 0) return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (N < 1 || N > 1024) return SVF_ERR_UNSUPPORTED;
+    if (!parent || !anc || !status) return SVF_ERR_ARG;
+    cudaError_t e = launch_tree_mask(parent, B, N, anc, depth, status,
+                                     reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+size_t svf_tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int dtype,
+                                           int max_pages, int page_size) {
+    if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_pages <= 0 ||
+        page_size <= 0)
+        return 0;
+    if (dtype != SVF_BF16 || D != 128) return 0;
+    return attn_tc_workspace_bytes(B, N, Hq, Hkv, max_pages, page_size);
+}
+
+int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache, int num_pages,
+                         int page_size, const int32_t *page_table, int max_pages,
+                         const int32_t *seq_lens, const uint64_t *anc, int B, int N, int Hq,
+                         int Hkv, int D, int dtype, float sm_scale, void *out, float *lse,
+                         void *workspace, size_t workspace_bytes, int32_t *status,
+                         svf_stream_t stream) {
+    if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 ||
+        max_pages <= 0)
+        return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !anc || !out || !status)
+        return SVF_ERR_ARG;
+    if (N < 1 || N > 64 || Hq % Hkv != 0) return SVF_ERR_UNSUPPORTED;
+    if ((long long)num_pages * page_size > INT_MAX) return SVF_ERR_UNSUPPORTED;
+    if ((long long)max_pages * page_size > INT_MAX) return SVF_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    AttnArgs a;
+    a.q = q; a.k_cache = k_cache; a.v_cache = v_cache;
+    a.num_pages = num_pages; a.page_size = page_size;
+    a.page_table = page_table; a.max_pages = max_pages;
+    a.seq_lens = seq_lens; a.anc = anc;
+    a.B = B; a.N = N; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.dtype = dtype;
+    a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.status = status;
+    if (dtype == SVF_F32) {
+        if (D != 64 && D != 128) return SVF_ERR_UNSUPPORTED;
+        if (cudaMemsetAsync(status, 0, sizeof(int32_t) * (size_t)B, s) != cudaSuccess)
+            return SVF_ERR_LAUNCH;
+        return launch_attn_simt(a, s) == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+    }
+    if (dtype != SVF_BF16) return SVF_ERR_UNSUPPORTED;
+    if (D != 128 || !tc_page_size_ok(page_size)) return SVF_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return SVF_ERR_ARG;
+    if (cudaMemsetAsync(status, 0, sizeof(int32_t) * (size_t)B, s) != cudaSuccess)
+        return SVF_ERR_LAUNCH;
+    return launch_attn_tc(a, workspace, workspace_bytes, s);
+}
+
+size_t svf_spec_accept_workspace_size(int B, int N, int V) {
+    if (B <= 0 || N <= 0 || V <= 0) return 0;
+    return accept_workspace_bytes(B, N, V);
+}
+
+int svf_spec_accept(const float *target_logits, const float *draft_logits, const int32_t *tokens,
+                    const int32_t *parent, const float *u_accept, const float *u_bonus, int B,
+                    int N, int V, int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                    float *ratio, void *workspace, size_t workspace_bytes, int32_t *status,
+                    svf_stream_t stream) {
+    if (B < 0 || N < 0 || V < 0) return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (!target_logits || !draft_logits || !tokens || !parent || !u_accept || !u_bonus ||
+        !accept_len || !path || !out_tokens || !status)
+        return SVF_ERR_ARG;
+    if (N < 1 || N > 1024 || V < 1 || V > 786432) return SVF_ERR_UNSUPPORTED;
+    if ((V & 3) == 0 && (!aligned16(target_logits) || !aligned16(draft_logits)))
+        return SVF_ERR_ARG;
+    const size_t need = accept_workspace_bytes(B, N, V);
+    if (!workspace || workspace_bytes < need) return SVF_ERR_WORKSPACE;
+    cudaError_t e = launch_accept(target_logits, draft_logits, tokens, parent, u_accept, u_bonus,
+                                  B, N, V, accept_len, path, out_tokens, ratio, workspace, status,
+                                  reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+}  // extern "C"

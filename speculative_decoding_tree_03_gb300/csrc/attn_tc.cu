@@ -1,0 +1,632 @@
+// attn_tc.cu -- tree attention on the 5th-generation tensor cores (bf16, head_dim 128).
+//
+// "EAGLE 演化史 (1 → 2 → 3) 与 DFlash 的回答", § Tree Verification 详解, A-B:
+// one target pass verifies the whole tree; node i sees the cached prefix and
+// tree positions L_b + j for j an ancestor of i (or i). The pages size the
+// cost as O(N·P) reads of the prefix plus a sparse O(N·avg_depth) tree part
+// (D.2), so the kernel is a KV-streaming decode kernel: every query row of one
+// (sequence, KV head) -- N nodes x G grouped heads -- shares each K/V tile.
+//
+// One CTA = (KV split, KV head [x row block], sequence). Roles:
+//   warp 0      TMA producer: K and V tiles of 128 tokens, page by page
+//               (128-byte swizzle), into a 2-stage ring.
+//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma:
+//                 S_h  = Q_h K^T  (A, B from shared memory, M=128, N=128)
+//                 O_h += P_h V    (A = P from tensor memory, B = V MN-major)
+//   warps 2..   softmax: one thread per query row (= TMEM lane). Reads S
+//               from TMEM, applies the ancestor mask on the tile(s) that
+//               reach the tree, keeps a lazily-updated running max (O is
+//               rescaled only when the max grows by more than 2^8), writes
+//               P as bf16 into the S columns, and finally reads O.
+// With more than 128 rows (N*G > 128) the rows form two halves with their own
+// S/O accumulators; the halves interleave on the tensor pipe.
+//
+// Splits of the KV range write normalised partial outputs and their
+// log-sum-exp to the workspace; attn_combine_kernel merges them.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace svf {
+
+namespace tc {
+constexpr int BN = 128;                  // KV tokens per tile
+constexpr int HD = 128;                  // head_dim
+constexpr int STAGES = 2;
+constexpr int HALF_BYTES = 128 * HD * 2;  // 32 KB: 128 rows x 128 bf16
+constexpr int ATOM_COL_BYTES = 128 * 128;  // one 64-element column block of a 128-row tile
+constexpr int TILE_BYTES = BN * HD * 2;   // 32 KB per K or V tile
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+}  // namespace tc
+
+struct TcParams {
+    const __nv_bfloat16 *q;
+    const int32_t *page_table;
+    const int32_t *seq_lens;
+    const uint64_t *anc;
+    int B, N, Hq, Hkv, G, M;
+    int num_pages, page_size, max_pages;
+    int splits, row_blocks;
+    float scale_log2;
+    __nv_bfloat16 *out;
+    float *lse;
+    float *part_o;    // [splits, B, N, Hq, HD]
+    float *part_lse;  // [splits, B, N, Hq]
+    int32_t *status;
+};
+
+template <int NH>
+struct TcSmem {
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + NH * tc::HALF_BYTES;
+    static constexpr int kV = kK + tc::STAGES * tc::TILE_BYTES;
+    static constexpr int kBar = kV + tc::STAGES * tc::TILE_BYTES;
+    static constexpr int kNumBars = 3 * tc::STAGES + 3 * NH;
+    static constexpr int kMisc = kBar + kNumBars * 8;
+    static constexpr int kBytes = kMisc + 64;
+    static constexpr int kDynamic = kBytes + 1024;  // slack to align the base to 1 KB
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    const bool ok = mbar_wait(bar, parity, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int NH>
+__global__ void __launch_bounds__(64 + 128 * NH, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   TcParams p) {
+    using S = TcSmem<NH>;
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem + S::kQ;
+    uint8_t *sK = smem + S::kK;
+    uint8_t *sV = smem + S::kV;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
+    uint64_t *k_full = bars;
+    uint64_t *v_full = bars + STAGES;
+    uint64_t *kv_empty = bars + 2 * STAGES;
+    uint64_t *s_full = bars + 3 * STAGES;
+    uint64_t *p_full = s_full + NH;
+    uint64_t *o_done = p_full + NH;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
+    int *err_flag = reinterpret_cast<int *>(smem + S::kMisc + 8);
+
+    constexpr uint32_t kTmemCols = NH == 1 ? 256 : 512;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int split = blockIdx.x;
+    const int g = blockIdx.y / p.row_blocks;
+    const int rb = blockIdx.y % p.row_blocks;
+    const int b = blockIdx.z;
+
+    const int L = p.seq_lens[b];
+    const long long T = (long long)L + p.N;
+    const bool len_ok = L >= 0 && T <= (long long)p.max_pages * p.page_size;
+    const int ntiles = len_ok ? (int)((T + BN - 1) / BN) : 0;
+    const int chunk = (ntiles + p.splits - 1) / p.splits;
+    const int j0 = split * chunk;
+    const int j1 = min(j0 + chunk, ntiles);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int h = 0; h < NH; ++h) {
+            mbar_init(&s_full[h], 1);
+            mbar_init(&p_full[h], 128);
+            mbar_init(&o_done[h], 1);
+        }
+        *abort_flag = 0;
+        *err_flag = 0;
+        mbar_fence_init();
+        if (!len_ok) atomicOr(&p.status[b], SVF_DEV_BAD_LENGTH);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    // Q rows of this (sequence, KV head, row block) -> shared memory, K-major,
+    // 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8)).
+    if (threadIdx.x >= 64) {
+        const int tid = threadIdx.x - 64;
+        const int rows = 128 * NH;
+        for (int idx = tid; idx < rows * 16; idx += 128 * NH) {
+            const int row = idx >> 4, c = idx & 15;
+            const int R = rb * rows + row;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (R < p.M) {
+                const int node = R / p.G, hq = g * p.G + R % p.G;
+                v = *reinterpret_cast<const uint4 *>(
+                    p.q + (((size_t)b * p.N + node) * p.Hq + hq) * HD + c * 8);
+            }
+            const int hh = row >> 7, r = row & 127, dh = c >> 3, c8 = c & 7;
+            *reinterpret_cast<uint4 *>(sQ + hh * HALF_BYTES + dh * ATOM_COL_BYTES + r * 128 +
+                                       ((c8 ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (j0 < j1 && warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const int ps = p.page_size;
+            const int box_rows = ps < BN ? ps : BN;
+            const int boxes = BN / box_rows;
+            const int oob = p.num_pages * ps;  // first slot past the cache: zero fill
+            const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
+            int issued = 0;
+            for (int j = j0; j < j1; ++j) {
+                const int it = j - j0, s = it % STAGES, use = it / STAGES;
+                int coord[BN / 16];
+                for (int x = 0; x < boxes; ++x) {
+                    const long long t0 = (long long)j * BN + (long long)x * box_rows;
+                    int c = oob;
+                    if (t0 < T) {
+                        const int id = pt[t0 / ps];
+                        if (id < 0 || id >= p.num_pages)
+                            *err_flag = 1;
+                        else
+                            c = id * ps + (int)(t0 % ps);
+                    }
+                    coord[x] = c;
+                }
+                if (use > 0 && !mbar_wait(&kv_empty[s], (use - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
+                for (int x = 0; x < boxes; ++x)
+                    for (int dh = 0; dh < 2; ++dh)
+                        tma_load_3d(sK + s * TILE_BYTES + dh * ATOM_COL_BYTES + x * box_rows * 128,
+                                    &tmk, dh * 64, g, coord[x], &k_full[s]);
+                mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
+                for (int x = 0; x < boxes; ++x)
+                    for (int dh = 0; dh < 2; ++dh)
+                        tma_load_3d(sV + s * TILE_BYTES + dh * ATOM_COL_BYTES + x * box_rows * 128,
+                                    &tmv, dh * 64, g, coord[x], &v_full[s]);
+                ++issued;
+            }
+            if (*err_flag) atomicOr(&p.status[b], SVF_DEV_BAD_PAGE);
+            // Never leave with copies in flight: wait (bounded, ignoring the
+            // abort flag) for the last use of every stage.
+            volatile int never = 0;
+            for (int s = 0; s < STAGES && s < issued; ++s) {
+                const int last_use = (issued - 1 - s) / STAGES;
+                mbar_wait(&k_full[s], last_use & 1, &never);
+                mbar_wait(&v_full[s], last_use & 1, &never);
+            }
+        }
+    } else if (j0 < j1 && warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+            auto issue_qk = [&](int s, int h) {
+                const uint32_t d = tmem + h * 128;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * ATOM_COL_BYTES + (kk & 3) * 32;
+                    umma_ss(d, smem_desc_sw128(aQ + h * HALF_BYTES + off, 16, 1024),
+                            smem_desc_sw128(aK + s * TILE_BYTES + off, 16, 1024), idesc_qk,
+                            kk > 0);
+                }
+                umma_commit(&s_full[h]);
+            };
+            auto issue_pv = [&](int s, int h, bool first) {
+                const uint32_t d = tmem + NH * 128 + h * 128;
+                const uint32_t a = tmem + h * 128;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_ts(d, a + kk * 8,
+                            smem_desc_sw128(aV + s * TILE_BYTES + kk * 2048, ATOM_COL_BYTES, 1024),
+                            idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                umma_commit(&o_done[h]);
+            };
+            bool ok = mbar_wait(&k_full[0], 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                for (int h = 0; h < NH; ++h) issue_qk(0, h);
+            }
+            for (int j = j0; ok && j < j1; ++j) {
+                const int it = j - j0, s = it % STAGES, use = it / STAGES;
+                if (!(ok = mbar_wait(&v_full[s], use & 1, abort_flag))) break;
+                for (int h = 0; h < NH && ok; ++h) {
+                    if (!(ok = mbar_wait(&p_full[h], it & 1, abort_flag))) break;
+                    tc_fence_after();
+                    issue_pv(s, h, it == 0);
+                }
+                if (!ok) break;
+                umma_commit(&kv_empty[s]);
+                if (j + 1 < j1) {
+                    const int s1 = (it + 1) % STAGES, use1 = (it + 1) / STAGES;
+                    if (!(ok = mbar_wait(&k_full[s1], use1 & 1, abort_flag))) break;
+                    for (int h = 0; h < NH && ok; ++h) {
+                        if (!(ok = mbar_wait(&o_done[h], it & 1, abort_flag))) break;
+                        tc_fence_after();
+                        issue_qk(s1, h);
+                    }
+                }
+            }
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------------------ softmax
+        const int h = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int R = rb * 128 * NH + h * 128 + r;
+        const bool row_valid = R < p.M;
+        const int node = row_valid ? R / p.G : 0;
+        const int hq = g * p.G + (row_valid ? R % p.G : 0);
+        const uint64_t anc = row_valid ? p.anc[(size_t)b * p.N + node] : 0ull;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + h * 128;
+        const uint32_t tO = tmem + lane_off + NH * 128 + h * 128;
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int j = j0; j < j1; ++j) {
+            const int it = j - j0, s = it % STAGES, use = it / STAGES;
+            if (!(ok = warp_wait(&s_full[h], it & 1, abort_flag))) break;
+            tc_fence_after();
+            const long long tbase = (long long)j * BN;
+            const bool masked_tile = tbase + BN > L;
+            // pass 1: tile max of the visible scaled scores
+            float mx = -INFINITY;
+            uint32_t v[32];
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                tmem_ld32(tS + c4 * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    float x = __uint_as_float(v[c]) * sl2;
+                    if (masked_tile) {
+                        const long long t = tbase + c4 * 32 + c;
+                        const long long jj = t - L;
+                        const bool vis = t < L || (jj < p.N && ((anc >> (int)jj) & 1ull));
+                        x = vis ? x : -INFINITY;
+                    }
+                    mx = fmaxf(mx, x);
+                }
+            }
+            // lazy rescale: move the reference max only when it grows by > 2^8
+            const bool need = mx > m_ref + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need)) {
+                const float alpha = need ? ex2_approx(m_ref - mx) : 1.0f;
+                if (need) {
+                    l *= alpha;
+                    m_ref = mx;
+                }
+                if (it > 0) {
+#pragma unroll 1
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        tmem_ld32(tO + c4 * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
+                        tmem_st32(tO + c4 * 32, v);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // pass 2: P = 2^(x - m_ref) as bf16 pairs into the first 64 S columns
+            const bool live = m_ref != -INFINITY;
+            float rs = 0.0f;
+            uint32_t pk[16];
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                tmem_ld32(tS + c4 * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float x0 = __uint_as_float(v[c]) * sl2;
+                    float x1 = __uint_as_float(v[c + 1]) * sl2;
+                    if (masked_tile) {
+                        const long long t = tbase + c4 * 32 + c;
+                        const long long j0t = t - L, j1t = t + 1 - L;
+                        const bool vis0 = t < L || (j0t < p.N && ((anc >> (int)j0t) & 1ull));
+                        const bool vis1 = t + 1 < L || (j1t < p.N && ((anc >> (int)j1t) & 1ull));
+                        x0 = vis0 ? x0 : -INFINITY;
+                        x1 = vis1 ? x1 : -INFINITY;
+                    }
+                    const float p0 = live ? ex2_approx(x0 - m_ref) : 0.0f;
+                    const float p1 = live ? ex2_approx(x1 - m_ref) : 0.0f;
+                    rs += p0 + p1;
+                    pk[c >> 1] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + c4 * 16, pk);  // 16 columns, over S columns already read
+            }
+            tmem_wait_st();
+            l += rs;
+            // V rows past the sequence end may hold anything: zero them before PV.
+            if (h == 0 && tbase + BN > T) {
+                if (!(ok = warp_wait(&v_full[s], use & 1, abort_flag))) break;
+                if (tbase + r >= T) {
+                    uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int dh = 0; dh < 2; ++dh)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(sV + s * TILE_BYTES + dh * ATOM_COL_BYTES +
+                                                       r * 128 + c * 16) = z;
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            mbar_arrive(&p_full[h]);
+        }
+        // epilogue
+        if (ok && j0 < j1) ok = warp_wait(&o_done[h], (j1 - j0 - 1) & 1, abort_flag);
+        tc_fence_after();
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const float lse_v =
+            l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        const size_t row = ((size_t)b * p.N + node) * p.Hq + hq;
+        if (p.splits == 1) {
+            __nv_bfloat16 *op = p.out + row * HD;
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t o[32];
+                if (j0 < j1 && ok) {
+                    tmem_ld32(tO + c4 * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = 0;
+                }
+                if (row_valid) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv,
+                                          __uint_as_float(o[8 * k + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv,
+                                          __uint_as_float(o[8 * k + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv,
+                                          __uint_as_float(o[8 * k + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv,
+                                          __uint_as_float(o[8 * k + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(op + c4 * 32 + 8 * k) = w;
+                    }
+                }
+            }
+            if (row_valid && p.lse) p.lse[row] = (j0 < j1) ? lse_v : 0.0f;
+        } else {
+            float *op = p.part_o + ((size_t)split * p.B * p.N * p.Hq + row) * HD;
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t o[32];
+                if (j0 < j1 && ok) {
+                    tmem_ld32(tO + c4 * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = 0;
+                }
+                if (row_valid) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        float4 w = make_float4(__uint_as_float(o[4 * k + 0]) * inv,
+                                               __uint_as_float(o[4 * k + 1]) * inv,
+                                               __uint_as_float(o[4 * k + 2]) * inv,
+                                               __uint_as_float(o[4 * k + 3]) * inv);
+                        *reinterpret_cast<float4 *>(op + c4 * 32 + 4 * k) = w;
+                    }
+                }
+            }
+            if (row_valid)
+                p.part_lse[(size_t)split * p.B * p.N * p.Hq + row] =
+                    (j0 < j1) ? lse_v : -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&p.status[b], SVF_DEV_TIMEOUT);
+    // With a single split this CTA wrote final outputs: a sequence with a bad
+    // page gets zeros (every CTA of the sequence saw the same page table).
+    if (p.splits == 1 && *err_flag && warp >= 2) {
+        const int h = (warp - 2) >> 2;
+        const int R = rb * 128 * NH + h * 128 + (warp & 3) * 32 + lane;
+        if (R < p.M) {
+            const size_t row = ((size_t)b * p.N + R / p.G) * p.Hq + g * p.G + R % p.G;
+            uint4 z = make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < HD / 8; ++k)
+                *reinterpret_cast<uint4 *>(p.out + row * HD + 8 * k) = z;
+            if (p.lse) p.lse[row] = 0.0f;
+        }
+    }
+}
+
+// Merge split partials: lse = log sum_s e^{lse_s}, out = sum_s e^{lse_s - lse} o_s.
+// One warp per (sequence, node, head) row; a sequence with any status bit set
+// gets zeros.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restrict__ part_o,
+                                                           const float *__restrict__ part_lse,
+                                                           int splits, long long rows, int per_b,
+                                                           const int32_t *__restrict__ status,
+                                                           __nv_bfloat16 *__restrict__ out,
+                                                           float *__restrict__ lse) {
+    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int b = (int)(row / per_b);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lse_out = 0.0f;
+    if (status[b] == 0) {
+        float mx = -INFINITY;
+        for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[(size_t)s * rows + row]);
+        float wsum = 0.0f;
+        if (mx != -INFINITY) {
+            for (int s = 0; s < splits; ++s) {
+                const float ls = part_lse[(size_t)s * rows + row];
+                if (ls == -INFINITY) continue;
+                const float w = expf(ls - mx);
+                wsum += w;
+                const float4 o =
+                    *reinterpret_cast<const float4 *>(part_o + ((size_t)s * rows + row) * 128 + lane * 4);
+                acc.x = fmaf(w, o.x, acc.x);
+                acc.y = fmaf(w, o.y, acc.y);
+                acc.z = fmaf(w, o.z, acc.z);
+                acc.w = fmaf(w, o.w, acc.w);
+            }
+            const float inv = 1.0f / wsum;
+            acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+            lse_out = mx + logf(wsum);
+        }
+    }
+    uint2 w;
+    w.x = pack_bf16x2(acc.x, acc.y);
+    w.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2 *>(out + (size_t)row * 128 + lane * 4) = w;
+    if (lse && lane == 0) lse[row] = lse_out;
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+static bool make_kv_map(CUtensorMap *map, const void *base, int num_pages, int page_size, int Hkv) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int box_rows = page_size < tc::BN ? page_size : tc::BN;
+    cuuint64_t dims[3] = {(cuuint64_t)tc::HD, (cuuint64_t)Hkv,
+                          (cuuint64_t)num_pages * (cuuint64_t)page_size};
+    cuuint64_t strides[2] = {(cuuint64_t)tc::HD * 2, (cuuint64_t)Hkv * tc::HD * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int row_halves(int M) { return M > 128 ? 2 : 1; }
+
+int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) {
+    const int G = Hq / Hkv;
+    const int M = N * G;
+    const int NH = row_halves(M);
+    const int row_blocks = (M + 128 * NH - 1) / (128 * NH);
+    const long long units = (long long)B * Hkv * row_blocks;
+    const long long kv_max = (long long)max_pages * page_size;
+    const int tiles = (int)((kv_max + tc::BN - 1) / tc::BN);
+    const int C = num_sms();
+    // partial output write + read per split and unit, in units of one KV tile
+    const double part_tiles = (double)(128 * NH) * (tc::HD + 1) * 4 * 2 / (2.0 * tc::TILE_BYTES);
+    double best = 1e300;
+    int best_s = 1;
+    const int smax = tiles < 64 ? tiles : 64;
+    for (int s = 1; s <= smax; ++s) {
+        const long long waves = (units * s + C - 1) / C;
+        const int per_cta = (tiles + s - 1) / s;
+        const double t_chain = (double)waves * (per_cta + 1.0) + (s > 1 ? 0.5 : 0.0);
+        const double t_bytes = (double)units * (tiles + (s > 1 ? s * part_tiles : 0.0)) / C;
+        const double t = t_chain > t_bytes ? t_chain : t_bytes;
+        if (t < best - 1e-9) {
+            best = t;
+            best_s = s;
+        }
+    }
+    return best_s;
+}
+
+size_t attn_tc_workspace_bytes(int B, int N, int Hq, int Hkv, int max_pages, int page_size) {
+    const int s = attn_tc_splits(B, N, Hq, Hkv, max_pages, page_size);
+    if (s <= 1) return 0;
+    const size_t rows = (size_t)B * N * Hq;
+    return (size_t)s * rows * (tc::HD + 1) * sizeof(float) + 256;
+}
+
+int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    const int G = a.Hq / a.Hkv;
+    const int M = a.N * G;
+    const int NH = row_halves(M);
+    const int row_blocks = (M + 128 * NH - 1) / (128 * NH);
+    const int splits = attn_tc_splits(a.B, a.N, a.Hq, a.Hkv, a.max_pages, a.page_size);
+    const size_t need = attn_tc_workspace_bytes(a.B, a.N, a.Hq, a.Hkv, a.max_pages, a.page_size);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SVF_ERR_WORKSPACE;
+
+    CUtensorMap tmk, tmv;
+    if (!make_kv_map(&tmk, a.k_cache, a.num_pages, a.page_size, a.Hkv) ||
+        !make_kv_map(&tmv, a.v_cache, a.num_pages, a.page_size, a.Hkv))
+        return SVF_ERR_LAUNCH;
+
+    TcParams p;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+    p.page_table = a.page_table;
+    p.seq_lens = a.seq_lens;
+    p.anc = a.anc;
+    p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.M = M;
+    p.num_pages = a.num_pages; p.page_size = a.page_size; p.max_pages = a.max_pages;
+    p.splits = splits;
+    p.row_blocks = row_blocks;
+    const float scale = a.sm_scale > 0.0f ? a.sm_scale : 1.0f / sqrtf((float)a.D);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
+    p.lse = a.lse;
+    const size_t rows = (size_t)a.B * a.N * a.Hq;
+    if (splits > 1) {
+        uintptr_t base = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~(uintptr_t)255;
+        p.part_o = reinterpret_cast<float *>(base);
+        p.part_lse = p.part_o + (size_t)splits * rows * tc::HD;
+    } else {
+        p.part_o = nullptr;
+        p.part_lse = nullptr;
+    }
+    p.status = a.status;
+
+    dim3 grid(splits, a.Hkv * row_blocks, a.B);
+    if (NH == 1) {
+        const int smem = TcSmem<1>::kDynamic;
+        cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attn_tc_kernel<1><<<grid, 64 + 128, smem, stream>>>(tmk, tmv, p);
+    } else {
+        const int smem = TcSmem<2>::kDynamic;
+        cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attn_tc_kernel<2><<<grid, 64 + 256, smem, stream>>>(tmk, tmv, p);
+    }
+    if (cudaGetLastError() != cudaSuccess) return SVF_ERR_LAUNCH;
+    if (splits > 1) {
+        const long long threads = (long long)rows * 32;
+        const int blocks = (int)((threads + 255) / 256);
+        attn_combine_kernel<<<blocks, 256, 0, stream>>>(
+            p.part_o, p.part_lse, splits, (long long)rows, a.N * a.Hq, a.status, p.out, a.lse);
+        if (cudaGetLastError() != cudaSuccess) return SVF_ERR_LAUNCH;
+    }
+    return SVF_OK;
+}
+
+}  // namespace svf

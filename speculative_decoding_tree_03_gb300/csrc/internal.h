@@ -1,0 +1,50 @@
+// internal.h -- launchers shared between the kernel files and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "specverify.h"
+
+namespace svf {
+
+// Ancestor bitmasks (mask.cu).
+cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint64_t *anc, int32_t *depth,
+                             int32_t *status, cudaStream_t stream);
+
+// Arguments of one tree-attention call, shared by both attention kernels.
+struct AttnArgs {
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    int num_pages, page_size;
+    const int32_t *page_table;
+    int max_pages;
+    const int32_t *seq_lens;
+    const uint64_t *anc;
+    int B, N, Hq, Hkv, D, dtype;
+    float sm_scale;
+    void *out;
+    float *lse;
+    int32_t *status;
+};
+
+// CUDA-core path for fp32 (and any dtype): one warp per (sequence, node, head) (attn_simt.cu).
+cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t stream);
+
+// Tensor-core path for bf16 (attn_tc.cu).
+size_t attn_tc_workspace_bytes(int B, int N, int Hq, int Hkv, int max_pages, int page_size);
+int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size);
+int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+// Acceptance walk (accept.cu).
+size_t accept_workspace_bytes(int B, int N, int V);
+cudaError_t launch_accept(const float *target, const float *draft, const int32_t *tokens,
+                          const int32_t *parent, const float *u_accept, const float *u_bonus, int B,
+                          int N, int V, int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                          float *ratio, void *workspace, int32_t *status, cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace svf

@@ -1,0 +1,111 @@
+"""The C-ABI library builds, loads without a GPU and exports every symbol
+include/specverify.h declares; host-side argument checks return their codes
+before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_tree_03_gb300 import build as b
+    b.build()
+    import speculative_decoding_tree_03_gb300 as sv
+    return sv.load_library()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "specverify.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char \*)\s*\*?\s*(svf_\w+)\s*\(",
+                                 text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("svf_tree_mask_build", "svf_tree_verify_attn", "svf_spec_accept",
+              "svf_tree_verify_attn_workspace_size", "svf_spec_accept_workspace_size",
+              "svf_status_string", "svf_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import speculative_decoding_tree_03_gb300 as sv
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+    assert sorted(sv.EXPORTED) == declared_symbols()
+
+
+def test_status_strings(lib):
+    import speculative_decoding_tree_03_gb300 as sv
+    assert sv.status_string(0) == "ok"
+    assert "workspace" in sv.status_string(-4)
+    assert "parent" in sv.status_string(1)
+    assert lib.svf_version() >= 100
+
+
+P = ctypes.c_void_p(256)  # never dereferenced: every call below returns before using it
+
+
+def test_mask_argument_checks(lib):
+    assert lib.svf_tree_mask_build(P, -1, 4, P, P, P, None) == -1
+    assert lib.svf_tree_mask_build(None, 0, 4, None, None, None, None) == 0
+    assert lib.svf_tree_mask_build(P, 1, 1025, P, P, P, None) == -2
+    assert lib.svf_tree_mask_build(P, 1, 0, P, P, P, None) == -2
+    assert lib.svf_tree_mask_build(None, 1, 4, P, P, P, None) == -1
+
+
+def _attn(lib, **kw):
+    a = dict(q=P, k=P, v=P, num_pages=4, page_size=16, table=P, max_pages=2, lens=P, anc=P, B=1,
+             N=3, Hq=8, Hkv=2, D=128, dtype=1, scale=0.0, out=P, lse=None, ws=None, wsb=0,
+             status=P)
+    a.update(kw)
+    return lib.svf_tree_verify_attn(a["q"], a["k"], a["v"], a["num_pages"], a["page_size"],
+                                    a["table"], a["max_pages"], a["lens"], a["anc"], a["B"],
+                                    a["N"], a["Hq"], a["Hkv"], a["D"], a["dtype"], a["scale"],
+                                    a["out"], a["lse"], a["ws"], a["wsb"], a["status"], None)
+
+
+def test_attention_argument_checks(lib):
+    assert _attn(lib, B=-1) == -1
+    assert _attn(lib, B=0, q=None) == 0
+    assert _attn(lib, q=None) == -1
+    assert _attn(lib, N=65) == -2
+    assert _attn(lib, Hq=6, Hkv=4) == -2
+    assert _attn(lib, D=64) == -2                       # bf16 needs head_dim 128
+    assert _attn(lib, page_size=48) == -2               # bf16 page sizes 16/32/64/128k
+    assert _attn(lib, dtype=0, D=96) == -2              # fp32 head_dim 64 or 128
+    assert _attn(lib, dtype=7) == -2
+    assert _attn(lib, q=ctypes.c_void_p(264)) == -1     # not 16-byte aligned
+
+
+def test_accept_argument_checks(lib):
+    def call(B=2, N=3, V=100, ws=P, wsb=1 << 20, t=P):
+        return lib.svf_spec_accept(t, P, P, P, P, P, B, N, V, P, P, P, None, ws, wsb, P, None)
+    assert call(B=-1) == -1
+    assert call(B=0, t=None) == 0
+    assert call(t=None) == -1
+    assert call(N=0) == -2 and call(N=1025) == -2
+    assert call(V=786433) == -2
+    assert call(ws=None) == -4
+    assert call(wsb=8) == -4
+    assert lib.svf_spec_accept_workspace_size(2, 3, 100) > 0
+
+
+def test_workspace_sizes_without_gpu(lib):
+    # bf16 attention with many KV tiles per (sequence, head) splits the KV range
+    n = lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 1, 1, 2176)
+    assert n >= 0
+    assert lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 0, 1, 2176) == 0
+
+
+def test_package_refuses_cpu_tensors():
+    import torch
+    import speculative_decoding_tree_03_gb300 as sv
+    with pytest.raises(sv.SpecVerifyError):
+        sv.tree_mask_build(torch.zeros((1, 3), dtype=torch.int32))

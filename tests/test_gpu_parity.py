@@ -1,0 +1,394 @@
+"""GPU parity: every kernel through the C ABI against the fp64 oracle.
+
+Masks, accepted paths, accepted lengths and tokens must match bit for bit
+(near ties aside, see gpu_common); attention outputs within max-abs 2e-2
+(bf16 inputs and output) or 1e-5 (fp32), lse within 2e-3 (bf16) or 1e-5.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import (bf16_tensor, compare_accept, compare_ratio, device_inputs,
+                        oracle_attention, as_f32)
+from synth import WORKLOADS, make_inputs, binary_tree_parent, chain_parent
+from synth.gen import Workload, f32_to_bf16_bits, bf16_bits_to_f32
+
+pytestmark = pytest.mark.gpu
+
+BF16_OUT_TOL = 2e-2
+BF16_LSE_TOL = 2e-3
+F32_TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def sv():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from speculative_decoding_tree_03_gb300 import build as _b
+    _b.build()
+    import speculative_decoding_tree_03_gb300 as m
+    return m
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+# ---------------------------------------------------------------------------
+# tree_mask_build
+# ---------------------------------------------------------------------------
+
+def _random_parents(rng, B, N):
+    return np.stack([np.array([-1] + [int(rng.integers(0, i)) for i in range(1, N)], np.int32)
+                     for _ in range(B)])
+
+
+@pytest.mark.parametrize("N", [1, 2, 7, 31, 60, 64, 65, 200, 1024])
+def test_mask_matches_oracle(sv, N):
+    rng = np.random.default_rng(N)
+    parent = _random_parents(rng, 5, N)
+    parent[1] = np.arange(-1, N - 1)  # a chain
+    anc, depth, status = sv.tree_mask_build(torch.from_numpy(parent).cuda())
+    oa, od, os_ = oracle.tree_mask(parent)
+    assert (_np(anc).view(np.uint64) == oa).all()
+    assert (_np(depth) == od).all() and (_np(status) == os_).all()
+
+
+def test_mask_invalid_trees(sv):
+    bad = np.array([[0, 0, 1, 2], [-1, 1, 0, 0], [-1, 0, 5, 1], [-1, 0, 1, 1]], np.int32)
+    anc, depth, status = sv.tree_mask_build(torch.from_numpy(bad).cuda())
+    oa, od, os_ = oracle.tree_mask(bad)
+    assert _np(status).tolist() == [1, 1, 1, 0]
+    assert (_np(anc).view(np.uint64) == oa).all() and (_np(depth) == od).all()
+
+
+def test_empty_batch_is_a_no_op(sv):
+    lib = sv.load_library()
+    assert lib.svf_tree_mask_build(None, 0, 4, None, None, None, None) == 0
+    assert lib.svf_spec_accept(None, None, None, None, None, None, 0, 4, 10, None, None, None,
+                               None, None, 0, None, None) == 0
+
+
+# ---------------------------------------------------------------------------
+# tree_verify_attn
+# ---------------------------------------------------------------------------
+
+def _attn_case(seed, B, N, parent, lens, Hq, Hkv, D, dtype, page_size, extra_pages=3):
+    """Random attention inputs with a paged (or contiguous) cache."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, np.int32)
+    T = lens.astype(np.int64) + N
+    if page_size == 0:
+        ps = int(-(-int(T.max()) // 128) * 128)
+        n = np.ones(B, np.int64)
+    else:
+        ps = page_size
+        n = -(-T // ps)
+    P = int(n.sum()) + extra_pages
+    perm = rng.permutation(P).astype(np.int32)
+    table = np.full((B, int(n.max())), -1, np.int32)
+    off = 0
+    for b in range(B):
+        table[b, : n[b]] = perm[off: off + n[b]]
+        off += int(n[b])
+    q = rng.standard_normal((B, N, Hq, D)).astype(np.float32)
+    kc = rng.standard_normal((P, ps, Hkv, D)).astype(np.float32)
+    vc = rng.standard_normal((P, ps, Hkv, D)).astype(np.float32)
+    if dtype == "bf16":
+        q, kc, vc = (bf16_bits_to_f32(f32_to_bf16_bits(x)) for x in (q, kc, vc))
+    # logical K/V for the oracle, read through the page table
+    Tcap = int(T.max())
+    K = np.zeros((B, Tcap, Hkv, D), np.float32)
+    V = np.zeros_like(K)
+    for b in range(B):
+        t = np.arange(T[b])
+        pages = table[b, t // ps]
+        K[b, : T[b]] = kc[pages, t % ps]
+        V[b, : T[b]] = vc[pages, t % ps]
+    return dict(q=q, kc=kc, vc=vc, table=table, lens=lens, parent=np.asarray(parent, np.int32),
+                K=K, V=V, ps=ps, P=P)
+
+
+def _run_attn(sv, c, dtype, poison_tail=False):
+    dev = "cuda"
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    q = torch.from_numpy(c["q"]).to(dev).to(tdt)
+    kc = torch.from_numpy(c["kc"]).to(dev).to(tdt)
+    vc = torch.from_numpy(c["vc"]).to(dev).to(tdt)
+    if poison_tail:
+        # slots past each sequence's end inside its last page hold NaN
+        B = c["q"].shape[0]
+        N = c["q"].shape[1]
+        for b in range(B):
+            T = int(c["lens"][b]) + N
+            last = int(c["table"][b, (T - 1) // c["ps"]])
+            s0 = T % c["ps"]
+            if s0:
+                kc[last, s0:] = float("nan")
+                vc[last, s0:] = float("nan")
+    parent = torch.from_numpy(c["parent"]).to(dev)
+    anc, _, _ = sv.tree_mask_build(parent)
+    out, lse, status = sv.tree_verify_attn(q, kc, vc, torch.from_numpy(c["table"]).to(dev),
+                                           torch.from_numpy(c["lens"]).to(dev), anc)
+    torch.cuda.synchronize()
+    return _np(out.float()), _np(lse), _np(status)
+
+
+CASES = [
+    # name, seed, B, parent, lens, Hq, Hkv, D, dtype, page_size
+    ("worked_tree_contig", 1, 2, "worked", [300, 129], 8, 2, 128, "bf16", 0),
+    ("binary31_paged16_g8", 2, 3, "binary4", [1000, 17, 385], 16, 2, 128, "bf16", 16),
+    ("random60_paged32_rowblocks", 3, 2, "random60", [700, 250], 8, 1, 128, "bf16", 32),
+    ("single_node_no_prefix", 4, 2, "single", [0, 5], 4, 4, 128, "bf16", 128),
+    ("tree_crosses_tile", 5, 2, "random64", [100, 64], 8, 2, 128, "bf16", 64),
+    ("chain16_paged256", 6, 3, "chain16", [2000, 1, 511], 32, 8, 128, "bf16", 256),
+    ("g1_many_heads", 7, 1, "binary3", [900], 8, 8, 128, "bf16", 16),
+    ("fp32_d64", 8, 2, "worked", [200, 3], 4, 4, 64, "f32", 0),
+    ("fp32_d128_paged", 9, 2, "binary3", [150, 40], 8, 2, 128, "f32", 16),
+]
+
+
+def _parent_of(kind, B, rng):
+    if kind == "worked":
+        p = np.array([-1, 0, 0, 1, 1, 2, 2], np.int32)
+    elif kind == "binary4":
+        p = binary_tree_parent(4)
+    elif kind == "binary3":
+        p = binary_tree_parent(3)
+    elif kind == "single":
+        p = np.array([-1], np.int32)
+    elif kind == "chain16":
+        p = chain_parent(16)
+    elif kind.startswith("random"):
+        N = int(kind[6:])
+        return _random_parents(rng, B, N)
+    return np.broadcast_to(p, (B, p.size)).copy()
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_attention_small_cases(sv, case):
+    name, seed, B, pk, lens, Hq, Hkv, D, dtype, ps = case
+    parent = _parent_of(pk, B, np.random.default_rng(seed + 100))
+    N = parent.shape[1]
+    c = _attn_case(seed, B, N, parent, lens, Hq, Hkv, D, dtype, ps)
+    out, lse, status = _run_attn(sv, c, dtype)
+    assert (status == 0).all()
+    o_ref, l_ref = oracle.tree_attn(c["q"], c["K"], c["V"], c["lens"], c["parent"])
+    o_ref = o_ref.reshape(out.shape)
+    l_ref = l_ref.reshape(lse.shape)
+    tol_o = BF16_OUT_TOL if dtype == "bf16" else F32_TOL
+    tol_l = BF16_LSE_TOL if dtype == "bf16" else F32_TOL
+    err_o = np.abs(out - o_ref).max()
+    err_l = np.abs(lse - l_ref).max()
+    print(f"{name}: max|out-ref| {err_o:.3g} max|lse-ref| {err_l:.3g}")
+    assert err_l <= tol_l, err_l
+    assert err_o <= tol_o, err_o
+
+
+def test_attention_ignores_garbage_past_sequence_end(sv):
+    parent = binary_tree_parent(3)
+    B = 2
+    parent = np.broadcast_to(parent, (B, parent.size)).copy()
+    c = _attn_case(11, B, parent.shape[1], parent, [77, 301], 8, 2, 128, "bf16", 0)
+    out, lse, status = _run_attn(sv, c, "bf16", poison_tail=True)
+    o_ref, _ = oracle.tree_attn(c["q"], c["K"], c["V"], c["lens"], c["parent"])
+    assert np.isfinite(out).all()
+    assert np.abs(out - o_ref.reshape(out.shape)).max() <= BF16_OUT_TOL
+
+
+def test_attention_bad_page_and_length_status(sv):
+    parent = binary_tree_parent(2)
+    B = 3
+    parent = np.broadcast_to(parent, (B, parent.size)).copy()
+    c = _attn_case(12, B, parent.shape[1], parent, [200, 90, 33], 8, 2, 128, "bf16", 16)
+    c["table"][1, 2] = c["P"] + 7          # page id outside the cache
+    c["lens"][2] = c["table"].shape[1] * 16  # overflows its page table
+    for dtype in ("bf16", "f32"):
+        out, lse, status = _run_attn(sv, c, dtype)
+        assert status.tolist() == [0, 4, 8], status
+        assert (out[1] == 0).all() and (out[2] == 0).all()
+        o_ref, _ = oracle.tree_attn(c["q"][:1], c["K"][:1], c["V"][:1], c["lens"][:1],
+                                    c["parent"][:1])
+        tol = BF16_OUT_TOL if dtype == "bf16" else F32_TOL
+        assert np.abs(out[0] - o_ref.reshape(out[0].shape)).max() <= tol
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3])
+def test_attention_workloads_full(sv, idx):
+    w = WORKLOADS[idx]
+    inp = make_inputs(w, 1000 + idx, with_kv=True, with_logits=False)
+    d = device_inputs(inp)
+    anc, _, _ = sv.tree_mask_build(d["parent"])
+    out, lse, status = sv.tree_verify_attn(d["q"], d["k"], d["v"], d["page_table"],
+                                           d["seq_lens"], anc)
+    torch.cuda.synchronize()
+    assert (_np(status) == 0).all()
+    o_ref, l_ref = oracle_attention(inp)
+    out = _np(out.float())
+    err_o = np.abs(out - o_ref.reshape(out.shape)).max()
+    err_l = np.abs(_np(lse) - l_ref.reshape(lse.shape)).max()
+    tol_o = BF16_OUT_TOL if w.dtype == "bf16" else F32_TOL
+    tol_l = BF16_LSE_TOL if w.dtype == "bf16" else F32_TOL
+    print(f"{w.name}: max|out-ref| {err_o:.3g} max|lse-ref| {err_l:.3g}")
+    assert err_o <= tol_o and err_l <= tol_l
+
+
+def test_attention_serving_70b_sampled(sv):
+    """Full-size 70B-shaped workload (8.6 GB paged cache) in the launch shape
+    the benchmark times; the oracle recomputes sampled rows one by one."""
+    w = WORKLOADS[4]
+    inp = make_inputs(w, 1004, with_kv=True, with_logits=False)
+    d = device_inputs(inp)
+    anc, _, _ = sv.tree_mask_build(d["parent"])
+    out, lse, status = sv.tree_verify_attn(d["q"], d["k"], d["v"], d["page_table"],
+                                           d["seq_lens"], anc)
+    torch.cuda.synchronize()
+    assert (_np(status) == 0).all()
+    rng = np.random.default_rng(7)
+    bs = [0, 33, 63]
+    rows = []
+    for n in range(len(bs)):
+        for i in (0, 1, 14, 30):
+            for h in rng.choice(w.Hq, size=6, replace=False):
+                rows.append((n, i, int(h)))
+    o_ref, l_ref = oracle_attention(inp, bs=bs, rows=np.array(rows))
+    out = _np(out.float())
+    lse = _np(lse)
+    for r, (n, i, h) in enumerate(rows):
+        b = bs[n]
+        assert np.abs(out[b, i, h] - o_ref[r]).max() <= BF16_OUT_TOL
+        assert abs(lse[b, i, h] - l_ref[r]) <= BF16_LSE_TOL
+
+
+# ---------------------------------------------------------------------------
+# spec_accept
+# ---------------------------------------------------------------------------
+
+def _accept_gpu(sv, arrs):
+    dev = "cuda"
+    t = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in arrs.items()}
+    res = sv.spec_accept(t["target"], t["draft"], t["tokens"], t["parent"], t["u_accept"],
+                         t["u_bonus"])
+    torch.cuda.synchronize()
+    return {k: (_np(v) if v is not None else None) for k, v in res.items()}
+
+
+def _arrays(inp):
+    return dict(target=inp.target, draft=inp.draft, tokens=inp.tokens, parent=inp.parent,
+                u_accept=inp.u_accept, u_bonus=inp.u_bonus)
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+def test_accept_workloads(sv, idx):
+    w = WORKLOADS[idx]
+    inp = make_inputs(w, 1000 + idx, with_kv=False, with_logits=True)
+    arrs = _arrays(inp)
+    gpu = _accept_gpu(sv, arrs)
+    orc = oracle.spec_accept(**arrs)
+    stats = compare_accept(gpu, arrs, orc)
+    rerr = compare_ratio(gpu["ratio"], orc)
+    print(f"{w.name}: {stats} max ratio err {rerr:.3g} accept_len {gpu['accept_len'][:8]}")
+    assert rerr < 1e-3
+
+
+def _synthetic_accept(seed, B, N, V, parent, sigma=3.0, noise=1.0, iid_children=True):
+    rng = np.random.default_rng(seed)
+    tgt = (sigma * rng.standard_normal((B, N, V))).astype(np.float32)
+    dft = (tgt + noise * rng.standard_normal((B, N, V))).astype(np.float32)
+    parent = np.broadcast_to(np.asarray(parent, np.int32), (B, N)).copy()
+    tokens = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for c in range(1, N):
+            j = parent[b, c]
+            d = dft[b, j].astype(np.float64)
+            q = np.exp(d - d.max()); q /= q.sum()
+            tokens[b, c] = rng.choice(V, p=q) if iid_children else int(np.argmax(q))
+    return dict(target=tgt, draft=dft, tokens=tokens, parent=parent,
+                u_accept=rng.random((B, N), dtype=np.float32),
+                u_bonus=rng.random(B, dtype=np.float32))
+
+
+@pytest.mark.parametrize("V", [8, 37, 1000, 2049, 5003, 32000])
+def test_accept_vocab_sizes(sv, V):
+    """Warp-per-sequence (V <= 2048) and block-per-sequence paths, vector and
+    scalar loads (V % 4)."""
+    arrs = _synthetic_accept(V, 64, 7, V, [-1, 0, 0, 1, 1, 2, 2], sigma=2.0, noise=0.7)
+    gpu = _accept_gpu(sv, arrs)
+    orc = oracle.spec_accept(**arrs)
+    stats = compare_accept(gpu, arrs, orc)
+    print(V, stats)
+
+
+def test_accept_root_only_and_chain(sv):
+    arrs = _synthetic_accept(21, 32, 1, 500, [-1])
+    gpu = _accept_gpu(sv, arrs)
+    orc = oracle.spec_accept(**arrs)
+    compare_accept(gpu, arrs, orc)
+    assert (gpu["accept_len"] == 0).all()
+    arrs = _synthetic_accept(22, 32, 12, 3000, chain_parent(12), sigma=1.0, noise=0.3)
+    gpu = _accept_gpu(sv, arrs)
+    compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
+
+
+def test_accept_status_errors(sv):
+    arrs = _synthetic_accept(23, 4, 4, 100, [-1, 0, 0, 1])
+    arrs["parent"][1, 2] = 3
+    arrs["tokens"][2, 3] = 100
+    arrs["tokens"][3, 1] = -5
+    gpu = _accept_gpu(sv, arrs)
+    orc = oracle.spec_accept(**arrs)
+    assert gpu["status"].tolist() == orc["status"].tolist() == [0, 1, 2, 2]
+    for b in (1, 2, 3):
+        assert gpu["accept_len"][b] == 0
+        assert (gpu["path"][b] == -1).all() and (gpu["out_tokens"][b] == -1).all()
+        assert np.isnan(gpu["ratio"][b]).all()
+    compare_accept(gpu, arrs, orc)
+
+
+def test_accept_chi_square_on_gpu(sv):
+    """One call with 10^6 sequences (V=8, chain of one draft drawn from q):
+    the emitted token follows p (chi-square), and every trial matches the
+    oracle bit for bit except near ties."""
+    from scipy.stats import chisquare
+    rng = np.random.default_rng(31)
+    V, B = 8, 1_000_000
+    p = rng.dirichlet(np.ones(V)); q = rng.dirichlet(np.ones(V))
+    lp, lq = np.log(p).astype(np.float32), np.log(q).astype(np.float32)
+    qq = np.exp(lq.astype(np.float64) - lq.max()); qq /= qq.sum()
+    pp = np.exp(lp.astype(np.float64) - lp.max()); pp /= pp.sum()
+    tokens = np.zeros((B, 2), np.int32)
+    tokens[:, 1] = rng.choice(V, size=B, p=qq)
+    arrs = dict(target=np.broadcast_to(lp, (B, 2, V)).copy(),
+                draft=np.broadcast_to(lq, (B, 2, V)).copy(), tokens=tokens,
+                parent=np.broadcast_to(np.array([-1, 0], np.int32), (B, 2)).copy(),
+                u_accept=rng.random((B, 2), dtype=np.float32),
+                u_bonus=rng.random(B, dtype=np.float32))
+    gpu = _accept_gpu(sv, arrs)
+    counts = np.bincount(gpu["out_tokens"][:, 0], minlength=V)
+    _, pval = chisquare(counts, pp * B)
+    assert pval > 1e-4, pval
+    orc = oracle.spec_accept(**arrs)
+    compare_accept(gpu, arrs, orc, max_flag_frac=1e-3)
+
+
+# ---------------------------------------------------------------------------
+# the whole step
+# ---------------------------------------------------------------------------
+
+def test_verify_step_tiny_chain(sv):
+    w = WORKLOADS[0]
+    inp = make_inputs(w, 1000)
+    d = device_inputs(inp)
+    out, lse, res, _ = sv.verify_step(d["parent"], d["tokens"], d["q"], d["k"], d["v"],
+                                      d["page_table"], d["seq_lens"], d["target"], d["draft"],
+                                      d["u_accept"], d["u_bonus"])
+    torch.cuda.synchronize()
+    o_ref, _ = oracle_attention(inp)
+    assert np.abs(_np(out) - o_ref.reshape(out.shape)).max() <= F32_TOL
+    arrs = _arrays(inp)
+    compare_accept({k: (_np(v) if v is not None else None) for k, v in res.items()}, arrs,
+                   oracle.spec_accept(**arrs))
