@@ -305,12 +305,30 @@ def run_ours(args, w, idx):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        # keep the GPU busy until the sampler reports (nvidia-smi starts in ~0.1-0.5 s)
+        t_soak = time.perf_counter()
+        i = 0
+        while (len(clk.lines) < 3 and time.perf_counter() - t_soak < 5.0) or i < args.warmup:
+            step(sets[i % nsets])
+            i += 1
+            if i % 16 == 0:
+                torch.cuda.synchronize(dev)
         barrier()
         t_start.record(stream)
         for i in range(args.steps):
             step(sets[i % nsets], evs[i])
         t_end.record(stream)
         barrier()
+        # a few more samples under load after the timed region
+        t_tail = time.perf_counter()
+        n0 = len(clk.lines)
+        i = 0
+        while len(clk.lines) < n0 + 2 and time.perf_counter() - t_tail < 2.0:
+            step(sets[i % nsets])
+            i += 1
+            if i % 16 == 0:
+                torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
     ms_local = t_start.elapsed_time(t_end) / args.steps
     attn_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     acc_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps

@@ -51,6 +51,7 @@ struct TcParams {
     int B, N, Hq, Hkv, G, M;
     int num_pages, page_size, max_pages;
     int splits, row_blocks;
+    int q_tma;        // 1: Q arrives by TMA (G a power of two <= 128)
     float scale_log2;
     __nv_bfloat16 *out;
     float *lse;
@@ -65,7 +66,7 @@ struct TcSmem {
     static constexpr int kK = kQ + NH * tc::HALF_BYTES;
     static constexpr int kV = kK + tc::STAGES * tc::TILE_BYTES;
     static constexpr int kBar = kV + tc::STAGES * tc::TILE_BYTES;
-    static constexpr int kNumBars = 3 * tc::STAGES + 3 * NH;
+    static constexpr int kNumBars = 3 * tc::STAGES + 3 * NH + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kDynamic = kBytes + 1024;  // slack to align the base to 1 KB
@@ -76,10 +77,23 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
+// Visibility of the 32 columns t = L + off + i (i = 0..31) for a row whose
+// ancestor set is `anc`: prefix columns (t < L) are visible, tree column
+// L + j is visible iff bit j of anc is set; columns past the tree have no bit.
+__device__ __forceinline__ uint32_t visible_bits(long long off, uint64_t anc) {
+    if (off <= -32) return 0xffffffffu;
+    if (off >= 64) return 0u;
+    if (off < 0) {
+        const int sh = (int)(-off);
+        return ((1u << sh) - 1u) | (uint32_t)(anc << sh);
+    }
+    return (uint32_t)(anc >> (int)off);
+}
+
 template <int NH>
 __global__ void __launch_bounds__(64 + 128 * NH, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                   TcParams p) {
+                   const __grid_constant__ CUtensorMap tmq, TcParams p) {
     using S = TcSmem<NH>;
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
@@ -95,6 +109,7 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
     uint64_t *s_full = bars + 3 * STAGES;
     uint64_t *p_full = s_full + NH;
     uint64_t *o_done = p_full + NH;
+    uint64_t *q_full = o_done + NH;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
     int *err_flag = reinterpret_cast<int *>(smem + S::kMisc + 8);
@@ -115,7 +130,45 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
     const int j0 = split * chunk;
     const int j1 = min(j0 + chunk, ntiles);
 
+    // Page-table lookup of one tile: the starting slot of each of its boxes
+    // (a slot past the cache, zero-filled by TMA, for boxes past the sequence
+    // or with a page id outside the cache).
+    const int ps = p.page_size;
+    const int box_rows = ps < BN ? ps : BN;
+    const int boxes = BN / box_rows;
+    const int oob = p.num_pages * ps;
+    const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
+    auto tile_coords = [&](int j, int *coord) {
+        for (int x = 0; x < boxes; ++x) {
+            const long long t0 = (long long)j * BN + (long long)x * box_rows;
+            int c = oob;
+            if (t0 < T) {
+                const int id = pt[t0 / ps];
+                if (id < 0 || id >= p.num_pages)
+                    *err_flag = 1;
+                else
+                    c = id * ps + (int)(t0 % ps);
+            }
+            coord[x] = c;
+        }
+    };
+    auto issue_tile = [&](int s, const int *coord) {
+        mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
+        for (int x = 0; x < boxes; ++x)
+            for (int dh = 0; dh < 2; ++dh)
+                tma_load_3d(sK + s * TILE_BYTES + dh * ATOM_COL_BYTES + x * box_rows * 128, &tmk,
+                            dh * 64, g, coord[x], &k_full[s]);
+        mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
+        for (int x = 0; x < boxes; ++x)
+            for (int dh = 0; dh < 2; ++dh)
+                tma_load_3d(sV + s * TILE_BYTES + dh * ATOM_COL_BYTES + x * box_rows * 128, &tmv,
+                            dh * 64, g, coord[x], &v_full[s]);
+    };
+
     if (threadIdx.x == 0) {
+        int coord0[BN / 16];
+        *err_flag = 0;
+        if (j0 < j1) tile_coords(j0, coord0);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&v_full[s], 1);
@@ -126,36 +179,52 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
             mbar_init(&p_full[h], 128);
             mbar_init(&o_done[h], 1);
         }
+        mbar_init(q_full, 1);
         *abort_flag = 0;
-        *err_flag = 0;
         mbar_fence_init();
         if (!len_ok) atomicOr(&p.status[b], SVF_DEV_BAD_LENGTH);
+        if (j0 < j1) {
+            if (p.q_tma) {
+                // rows (node, head) of this block: box = 64 dims x G heads x 128/G nodes
+                mbar_arrive_expect_tx(q_full, NH * HALF_BYTES);
+                const int nodes = 128 / p.G;
+                for (int hh = 0; hh < NH; ++hh)
+                    for (int dh = 0; dh < 2; ++dh)
+                        tma_load_4d(sQ + hh * HALF_BYTES + dh * ATOM_COL_BYTES, &tmq, dh * 64,
+                                    g * p.G, (rb * NH + hh) * nodes, b, q_full);
+            }
+            issue_tile(0, coord0);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmk);
-        tma_prefetch_desc(&tmv);
-    }
-    // Q rows of this (sequence, KV head, row block) -> shared memory, K-major,
-    // 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8)).
-    if (threadIdx.x >= 64) {
+    if (!p.q_tma && threadIdx.x >= 64) {
+        // Q rows -> shared memory by the softmax threads (K-major, 128-byte
+        // swizzle: 16-byte chunk c of row r lands at chunk c ^ (r % 8)).
         const int tid = threadIdx.x - 64;
-        const int rows = 128 * NH;
-        for (int idx = tid; idx < rows * 16; idx += 128 * NH) {
+        constexpr int kIters = 16;
+        uint4 v[kIters];
+#pragma unroll
+        for (int k = 0; k < kIters; ++k) {
+            const int idx = tid + k * 128 * NH;
             const int row = idx >> 4, c = idx & 15;
-            const int R = rb * rows + row;
-            uint4 v = make_uint4(0, 0, 0, 0);
+            const int R = rb * 128 * NH + row;
+            v[k] = make_uint4(0, 0, 0, 0);
             if (R < p.M) {
                 const int node = R / p.G, hq = g * p.G + R % p.G;
-                v = *reinterpret_cast<const uint4 *>(
+                v[k] = *reinterpret_cast<const uint4 *>(
                     p.q + (((size_t)b * p.N + node) * p.Hq + hq) * HD + c * 8);
             }
+        }
+#pragma unroll
+        for (int k = 0; k < kIters; ++k) {
+            const int idx = tid + k * 128 * NH;
+            const int row = idx >> 4, c = idx & 15;
             const int hh = row >> 7, r = row & 127, dh = c >> 3, c8 = c & 7;
             *reinterpret_cast<uint4 *>(sQ + hh * HALF_BYTES + dh * ATOM_COL_BYTES + r * 128 +
-                                       ((c8 ^ (r & 7)) << 4)) = v;
+                                       ((c8 ^ (r & 7)) << 4)) = v[k];
         }
         fence_proxy_async_smem();
     }
@@ -167,38 +236,13 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
     if (j0 < j1 && warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const int ps = p.page_size;
-            const int box_rows = ps < BN ? ps : BN;
-            const int boxes = BN / box_rows;
-            const int oob = p.num_pages * ps;  // first slot past the cache: zero fill
-            const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
-            int issued = 0;
-            for (int j = j0; j < j1; ++j) {
+            int issued = 1;  // tile j0 went out during setup
+            for (int j = j0 + 1; j < j1; ++j) {
                 const int it = j - j0, s = it % STAGES, use = it / STAGES;
                 int coord[BN / 16];
-                for (int x = 0; x < boxes; ++x) {
-                    const long long t0 = (long long)j * BN + (long long)x * box_rows;
-                    int c = oob;
-                    if (t0 < T) {
-                        const int id = pt[t0 / ps];
-                        if (id < 0 || id >= p.num_pages)
-                            *err_flag = 1;
-                        else
-                            c = id * ps + (int)(t0 % ps);
-                    }
-                    coord[x] = c;
-                }
+                tile_coords(j, coord);
                 if (use > 0 && !mbar_wait(&kv_empty[s], (use - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
-                for (int x = 0; x < boxes; ++x)
-                    for (int dh = 0; dh < 2; ++dh)
-                        tma_load_3d(sK + s * TILE_BYTES + dh * ATOM_COL_BYTES + x * box_rows * 128,
-                                    &tmk, dh * 64, g, coord[x], &k_full[s]);
-                mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
-                for (int x = 0; x < boxes; ++x)
-                    for (int dh = 0; dh < 2; ++dh)
-                        tma_load_3d(sV + s * TILE_BYTES + dh * ATOM_COL_BYTES + x * box_rows * 128,
-                                    &tmv, dh * 64, g, coord[x], &v_full[s]);
+                issue_tile(s, coord);
                 ++issued;
             }
             if (*err_flag) atomicOr(&p.status[b], SVF_DEV_BAD_PAGE);
@@ -210,6 +254,7 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                 mbar_wait(&k_full[s], last_use & 1, &never);
                 mbar_wait(&v_full[s], last_use & 1, &never);
             }
+            if (p.q_tma) mbar_wait(q_full, 0, &never);
         }
     } else if (j0 < j1 && warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -238,7 +283,8 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                             idesc_pv, (!first || kk > 0) ? 1u : 0u);
                 umma_commit(&o_done[h]);
             };
-            bool ok = mbar_wait(&k_full[0], 0, abort_flag);
+            bool ok = !p.q_tma || mbar_wait(q_full, 0, abort_flag);
+            ok = ok && mbar_wait(&k_full[0], 0, abort_flag);
             if (ok) {
                 tc_fence_after();
                 for (int h = 0; h < NH; ++h) issue_qk(0, h);
@@ -284,27 +330,32 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
             const int it = j - j0, s = it % STAGES, use = it / STAGES;
             if (!(ok = warp_wait(&s_full[h], it & 1, abort_flag))) break;
             tc_fence_after();
+            uint32_t v[128];
+            tmem_ld32(tS, v);
+            tmem_ld32(tS + 32, v + 32);
+            tmem_ld32(tS + 64, v + 64);
+            tmem_ld32(tS + 96, v + 96);
+            tmem_wait_ld();
             const long long tbase = (long long)j * BN;
-            const bool masked_tile = tbase + BN > L;
-            // pass 1: tile max of the visible scaled scores
-            float mx = -INFINITY;
-            uint32_t v[32];
-#pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-                tmem_ld32(tS + c4 * 32, v);
-                tmem_wait_ld();
+            if (tbase + BN > L) {
+                // this tile reaches the tree: ancestor mask (-inf where hidden)
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float x = __uint_as_float(v[c]) * sl2;
-                    if (masked_tile) {
-                        const long long t = tbase + c4 * 32 + c;
-                        const long long jj = t - L;
-                        const bool vis = t < L || (jj < p.N && ((anc >> (int)jj) & 1ull));
-                        x = vis ? x : -INFINITY;
-                    }
-                    mx = fmaxf(mx, x);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const uint32_t vis = visible_bits(tbase + 32 * c4 - L, anc);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        v[32 * c4 + c] = ((vis >> c) & 1u) ? v[32 * c4 + c] : 0xff800000u;
                 }
             }
+            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                m0 = fmaxf(m0, __uint_as_float(v[c]));
+                m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
+                m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
+                m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
+            }
+            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
             // lazy rescale: move the reference max only when it grows by > 2^8
             const bool need = mx > m_ref + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
@@ -316,45 +367,32 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                 if (it > 0) {
 #pragma unroll 1
                     for (int c4 = 0; c4 < 4; ++c4) {
-                        tmem_ld32(tO + c4 * 32, v);
+                        uint32_t o[32];
+                        tmem_ld32(tO + c4 * 32, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
-                        tmem_st32(tO + c4 * 32, v);
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st32(tO + c4 * 32, o);
                     }
                     tmem_wait_st();
                 }
             }
-            // pass 2: P = 2^(x - m_ref) as bf16 pairs into the first 64 S columns
-            const bool live = m_ref != -INFINITY;
-            float rs = 0.0f;
-            uint32_t pk[16];
-#pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-                tmem_ld32(tS + c4 * 32, v);
-                tmem_wait_ld();
+            // P = 2^(s*scale - m_ref), packed in place as bf16 pairs into the first 64 S columns
+            const float mneg = m_ref == -INFINITY ? 0.0f : -m_ref;
+            float r0 = 0.0f, r1 = 0.0f;
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float x0 = __uint_as_float(v[c]) * sl2;
-                    float x1 = __uint_as_float(v[c + 1]) * sl2;
-                    if (masked_tile) {
-                        const long long t = tbase + c4 * 32 + c;
-                        const long long j0t = t - L, j1t = t + 1 - L;
-                        const bool vis0 = t < L || (j0t < p.N && ((anc >> (int)j0t) & 1ull));
-                        const bool vis1 = t + 1 < L || (j1t < p.N && ((anc >> (int)j1t) & 1ull));
-                        x0 = vis0 ? x0 : -INFINITY;
-                        x1 = vis1 ? x1 : -INFINITY;
-                    }
-                    const float p0 = live ? ex2_approx(x0 - m_ref) : 0.0f;
-                    const float p1 = live ? ex2_approx(x1 - m_ref) : 0.0f;
-                    rs += p0 + p1;
-                    pk[c >> 1] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tS + c4 * 16, pk);  // 16 columns, over S columns already read
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * c]), sl2, mneg));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * c + 1]), sl2, mneg));
+                r0 += p0;
+                r1 += p1;
+                v[c] = pack_bf16x2(p0, p1);
             }
+            tmem_st32(tS, v);
+            tmem_st32(tS + 32, v + 32);
             tmem_wait_st();
-            l += rs;
+            l += r0 + r1;
             // V rows past the sequence end may hold anything: zero them before PV.
             if (h == 0 && tbase + BN > T) {
                 if (!(ok = warp_wait(&v_full[s], use & 1, abort_flag))) break;
@@ -379,61 +417,38 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
         const float lse_v =
             l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         const size_t row = ((size_t)b * p.N + node) * p.Hq + hq;
-        if (p.splits == 1) {
-            __nv_bfloat16 *op = p.out + row * HD;
-#pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t o[32];
-                if (j0 < j1 && ok) {
-                    tmem_ld32(tO + c4 * 32, o);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] = 0;
-                }
-                if (row_valid) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv,
-                                          __uint_as_float(o[8 * k + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv,
-                                          __uint_as_float(o[8 * k + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv,
-                                          __uint_as_float(o[8 * k + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv,
-                                          __uint_as_float(o[8 * k + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(op + c4 * 32 + 8 * k) = w;
-                    }
-                }
-            }
-            if (row_valid && p.lse) p.lse[row] = (j0 < j1) ? lse_v : 0.0f;
+        uint32_t o[128];
+        if (j0 < j1 && ok) {
+            tmem_ld32(tO, o);
+            tmem_ld32(tO + 32, o + 32);
+            tmem_ld32(tO + 64, o + 64);
+            tmem_ld32(tO + 96, o + 96);
+            tmem_wait_ld();
         } else {
-            float *op = p.part_o + ((size_t)split * p.B * p.N * p.Hq + row) * HD;
-#pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t o[32];
-                if (j0 < j1 && ok) {
-                    tmem_ld32(tO + c4 * 32, o);
-                    tmem_wait_ld();
-                } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] = 0;
-                }
-                if (row_valid) {
+            for (int c = 0; c < 128; ++c) o[c] = 0;
+        }
+        if (row_valid) {
+            if (p.splits == 1) {
+                uint4 *op = reinterpret_cast<uint4 *>(p.out + row * HD);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float4 w = make_float4(__uint_as_float(o[4 * k + 0]) * inv,
-                                               __uint_as_float(o[4 * k + 1]) * inv,
-                                               __uint_as_float(o[4 * k + 2]) * inv,
-                                               __uint_as_float(o[4 * k + 3]) * inv);
-                        *reinterpret_cast<float4 *>(op + c4 * 32 + 4 * k) = w;
-                    }
+                for (int k = 0; k < 16; ++k) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+                    op[k] = w;
                 }
+                if (p.lse) p.lse[row] = (j0 < j1) ? lse_v : 0.0f;
+            } else {
+                float4 *op = reinterpret_cast<float4 *>(p.part_o + ((size_t)split * p.B * p.N * p.Hq + row) * HD);
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    op[k] = make_float4(__uint_as_float(o[4 * k + 0]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                        __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                p.part_lse[(size_t)split * p.B * p.N * p.Hq + row] = (j0 < j1) ? lse_v : -INFINITY;
             }
-            if (row_valid)
-                p.part_lse[(size_t)split * p.B * p.N * p.Hq + row] =
-                    (j0 < j1) ? lse_v : -INFINITY;
         }
     }
 
@@ -460,8 +475,9 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
 }
 
 // Merge split partials: lse = log sum_s e^{lse_s}, out = sum_s e^{lse_s - lse} o_s.
-// One warp per (sequence, node, head) row; a sequence with any status bit set
-// gets zeros.
+// One warp per (sequence, node, head) row; lane s holds split s's lse (and
+// s + 32's), and the partial rows are loaded eight splits at a time so their
+// latencies overlap. A sequence with any status bit set gets zeros.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restrict__ part_o,
                                                            const float *__restrict__ part_lse,
                                                            int splits, long long rows, int per_b,
@@ -475,21 +491,32 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restri
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lse_out = 0.0f;
     if (status[b] == 0) {
-        float mx = -INFINITY;
-        for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[(size_t)s * rows + row]);
-        float wsum = 0.0f;
+        const float l0 = lane < splits ? part_lse[(size_t)lane * rows + row] : -INFINITY;
+        const float l1 = lane + 32 < splits ? part_lse[(size_t)(lane + 32) * rows + row] : -INFINITY;
+        const float mx = warp_max(fmaxf(l0, l1));
         if (mx != -INFINITY) {
-            for (int s = 0; s < splits; ++s) {
-                const float ls = part_lse[(size_t)s * rows + row];
-                if (ls == -INFINITY) continue;
-                const float w = expf(ls - mx);
-                wsum += w;
-                const float4 o =
-                    *reinterpret_cast<const float4 *>(part_o + ((size_t)s * rows + row) * 128 + lane * 4);
-                acc.x = fmaf(w, o.x, acc.x);
-                acc.y = fmaf(w, o.y, acc.y);
-                acc.z = fmaf(w, o.z, acc.z);
-                acc.w = fmaf(w, o.w, acc.w);
+            const float w0 = l0 == -INFINITY ? 0.0f : expf(l0 - mx);
+            const float w1 = l1 == -INFINITY ? 0.0f : expf(l1 - mx);
+            const float wsum = warp_sum(w0 + w1);
+            for (int s0 = 0; s0 < splits; s0 += 8) {
+                float4 o[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    o[k] = s0 + k < splits
+                               ? *reinterpret_cast<const float4 *>(
+                                     part_o + ((size_t)(s0 + k) * rows + row) * 128 + lane * 4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int sidx = s0 + k;
+                    const float wa = __shfl_sync(0xffffffffu, w0, sidx & 31);
+                    const float wb = __shfl_sync(0xffffffffu, w1, sidx & 31);
+                    const float w = sidx < 32 ? wa : wb;
+                    acc.x = fmaf(w, o[k].x, acc.x);
+                    acc.y = fmaf(w, o[k].y, acc.y);
+                    acc.z = fmaf(w, o[k].z, acc.z);
+                    acc.w = fmaf(w, o[k].w, acc.w);
+                }
             }
             const float inv = 1.0f / wsum;
             acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
@@ -529,6 +556,20 @@ static bool make_kv_map(CUtensorMap *map, const void *base, int num_pages, int p
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static bool make_q_map(CUtensorMap *map, const void *q, int B, int N, int Hq, int G) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)tc::HD, (cuuint64_t)Hq, (cuuint64_t)N, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)tc::HD * 2, (cuuint64_t)Hq * tc::HD * 2,
+                             (cuuint64_t)N * Hq * tc::HD * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -579,10 +620,17 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
     const size_t need = attn_tc_workspace_bytes(a.B, a.N, a.Hq, a.Hkv, a.max_pages, a.page_size);
     if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SVF_ERR_WORKSPACE;
 
-    CUtensorMap tmk, tmv;
+    CUtensorMap tmk, tmv, tmq;
     if (!make_kv_map(&tmk, a.k_cache, a.num_pages, a.page_size, a.Hkv) ||
         !make_kv_map(&tmv, a.v_cache, a.num_pages, a.page_size, a.Hkv))
         return SVF_ERR_LAUNCH;
+    // Q by TMA when a box of 128 rows is G heads x 128/G nodes
+    const bool q_tma = G <= 128 && (G & (G - 1)) == 0;
+    if (q_tma) {
+        if (!make_q_map(&tmq, a.q, a.B, a.N, a.Hq, G)) return SVF_ERR_LAUNCH;
+    } else {
+        memset(&tmq, 0, sizeof(tmq));
+    }
 
     TcParams p;
     p.q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
@@ -593,6 +641,7 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
     p.num_pages = a.num_pages; p.page_size = a.page_size; p.max_pages = a.max_pages;
     p.splits = splits;
     p.row_blocks = row_blocks;
+    p.q_tma = q_tma ? 1 : 0;
     const float scale = a.sm_scale > 0.0f ? a.sm_scale : 1.0f / sqrtf((float)a.D);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
@@ -612,11 +661,11 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
     if (NH == 1) {
         const int smem = TcSmem<1>::kDynamic;
         cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        attn_tc_kernel<1><<<grid, 64 + 128, smem, stream>>>(tmk, tmv, p);
+        attn_tc_kernel<1><<<grid, 64 + 128, smem, stream>>>(tmk, tmv, tmq, p);
     } else {
         const int smem = TcSmem<2>::kDynamic;
         cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        attn_tc_kernel<2><<<grid, 64 + 256, smem, stream>>>(tmk, tmv, p);
+        attn_tc_kernel<2><<<grid, 64 + 256, smem, stream>>>(tmk, tmv, tmq, p);
     }
     if (cudaGetLastError() != cudaSuccess) return SVF_ERR_LAUNCH;
     if (splits > 1) {
