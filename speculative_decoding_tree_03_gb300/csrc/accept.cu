@@ -287,11 +287,14 @@ __device__ double cluster_total(WalkShared &ws, double mine, int pass, double *b
     cluster.sync();
     double total = 0.0, before = 0.0;
     const unsigned me = cluster.block_rank();
+    double v[CL];
+#pragma unroll
+    for (int r = 0; r < CL; ++r) v[r] = *cluster.map_shared_rank(&ws.slot[slot], r);
+#pragma unroll
     for (int r = 0; r < CL; ++r) {
-        const double v = *cluster.map_shared_rank(&ws.slot[slot], r);
-        per_rank[r] = v;
-        if ((unsigned)r < me) before += v;
-        total += v;
+        per_rank[r] = v[r];
+        if ((unsigned)r < me) before += v[r];
+        total += v[r];
     }
     *before_me = before;
     return total;
@@ -358,23 +361,34 @@ __global__ void __launch_bounds__(NT) accept_walk_kernel(
     // probabilities under its parent's target and draft softmax
     for (int i = 1 + threadIdx.x; i < N; i += NT) sch[sp[i]] = 1;
     __syncthreads();
-    for (int j = threadIdx.x; j < N; j += NT) {
-        float m = -INFINITY, z = 0.0f;
-        for (int c = 0; c < nchunks; ++c) {
-            const float2 pc = part[(base + j) * nchunks + c];
-            ms_merge(m, z, pc.x, pc.y);
-        }
-        st_t[j] = make_float2(m * acc::kLog2e, z);
-        m = -INFINITY;
-        z = 1.0f;
-        if (sch[j]) {
-            z = 0.0f;
-            for (int c = 0; c < nchunks; ++c) {
-                const float2 pc = part[(rows + base + j) * nchunks + c];
-                ms_merge(m, z, pc.x, pc.y);
+    {
+        // one warp per row: lanes load chunks in parallel, a butterfly merges
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int j = warp; j < N; j += NT / 32) {
+            float mt = -INFINITY, zt = 0.0f, md = -INFINITY, zd = 0.0f;
+            const bool internal = sch[j] != 0;
+            for (int c = lane; c < nchunks; c += 32) {
+                const float2 a = part[(base + j) * nchunks + c];
+                ms_merge(mt, zt, a.x, a.y);
+                if (internal) {
+                    const float2 d = part[(rows + base + j) * nchunks + c];
+                    ms_merge(md, zd, d.x, d.y);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, mt, o);
+                const float z2 = __shfl_xor_sync(0xffffffffu, zt, o);
+                ms_merge(mt, zt, m2, z2);
+                const float m3 = __shfl_xor_sync(0xffffffffu, md, o);
+                const float z3 = __shfl_xor_sync(0xffffffffu, zd, o);
+                ms_merge(md, zd, m3, z3);
+            }
+            if (lane == 0) {
+                st_t[j] = make_float2(mt * acc::kLog2e, zt);
+                st_d[j] = internal ? make_float2(md * acc::kLog2e, zd) : make_float2(0.0f, 1.0f);
             }
         }
-        st_d[j] = make_float2(m == -INFINITY ? 0.0f : m * acc::kLog2e, z);
     }
     __syncthreads();
     for (int c = 1 + threadIdx.x; c < N; c += NT) {

@@ -36,11 +36,18 @@ namespace svf {
 namespace tc {
 constexpr int BN = 128;                  // KV tokens per tile
 constexpr int HD = 128;                  // head_dim
-constexpr int STAGES = 2;
+// Ring depths for K and V tiles (32 KB each). K frees as soon as the QK^T
+// that reads it completes, V only after its PV, so K runs further ahead. One
+// 128-row half (32 KB of Q) fits 3 + 3 stages; two halves (64 KB) 3 + 2.
+__host__ __device__ constexpr int kstages_for(int NH) { return 3; }
+__host__ __device__ constexpr int vstages_for(int NH) { return NH == 1 ? 3 : 2; }
+constexpr int CRING = 16;  // page coordinates kept for tiles ahead of the V ring
 constexpr int HALF_BYTES = 128 * HD * 2;  // 32 KB: 128 rows x 128 bf16
 constexpr int ATOM_COL_BYTES = 128 * 128;  // one 64-element column block of a 128-row tile
 constexpr int TILE_BYTES = BN * HD * 2;   // 32 KB per K or V tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int PREFETCH = 3;               // tiles pulled into L2 ahead of the smem ring
+constexpr int MAX_BOX_ROWS = 32;          // TMA box height (tokens) for large pages
 }  // namespace tc
 
 struct TcParams {
@@ -64,9 +71,11 @@ template <int NH>
 struct TcSmem {
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + NH * tc::HALF_BYTES;
-    static constexpr int kV = kK + tc::STAGES * tc::TILE_BYTES;
-    static constexpr int kBar = kV + tc::STAGES * tc::TILE_BYTES;
-    static constexpr int kNumBars = 3 * tc::STAGES + 3 * NH + 1;
+    static constexpr int kKS = tc::kstages_for(NH);
+    static constexpr int kVS = tc::vstages_for(NH);
+    static constexpr int kV = kK + kKS * tc::TILE_BYTES;
+    static constexpr int kBar = kV + kVS * tc::TILE_BYTES;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 3 * 2 + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kDynamic = kBytes + 1024;  // slack to align the base to 1 KB
@@ -96,6 +105,8 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                    const __grid_constant__ CUtensorMap tmq, TcParams p) {
     using S = TcSmem<NH>;
     using namespace tc;
+    constexpr int KS = S::kKS;
+    constexpr int VS = S::kVS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -104,17 +115,21 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
     uint8_t *sV = smem + S::kV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
     uint64_t *k_full = bars;
-    uint64_t *v_full = bars + STAGES;
-    uint64_t *kv_empty = bars + 2 * STAGES;
-    uint64_t *s_full = bars + 3 * STAGES;
-    uint64_t *p_full = s_full + NH;
-    uint64_t *o_done = p_full + NH;
-    uint64_t *q_full = o_done + NH;
+    uint64_t *k_empty = k_full + KS;
+    uint64_t *v_full = k_empty + KS;
+    uint64_t *v_empty = v_full + VS;
+    // S slots: the two row halves (NH = 2), or two buffers of one half (NH = 1)
+    uint64_t *s_full = v_empty + VS;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_done = p_full + 2;
+    uint64_t *q_full = o_done + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
     int *err_flag = reinterpret_cast<int *>(smem + S::kMisc + 8);
 
-    constexpr uint32_t kTmemCols = NH == 1 ? 256 : 512;
+    // tensor memory: S slot k at columns [128 k, 128 k + 128), O of half h at
+    // [256 + 128 h, ...); P is written over the first 64 columns of its S slot
+    constexpr uint32_t kTmemCols = 512;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int split = blockIdx.x;
@@ -130,61 +145,78 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
     const int j0 = split * chunk;
     const int j1 = min(j0 + chunk, ntiles);
 
-    // Page-table lookup of one tile: the starting slot of each of its boxes
-    // (a slot past the cache, zero-filled by TMA, for boxes past the sequence
-    // or with a page id outside the cache).
+    // Page-table lookup of one tile, one box per lane of the producer warp:
+    // the starting slot of box `lane` (a slot past the cache, zero-filled by
+    // TMA, for boxes past the sequence or with a page id outside the cache).
+    // Every index fits in 32 bits (num_pages * page_size <= INT_MAX).
     const int ps = p.page_size;
-    const int box_rows = ps < BN ? ps : BN;
+    const int box_rows = ps < MAX_BOX_ROWS ? ps : MAX_BOX_ROWS;
     const int boxes = BN / box_rows;
     const int oob = p.num_pages * ps;
-    const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
-    auto tile_coords = [&](int j, int *coord) {
-        for (int x = 0; x < boxes; ++x) {
-            const long long t0 = (long long)j * BN + (long long)x * box_rows;
-            int c = oob;
-            if (t0 < T) {
-                const int id = pt[t0 / ps];
-                if (id < 0 || id >= p.num_pages)
-                    *err_flag = 1;
-                else
-                    c = id * ps + (int)(t0 % ps);
+    const int Ti = (int)T;
+    const int32_t *__restrict__ pt = p.page_table + (size_t)b * p.max_pages;
+    auto lane_coord = [&](int j, int &bad) -> int {
+        if (lane >= boxes || j >= j1) return oob;
+        const int t0 = j * BN + lane * box_rows;
+        if (t0 >= Ti) return oob;
+        const int page = t0 / ps;
+        const int id = __ldg(pt + page);
+        if (id < 0 || id >= p.num_pages) {
+            bad = 1;
+            return oob;
+        }
+        return id * ps + (t0 - page * ps);
+    };
+    // Lane 0 issues the K (or V) boxes of one tile into one stage; lane x's
+    // coordinate is broadcast by shuffle (all lanes of warp 0 take part).
+    auto issue_boxes = [&](const CUtensorMap *map, uint8_t *dst, uint64_t *bar, int my_coord) {
+        int cs[BN / 16];
+        for (int x = 0; x < boxes; ++x) cs[x] = __shfl_sync(0xffffffffu, my_coord, x);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, TILE_BYTES);
+            for (int x = 0; x < boxes; ++x)
+                for (int dh = 0; dh < 2; ++dh)
+                    tma_load_3d(dst + dh * ATOM_COL_BYTES + x * box_rows * 128, map, dh * 64, g,
+                                cs[x], bar);
+        }
+    };
+    auto prefetch_coord = [&](int c) {
+        if (lane < boxes && c != oob) {
+            for (int dh = 0; dh < 2; ++dh) {
+                tma_prefetch_l2_3d(&tmk, dh * 64, g, c);
+                tma_prefetch_l2_3d(&tmv, dh * 64, g, c);
             }
-            coord[x] = c;
         }
     };
-    auto issue_tile = [&](int s, const int *coord) {
-        mbar_arrive_expect_tx(&k_full[s], TILE_BYTES);
-        for (int x = 0; x < boxes; ++x)
-            for (int dh = 0; dh < 2; ++dh)
-                tma_load_3d(sK + s * TILE_BYTES + dh * ATOM_COL_BYTES + x * box_rows * 128, &tmk,
-                            dh * 64, g, coord[x], &k_full[s]);
-        mbar_arrive_expect_tx(&v_full[s], TILE_BYTES);
-        for (int x = 0; x < boxes; ++x)
-            for (int dh = 0; dh < 2; ++dh)
-                tma_load_3d(sV + s * TILE_BYTES + dh * ATOM_COL_BYTES + x * box_rows * 128, &tmv,
-                            dh * 64, g, coord[x], &v_full[s]);
-    };
-
-    if (threadIdx.x == 0) {
-        int coord0[BN / 16];
-        *err_flag = 0;
-        if (j0 < j1) tile_coords(j0, coord0);
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
-        }
-        for (int h = 0; h < NH; ++h) {
-            mbar_init(&s_full[h], 1);
-            mbar_init(&p_full[h], 128);
-            mbar_init(&o_done[h], 1);
-        }
-        mbar_init(q_full, 1);
-        *abort_flag = 0;
-        mbar_fence_init();
-        if (!len_ok) atomicOr(&p.status[b], SVF_DEV_BAD_LENGTH);
-        if (j0 < j1) {
-            if (p.q_tma) {
+    // page coordinates of upcoming tiles, kept in a ring indexed by tile
+    int ring[CRING];
+    int bad_pages = 0;
+    int filled = j0;  // tiles [j0, filled) have their coordinates in the ring
+    if (warp == 0) {
+#pragma unroll
+        for (int k = 0; k <= PREFETCH; ++k) ring[(j0 + k) % CRING] = lane_coord(j0 + k, bad_pages);
+        filled = j0 + PREFETCH + 1;
+        const int bad0 = __reduce_or_sync(0xffffffffu, bad_pages);
+        if (lane == 0) {
+            *err_flag = bad0;
+            for (int s2 = 0; s2 < KS; ++s2) {
+                mbar_init(&k_full[s2], 1);
+                mbar_init(&k_empty[s2], 1);
+            }
+            for (int s2 = 0; s2 < VS; ++s2) {
+                mbar_init(&v_full[s2], 1);
+                mbar_init(&v_empty[s2], 1);
+            }
+            for (int k = 0; k < 2; ++k) {
+                mbar_init(&s_full[k], 1);
+                mbar_init(&p_full[k], 128);
+                mbar_init(&o_done[k], 1);
+            }
+            mbar_init(q_full, 1);
+            *abort_flag = 0;
+            mbar_fence_init();
+            if (!len_ok) atomicOr(&p.status[b], SVF_DEV_BAD_LENGTH);
+            if (j0 < j1 && p.q_tma) {
                 // rows (node, head) of this block: box = 64 dims x G heads x 128/G nodes
                 mbar_arrive_expect_tx(q_full, NH * HALF_BYTES);
                 const int nodes = 128 / p.G;
@@ -193,7 +225,14 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                         tma_load_4d(sQ + hh * HALF_BYTES + dh * ATOM_COL_BYTES, &tmq, dh * 64,
                                     g * p.G, (rb * NH + hh) * nodes, b, q_full);
             }
-            issue_tile(0, coord0);
+        }
+        __syncwarp();
+        if (j0 < j1) {
+            const int c0 = ring[j0 % CRING];
+            issue_boxes(&tmk, sK, &k_full[0], c0);
+            issue_boxes(&tmv, sV, &v_full[0], c0);
+#pragma unroll
+            for (int k = 1; k <= PREFETCH; ++k) prefetch_coord(ring[(j0 + k) % CRING]);
         }
     }
     if (warp == 1) {
@@ -235,25 +274,68 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
 
     if (j0 < j1 && warp == 0) {
         // ------------------------------------------------------------ producer
+        // K and V of every tile, each into its own ring as soon as a stage is
+        // free (polling both, K first), the page coordinates PREFETCH tiles
+        // ahead of the next K tile, and those tiles pulled into L2.
+        int kj = j0 + 1, vj = j0 + 1;  // next tiles to issue
+        int bad = bad_pages;
+        // one page-table load in flight: its coordinate is stored (and its
+        // boxes prefetched) at the next K issue, when the load has landed
+        int pending_tile = -1, pending = oob;
+        unsigned long long t_last = globaltimer_ns();
+        while ((kj < j1 || vj < j1) && !*abort_flag) {
+            bool progressed = false;
+            if (kj < j1) {
+                const int it = kj - j0, st = it % KS, use = it / KS;
+                bool free_ = use == 0 || mbar_test_wait(&k_empty[st], (use - 1) & 1);
+                free_ = __shfl_sync(0xffffffffu, free_, 0);
+                if (free_) {
+                    issue_boxes(&tmk, sK + st * TILE_BYTES, &k_full[st], ring[kj % CRING]);
+                    ++kj;
+                    if (pending_tile >= 0) {
+                        ring[pending_tile % CRING] = pending;
+                        prefetch_coord(pending);
+                    }
+                    pending_tile = filled;
+                    pending = lane_coord(filled, bad);
+                    ++filled;
+                    progressed = true;
+                }
+            }
+            if (vj < kj && vj < j1) {
+                const int it = vj - j0, st = it % VS, use = it / VS;
+                bool free_ = use == 0 || mbar_test_wait(&v_empty[st], (use - 1) & 1);
+                free_ = __shfl_sync(0xffffffffu, free_, 0);
+                if (free_) {
+                    issue_boxes(&tmv, sV + st * TILE_BYTES, &v_full[st], ring[vj % CRING]);
+                    ++vj;
+                    progressed = true;
+                }
+            }
+            if (progressed) {
+                t_last = globaltimer_ns();
+            } else {
+                __nanosleep(64);
+                if (globaltimer_ns() - t_last > kWaitDeadlineNs) {
+                    if (lane == 0) *abort_flag = 1;
+                    break;
+                }
+            }
+        }
+        bad = __reduce_or_sync(0xffffffffu, bad);
         if (lane == 0) {
-            int issued = 1;  // tile j0 went out during setup
-            for (int j = j0 + 1; j < j1; ++j) {
-                const int it = j - j0, s = it % STAGES, use = it / STAGES;
-                int coord[BN / 16];
-                tile_coords(j, coord);
-                if (use > 0 && !mbar_wait(&kv_empty[s], (use - 1) & 1, abort_flag)) break;
-                issue_tile(s, coord);
-                ++issued;
+            if (bad || *err_flag) {
+                *err_flag = 1;
+                atomicOr(&p.status[b], SVF_DEV_BAD_PAGE);
             }
-            if (*err_flag) atomicOr(&p.status[b], SVF_DEV_BAD_PAGE);
             // Never leave with copies in flight: wait (bounded, ignoring the
-            // abort flag) for the last use of every stage.
+            // abort flag) for the last use of every stage that was loaded.
             volatile int never = 0;
-            for (int s = 0; s < STAGES && s < issued; ++s) {
-                const int last_use = (issued - 1 - s) / STAGES;
-                mbar_wait(&k_full[s], last_use & 1, &never);
-                mbar_wait(&v_full[s], last_use & 1, &never);
-            }
+            const int nk = kj - j0, nv = vj - j0;
+            for (int st = 0; st < KS && st < nk; ++st)
+                mbar_wait(&k_full[st], ((nk - 1 - st) / KS) & 1, &never);
+            for (int st = 0; st < VS && st < nv; ++st)
+                mbar_wait(&v_full[st], ((nv - 1 - st) / VS) & 1, &never);
             if (p.q_tma) mbar_wait(q_full, 0, &never);
         }
     } else if (j0 < j1 && warp == 1) {
@@ -262,50 +344,90 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-            auto issue_qk = [&](int s, int h) {
-                const uint32_t d = tmem + h * 128;
+            // S_slot = Q_h K^T
+            auto issue_qk = [&](int stage, int h, int slot) {
+                const uint32_t d = tmem + slot * 128;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * ATOM_COL_BYTES + (kk & 3) * 32;
                     umma_ss(d, smem_desc_sw128(aQ + h * HALF_BYTES + off, 16, 1024),
-                            smem_desc_sw128(aK + s * TILE_BYTES + off, 16, 1024), idesc_qk,
+                            smem_desc_sw128(aK + stage * TILE_BYTES + off, 16, 1024), idesc_qk,
                             kk > 0);
                 }
-                umma_commit(&s_full[h]);
+                umma_commit(&s_full[slot]);
             };
-            auto issue_pv = [&](int s, int h, bool first) {
-                const uint32_t d = tmem + NH * 128 + h * 128;
-                const uint32_t a = tmem + h * 128;
+            // O_h += P_slot V
+            auto issue_pv = [&](int stage, int h, int slot, bool first) {
+                const uint32_t d = tmem + 256 + h * 128;
+                const uint32_t a = tmem + slot * 128;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     umma_ts(d, a + kk * 8,
-                            smem_desc_sw128(aV + s * TILE_BYTES + kk * 2048, ATOM_COL_BYTES, 1024),
+                            smem_desc_sw128(aV + stage * TILE_BYTES + kk * 2048, ATOM_COL_BYTES,
+                                            1024),
                             idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                umma_commit(&o_done[h]);
+                umma_commit(&o_done[slot]);
             };
+            auto kst = [&](int it) { return it % KS; };
+            auto kph = [&](int it) { return (uint32_t)((it / KS) & 1); };
+            auto vst = [&](int it) { return it % VS; };
+            auto vph = [&](int it) { return (uint32_t)((it / VS) & 1); };
             bool ok = !p.q_tma || mbar_wait(q_full, 0, abort_flag);
-            ok = ok && mbar_wait(&k_full[0], 0, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                for (int h = 0; h < NH; ++h) issue_qk(0, h);
-            }
-            for (int j = j0; ok && j < j1; ++j) {
-                const int it = j - j0, s = it % STAGES, use = it / STAGES;
-                if (!(ok = mbar_wait(&v_full[s], use & 1, abort_flag))) break;
-                for (int h = 0; h < NH && ok; ++h) {
-                    if (!(ok = mbar_wait(&p_full[h], it & 1, abort_flag))) break;
+            if (NH == 2) {
+                // Ping-pong: PV(h0, j), QK(h0, j+1), PV(h1, j), QK(h1, j+1), so
+                // one half's softmax overlaps the other half's MMAs. A slot's S
+                // (and the P written over it) is reused only after its PV is done.
+                ok = ok && mbar_wait(&k_full[kst(0)], kph(0), abort_flag);
+                if (ok) {
                     tc_fence_after();
-                    issue_pv(s, h, it == 0);
+                    issue_qk(kst(0), 0, 0);
+                    issue_qk(kst(0), 1, 1);
+                    umma_commit(&k_empty[kst(0)]);
                 }
-                if (!ok) break;
-                umma_commit(&kv_empty[s]);
-                if (j + 1 < j1) {
-                    const int s1 = (it + 1) % STAGES, use1 = (it + 1) / STAGES;
-                    if (!(ok = mbar_wait(&k_full[s1], use1 & 1, abort_flag))) break;
-                    for (int h = 0; h < NH && ok; ++h) {
-                        if (!(ok = mbar_wait(&o_done[h], it & 1, abort_flag))) break;
+                for (int j = j0; ok && j < j1; ++j) {
+                    const int it = j - j0;
+                    const bool more = j + 1 < j1;
+                    if (!(ok = mbar_wait(&v_full[vst(it)], vph(it), abort_flag))) break;
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        if (!(ok = mbar_wait(&p_full[h], it & 1, abort_flag))) break;
                         tc_fence_after();
-                        issue_qk(s1, h);
+                        issue_pv(vst(it), h, h, it == 0);
+                        if (h == 1) umma_commit(&v_empty[vst(it)]);
+                        if (more) {
+                            if (h == 0 &&
+                                !(ok = mbar_wait(&k_full[kst(it + 1)], kph(it + 1), abort_flag)))
+                                break;
+                            if (!(ok = mbar_wait(&o_done[h], it & 1, abort_flag))) break;
+                            tc_fence_after();
+                            issue_qk(kst(it + 1), h, h);
+                            if (h == 1) umma_commit(&k_empty[kst(it + 1)]);
+                        }
+                    }
+                }
+            } else {
+                // One half, S double-buffered: QK(j + 2) goes into the slot PV(j)
+                // has just finished reading, while the softmax works on tile j + 1.
+                for (int k = 0; k < 2 && ok && j0 + k < j1; ++k) {
+                    if (!(ok = mbar_wait(&k_full[kst(k)], kph(k), abort_flag))) break;
+                    tc_fence_after();
+                    issue_qk(kst(k), 0, k);
+                    umma_commit(&k_empty[kst(k)]);
+                }
+                for (int j = j0; ok && j < j1; ++j) {
+                    const int it = j - j0, slot = it & 1;
+                    const uint32_t sph = (uint32_t)((it >> 1) & 1);
+                    if (!(ok = mbar_wait(&v_full[vst(it)], vph(it), abort_flag))) break;
+                    if (!(ok = mbar_wait(&p_full[slot], sph, abort_flag))) break;
+                    tc_fence_after();
+                    issue_pv(vst(it), 0, slot, it == 0);
+                    umma_commit(&v_empty[vst(it)]);
+                    if (j + 2 < j1) {
+                        if (!(ok = mbar_wait(&k_full[kst(it + 2)], kph(it + 2), abort_flag)))
+                            break;
+                        if (!(ok = mbar_wait(&o_done[slot], sph, abort_flag))) break;
+                        tc_fence_after();
+                        issue_qk(kst(it + 2), 0, slot);
+                        umma_commit(&k_empty[kst(it + 2)]);
                     }
                 }
             }
@@ -321,39 +443,44 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
         const int hq = g * p.G + (row_valid ? R % p.G : 0);
         const uint64_t anc = row_valid ? p.anc[(size_t)b * p.N + node] : 0ull;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off + h * 128;
-        const uint32_t tO = tmem + lane_off + NH * 128 + h * 128;
+        const uint32_t tO = tmem + lane_off + 256 + h * 128;
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = j0; j < j1; ++j) {
-            const int it = j - j0, s = it % STAGES, use = it / STAGES;
-            if (!(ok = warp_wait(&s_full[h], it & 1, abort_flag))) break;
+            const int it = j - j0, s = it % VS, use = it / VS;
+            // S slot of this tile and the parity of its barriers
+            const int slot = NH == 2 ? h : (it & 1);
+            const uint32_t sph = NH == 2 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
+            const uint32_t tS = tmem + lane_off + slot * 128;
+            if (!(ok = warp_wait(&s_full[slot], sph, abort_flag))) break;
             tc_fence_after();
-            uint32_t v[128];
-            tmem_ld32(tS, v);
-            tmem_ld32(tS + 32, v + 32);
-            tmem_ld32(tS + 64, v + 64);
-            tmem_ld32(tS + 96, v + 96);
-            tmem_wait_ld();
             const long long tbase = (long long)j * BN;
-            if (tbase + BN > L) {
-                // this tile reaches the tree: ancestor mask (-inf where hidden)
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const uint32_t vis = visible_bits(tbase + 32 * c4 - L, anc);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        v[32 * c4 + c] = ((vis >> c) & 1u) ? v[32 * c4 + c] : 0xff800000u;
-                }
-            }
+            const bool masked_tile = tbase + BN > L;  // this tile reaches the tree
+            // pass 1: row max of the visible scores, two 64-column halves
             float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll 1
+            for (int c64 = 0; c64 < 2; ++c64) {
+                uint32_t v[64];
+                tmem_ld32(tS + c64 * 64, v);
+                tmem_ld32(tS + c64 * 64 + 32, v + 32);
+                tmem_wait_ld();
+                if (masked_tile) {
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                m0 = fmaxf(m0, __uint_as_float(v[c]));
-                m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
-                m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
-                m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const uint32_t vis = visible_bits(tbase + 64 * c64 + 32 * c2 - L, anc);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            v[32 * c2 + c] = ((vis >> c) & 1u) ? v[32 * c2 + c] : 0xff800000u;
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 64; c += 4) {
+                    m0 = fmaxf(m0, __uint_as_float(v[c]));
+                    m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
+                    m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
+                    m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
+                }
             }
             const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
             // lazy rescale: move the reference max only when it grows by > 2^8
@@ -365,6 +492,14 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                     m_ref = mx;
                 }
                 if (it > 0) {
+                    if (NH == 1) {
+                        // O is being accumulated by PV(j - 1) on the other slot
+                        const int pit = it - 1;
+                        if (!(ok = warp_wait(&o_done[pit & 1], (uint32_t)((pit >> 1) & 1),
+                                             abort_flag)))
+                            break;
+                        tc_fence_after();
+                    }
 #pragma unroll 1
                     for (int c4 = 0; c4 < 4; ++c4) {
                         uint32_t o[32];
@@ -378,19 +513,36 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                     tmem_wait_st();
                 }
             }
-            // P = 2^(s*scale - m_ref), packed in place as bf16 pairs into the first 64 S columns
+            // pass 2: P = 2^(s*scale - m_ref) as bf16 pairs; the 32 packed
+            // columns of half c64 go over S columns [32 c64, 32 c64 + 32),
+            // which pass 2 has already read
             const float mneg = m_ref == -INFINITY ? 0.0f : -m_ref;
             float r0 = 0.0f, r1 = 0.0f;
+#pragma unroll 1
+            for (int c64 = 0; c64 < 2; ++c64) {
+                uint32_t v[64];
+                tmem_ld32(tS + c64 * 64, v);
+                tmem_ld32(tS + c64 * 64 + 32, v + 32);
+                tmem_wait_ld();
+                if (masked_tile) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * c]), sl2, mneg));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * c + 1]), sl2, mneg));
-                r0 += p0;
-                r1 += p1;
-                v[c] = pack_bf16x2(p0, p1);
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const uint32_t vis = visible_bits(tbase + 64 * c64 + 32 * c2 - L, anc);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            v[32 * c2 + c] = ((vis >> c) & 1u) ? v[32 * c2 + c] : 0xff800000u;
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * c]), sl2, mneg));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * c + 1]), sl2, mneg));
+                    r0 += p0;
+                    r1 += p1;
+                    v[c] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + c64 * 32, v);
             }
-            tmem_st32(tS, v);
-            tmem_st32(tS + 32, v + 32);
             tmem_wait_st();
             l += r0 + r1;
             // V rows past the sequence end may hold anything: zero them before PV.
@@ -408,45 +560,56 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                 fence_proxy_async_smem();
             }
             tc_fence_before();
-            mbar_arrive(&p_full[h]);
+            mbar_arrive(&p_full[slot]);
         }
         // epilogue
-        if (ok && j0 < j1) ok = warp_wait(&o_done[h], (j1 - j0 - 1) & 1, abort_flag);
+        if (ok && j0 < j1) {
+            const int lit = j1 - j0 - 1;  // the last PV of this half
+            ok = NH == 2 ? warp_wait(&o_done[h], (uint32_t)(lit & 1), abort_flag)
+                         : warp_wait(&o_done[lit & 1], (uint32_t)((lit >> 1) & 1), abort_flag);
+        }
         tc_fence_after();
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const float lse_v =
             l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         const size_t row = ((size_t)b * p.N + node) * p.Hq + hq;
-        uint32_t o[128];
-        if (j0 < j1 && ok) {
-            tmem_ld32(tO, o);
-            tmem_ld32(tO + 32, o + 32);
-            tmem_ld32(tO + 64, o + 64);
-            tmem_ld32(tO + 96, o + 96);
-            tmem_wait_ld();
-        } else {
+#pragma unroll 1
+        for (int c64 = 0; c64 < 2; ++c64) {
+            uint32_t o[64];
+            if (j0 < j1 && ok) {
+                tmem_ld32(tO + c64 * 64, o);
+                tmem_ld32(tO + c64 * 64 + 32, o + 32);
+                tmem_wait_ld();
+            } else {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) o[c] = 0;
+                for (int c = 0; c < 64; ++c) o[c] = 0;
+            }
+            if (row_valid) {
+                if (p.splits == 1) {
+                    uint4 *op = reinterpret_cast<uint4 *>(p.out + row * HD + c64 * 64);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+                        op[k] = w;
+                    }
+                } else {
+                    float4 *op = reinterpret_cast<float4 *>(
+                        p.part_o + ((size_t)split * p.B * p.N * p.Hq + row) * HD + c64 * 64);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        op[k] = make_float4(__uint_as_float(o[4 * k + 0]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                            __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                }
+            }
         }
         if (row_valid) {
             if (p.splits == 1) {
-                uint4 *op = reinterpret_cast<uint4 *>(p.out + row * HD);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
-                    op[k] = w;
-                }
                 if (p.lse) p.lse[row] = (j0 < j1) ? lse_v : 0.0f;
             } else {
-                float4 *op = reinterpret_cast<float4 *>(p.part_o + ((size_t)split * p.B * p.N * p.Hq + row) * HD);
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    op[k] = make_float4(__uint_as_float(o[4 * k + 0]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                        __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
                 p.part_lse[(size_t)split * p.B * p.N * p.Hq + row] = (j0 < j1) ? lse_v : -INFINITY;
             }
         }
@@ -548,7 +711,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 static bool make_kv_map(CUtensorMap *map, const void *base, int num_pages, int page_size, int Hkv) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const int box_rows = page_size < tc::BN ? page_size : tc::BN;
+    const int box_rows = page_size < tc::MAX_BOX_ROWS ? page_size : tc::MAX_BOX_ROWS;
     cuuint64_t dims[3] = {(cuuint64_t)tc::HD, (cuuint64_t)Hkv,
                           (cuuint64_t)num_pages * (cuuint64_t)page_size};
     cuuint64_t strides[2] = {(cuuint64_t)tc::HD * 2, (cuuint64_t)Hkv * tc::HD * 2};
