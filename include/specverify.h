@@ -56,7 +56,8 @@ enum svf_status {
     SVF_ERR_ARG = -1,         /* null pointer, negative size, bad alignment */
     SVF_ERR_UNSUPPORTED = -2, /* sizes outside the limits stated per call */
     SVF_ERR_LAUNCH = -3,      /* a CUDA launch or driver call failed */
-    SVF_ERR_WORKSPACE = -4    /* workspace missing or smaller than required */
+    SVF_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
+    SVF_ERR_SCRATCH_LIMIT = -5 /* request larger than svf_spec_accept_noalloc's fixed scratch */
 };
 
 /* Device-side status bits, OR-ed into status[b]. */
@@ -176,6 +177,40 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
                     int N, int V, int32_t *accept_len, int32_t *path, int32_t *out_tokens,
                     float *ratio, void *workspace, size_t workspace_bytes, int32_t *status,
                     svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * svf_spec_accept_noalloc -- svf_spec_accept for callers that cannot provide
+ * device scratch memory.
+ *
+ * The pages have no counterpart to this call. It is here for users of the
+ * library who have no way to allocate device memory where they run the
+ * acceptance step: an inference runtime that gives a plugin only its input
+ * and output buffers, or a serving loop that reserved all device memory at
+ * start-up and must not allocate (or risk an allocation's implicit
+ * synchronisation) afterwards.
+ *
+ * Arguments, layouts, results and status bits are those of svf_spec_accept,
+ * without the workspace. The kernels' scratch lives instead in one 4 MiB
+ * array that the library itself defines in device memory; every GPU that
+ * loads the library holds it until the process exits. The call allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *   - Limits: those of svf_spec_accept, and a request whose scratch
+ *     (svf_spec_accept_workspace_size(B, N, V)) exceeds 4 MiB returns
+ *     SVF_ERR_SCRATCH_LIMIT without launching anything.
+ *   - The first call on a device looks up that array's device address (once
+ *     per device, with the device current). Make that first call before any
+ *     stream capture begins.
+ *   - Every call shares the one array. Calls that overlap on the GPU (on
+ *     different streams, or from different host threads without ordering)
+ *     race on it and corrupt each other's results; order them. Nothing in
+ *     the array needs to start at zero: each call writes every entry it
+ *     reads.
+ * ---------------------------------------------------------------------- */
+int svf_spec_accept_noalloc(const float *target_logits, const float *draft_logits,
+                            const int32_t *tokens, const int32_t *parent, const float *u_accept,
+                            const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                            int32_t *path, int32_t *out_tokens, float *ratio, int32_t *status,
+                            svf_stream_t stream);
 
 /* Human-readable name of a host return code or of one device status bit. */
 const char *svf_status_string(int code);

@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libspecverify.so")
 
 SVF_F32, SVF_BF16 = 0, 1
 SVF_OK, SVF_ERR_ARG, SVF_ERR_UNSUPPORTED, SVF_ERR_LAUNCH, SVF_ERR_WORKSPACE = 0, -1, -2, -3, -4
+SVF_ERR_SCRATCH_LIMIT = -5
 SVF_DEV_BAD_PARENT, SVF_DEV_BAD_TOKEN, SVF_DEV_BAD_PAGE, SVF_DEV_BAD_LENGTH, SVF_DEV_TIMEOUT = (
     1, 2, 4, 8, 16)
 
@@ -35,6 +36,7 @@ EXPORTED = [
     "svf_tree_verify_attn",
     "svf_spec_accept_workspace_size",
     "svf_spec_accept",
+    "svf_spec_accept_noalloc",
     "svf_status_string",
     "svf_version",
 ]
@@ -67,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_spec_accept_workspace_size.restype = Z
     lib.svf_spec_accept.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, Z, P, P]
     lib.svf_spec_accept.restype = I
+    lib.svf_spec_accept_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.svf_spec_accept_noalloc.restype = I
     lib.svf_status_string.argtypes = [I]
     lib.svf_status_string.restype = ctypes.c_char_p
     lib.svf_version.argtypes = []

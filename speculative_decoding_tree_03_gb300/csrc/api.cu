@@ -44,6 +44,7 @@ const char *svf_status_string(int code) {
         case SVF_ERR_UNSUPPORTED: return "unsupported size or dtype";
         case SVF_ERR_LAUNCH: return "CUDA launch or driver call failed";
         case SVF_ERR_WORKSPACE: return "workspace missing or too small";
+        case SVF_ERR_SCRATCH_LIMIT: return "request exceeds the fixed 4 MiB scratch of the allocation-free call";
         case SVF_DEV_BAD_PARENT: return "device: parent[] is not a BFS-flattened tree";
         case SVF_DEV_BAD_TOKEN: return "device: draft token outside the vocabulary";
         case SVF_DEV_BAD_PAGE: return "device: page id outside the cache";
