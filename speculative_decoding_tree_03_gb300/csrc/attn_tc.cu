@@ -36,11 +36,12 @@ namespace svf {
 namespace tc {
 constexpr int BN = 128;                  // KV tokens per tile
 constexpr int HD = 128;                  // head_dim
-// Ring depths for K and V tiles (32 KB each). K frees as soon as the QK^T
-// that reads it completes, V only after its PV, so K runs further ahead. One
-// 128-row half (32 KB of Q) fits 3 + 3 stages; two halves (64 KB) 3 + 2.
-__host__ __device__ constexpr int kstages_for(int NH) { return 3; }
-__host__ __device__ constexpr int vstages_for(int NH) { return NH == 1 ? 3 : 2; }
+// Ring depths for K and V tiles (32 KB each). One 128-row half (32 KB of Q)
+// fits 3 + 3 stages; two halves (64 KB of Q) fit 5 stages. There K frees as
+// soon as the QK^T that reads it completes, early enough for 2 stages, while
+// V waits for its PV, the last use of a tile, and gets the third stage.
+__host__ __device__ constexpr int kstages_for(int NH) { return NH == 1 ? 3 : 2; }
+__host__ __device__ constexpr int vstages_for(int NH) { return 3; }
 constexpr int CRING = 16;  // page coordinates kept for tiles ahead of the V ring
 constexpr int HALF_BYTES = 128 * HD * 2;  // 32 KB: 128 rows x 128 bf16
 constexpr int ATOM_COL_BYTES = 128 * 128;  // one 64-element column block of a 128-row tile
