@@ -165,7 +165,11 @@ int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache
  *   out_tokens [B, N] int32   out: accepted draft tokens, the bonus, then -1
  *   ratio      [B, N] float32 out, may be NULL: p~(x)/q_j(x) for every tested
  *                             node, NaN for nodes never tested
- *   workspace  at least svf_spec_accept_workspace_size(B, N, V) bytes
+ *   workspace  at least svf_spec_accept_workspace_size(B, N, V) bytes; that
+ *              size is 0 (workspace may be NULL) for V <= 262144, whose
+ *              rows the walk holds on chip. Larger vocabularies stream
+ *              their rows from memory after a statistics pre-pass that
+ *              keeps per-(row, chunk) results in the workspace.
  *   status     [B] int32      out: SVF_DEV_BAD_PARENT, SVF_DEV_BAD_TOKEN; a
  *                             bad sequence gets accept_len 0 and -1 in path
  *                             and out_tokens (ratio NaN).
@@ -190,9 +194,10 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
  * synchronisation) afterwards.
  *
  * Arguments, layouts, results and status bits are those of svf_spec_accept,
- * without the workspace. The kernels' scratch lives instead in one 4 MiB
- * array that the library itself defines in device memory; every GPU that
- * loads the library holds it until the process exits. The call allocates
+ * without the workspace. Vocabularies up to 262144 need no scratch at all;
+ * for larger ones the streaming kernels' scratch lives in one 4 MiB array
+ * that the library itself defines in device memory; every GPU that loads
+ * the library holds it until the process exits. The call allocates
  * nothing: no cudaMalloc, cudaFree or allocating library routine.
  *   - Limits: those of svf_spec_accept, and a request whose scratch
  *     (svf_spec_accept_workspace_size(B, N, V)) exceeds 4 MiB returns

@@ -9,31 +9,31 @@
 // accepted path is the longest accepted prefix; the bonus token is drawn at
 // the last node.
 //
-// Two kernels:
-//   accept_rowstats  streams every logits row the walk may touch once: the
-//                    target row of every node, the draft row of every node
-//                    with children. Per (row, chunk): max m and
-//                    Z = sum 2^((l - m) log2 e).
-//   accept_walk      one cluster of CTAs (or one warp for small
-//                    vocabularies) per sequence; each CTA owns a slice of the
-//                    vocabulary. A prologue gathers every child's p_parent(x),
-//                    q_parent(x) and uniform into shared memory, so every
-//                    decision is taken (identically, by every thread) from
-//                    shared memory. A rejection needs the mass of the new
-//                    residual, one pass over the parent's two rows; the CTAs
-//                    of the cluster add their slices and exchange the totals
-//                    through distributed shared memory. The residual after k
-//                    rejections is kept in closed form, p~ = max(0, p - c q)/S
-//                    with c_0 = 0, S_0 = 1, c_{k+1} = c_k + S_k and
-//                    S_{k+1} = sum_v max(0, p_v - c_{k+1} q_v): subtracting q
-//                    from max(0, p - c q)/S and renormalising gives exactly
-//                    that form. The bonus token is an inverse-CDF search: the
-//                    cluster's slice totals, then 128-element group sums of
-//                    the crossing slice, then the crossing inside one group.
-// Element probabilities are 2^(l log2 e - m log2 e) / Z: one FFMA and one
-// ex2.approx per element. Group sums are fp32; prefixes over groups, slices
-// and residual masses are fp64.
+// One kernel, one sequence per CTA cluster (or per CTA for small
+// vocabularies). The walk only ever needs the two logits rows of the nodes it
+// visits, so those are the only rows it reads: every CTA of the cluster owns
+// a fixed slice of the vocabulary and holds its slice of the current node's
+// target and draft rows in registers, as 128-element groups (one float4 per
+// lane per group). Per visited node:
+//   1. load the node's two rows (the draft row only if the node has
+//      children) into registers, and ask L2 for the first child's rows;
+//   2. softmax statistics: per-thread (max, sum e^(l - max)) pairs, merged
+//      over the warp, the CTA and (through distributed shared memory, in rank
+//      order) the cluster, so that every CTA holds identical (m, Z) values;
+//   3. scale the registers to probabilities p_v and q_v;
+//   4. test the children in ascending index order from scalars gathered at
+//      kernel start; a rejection needs the mass of the next residual, a
+//      register-only pass over the slice plus one cluster exchange.
+// The residual after k rejections is kept in closed form,
+// p~ = max(0, p - c q)/S with c_0 = 0, S_0 = 1, c_{k+1} = c_k + S_k and
+// S_{k+1} = sum_v max(0, p_v - c_{k+1} q_v): subtracting q from
+// max(0, p - c q)/S and renormalising gives exactly that form. The bonus token
+// is an inverse-CDF search: rank totals, then 128-element group sums of the
+// crossing slice, then the crossing inside one group, found by the warp whose
+// registers hold it. Group sums are fp32; prefixes over groups, slices and
+// residual masses are fp64.
 #include <cooperative_groups.h>
+#include <limits.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -44,18 +44,18 @@ namespace cg = cooperative_groups;
 namespace svf {
 
 namespace acc {
-constexpr int kSmallV = 2048;      // at or below: one warp per row / per sequence
-constexpr int kCluster = 8;        // CTAs per sequence above that
-constexpr int kWalkThreads = 512;  // threads per walk CTA above that
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxCluster = 16;
+constexpr int kLargeThreads = 512;  // threads per CTA of the clustered variants
 }  // namespace acc
 
-// 2^(l log2 e - ml2) with ml2 = m log2 e: e^(l - m) in one FFMA and one MUFU op.
+// 2^(l log2 e - ml2): e^(l - m) for ml2 = m log2 e, in one FFMA and one MUFU op.
 __device__ __forceinline__ float e2(float l, float ml2) {
     return ex2_approx(fmaf(l, acc::kLog2e, -ml2));
 }
 
-// Online (max, sum 2^((x - max) log2 e)) pair merge.
+// Online (max, sum e^(x - max)) pair merge. Symmetric in its two operands, so
+// butterfly reductions leave the same value in every lane.
 __device__ __forceinline__ void ms_merge(float &m, float &s, float m2, float s2) {
     if (m2 == -INFINITY) return;
     if (m == -INFINITY) {
@@ -71,264 +71,173 @@ __device__ __forceinline__ void ms_merge(float &m, float &s, float m2, float s2)
     }
 }
 
-__device__ __forceinline__ void ms_add4(float &m, float &s, float4 x) {
-    const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-    if (mx > m) {
-        s = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - mx) * acc::kLog2e);
-        m = mx;
-    }
-    const float ml2 = m * acc::kLog2e;
-    s += (e2(x.x, ml2) + e2(x.y, ml2)) + (e2(x.z, ml2) + e2(x.w, ml2));
+__device__ __forceinline__ float4 neg_inf4() {
+    return make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 }
 
-__device__ __forceinline__ void ms_add(float &m, float &s, float x) {
-    ms_add4(m, s, make_float4(x, -INFINITY, -INFINITY, -INFINITY));
-}
-
-// Does node j of sequence b have a child?  (parent[] in global memory)
-__device__ __forceinline__ bool has_child_lane(const int32_t *par, int N, int j, int lane,
-                                               int width) {
-    int hit = 0;
-    for (int c = j + 1 + lane; c < N; c += width) hit |= (par[c] == j);
-    return hit != 0;
-}
-
-// Row statistics. One warp per row (small V) or one block per chunk of a row
-// (large V; a row splits into `nchunks` chunks of `chunk` elements so that
-// small batches still fill the GPU). part[kind][row][chunk] = (m, Z) over
-// that chunk; kind 0 = target, 1 = draft (rows of leaves are skipped).
-template <bool WARP_PER_ROW>
-__global__ void __launch_bounds__(256) accept_rowstats_kernel(const float *__restrict__ target,
-                                                              const float *__restrict__ draft,
-                                                              const int32_t *__restrict__ parent,
-                                                              int B, int N, int V, int nchunks,
-                                                              int chunk,
-                                                              float2 *__restrict__ part) {
-    const int kind = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const long long rows = (long long)B * N;
-    long long r;
-    int tid, width, c = 0, beg = 0, end = V;
-    if (WARP_PER_ROW) {
-        r = (long long)blockIdx.x * 8 + warp;
-        tid = lane;
-        width = 32;
-        if (r >= rows) return;
-    } else {
-        r = blockIdx.x / nchunks;
-        c = blockIdx.x % nchunks;
-        beg = c * chunk;
-        end = min(V, beg + chunk);
-        tid = threadIdx.x;
-        width = blockDim.x;
-    }
-    const int b = (int)(r / N), j = (int)(r % N);
-    if (kind == 1) {
-        bool hc;
-        if (WARP_PER_ROW) {
-            hc = __any_sync(0xffffffffu, has_child_lane(parent + (size_t)b * N, N, j, lane, 32));
+// This warp's slice of one logits row: group k covers elements
+// [128 (g0 + k), 128 (g0 + k) + 128), lane l holds elements 4l .. 4l + 3 of
+// it; elements past V read as -inf.
+template <int E4, bool VEC>
+__device__ __forceinline__ void load_slice(const float *__restrict__ row, int V, int g0, int lane,
+                                           float4 (&x)[E4]) {
+#pragma unroll
+    for (int k = 0; k < E4; ++k) {
+        const int v0 = (g0 + k) * 128 + lane * 4;
+        if (VEC) {
+            x[k] = v0 < V ? __ldg(reinterpret_cast<const float4 *>(row + v0)) : neg_inf4();
         } else {
-            hc = __syncthreads_or(has_child_lane(parent + (size_t)b * N, N, j, tid, width));
+            x[k].x = v0 + 0 < V ? __ldg(row + v0 + 0) : -INFINITY;
+            x[k].y = v0 + 1 < V ? __ldg(row + v0 + 1) : -INFINITY;
+            x[k].z = v0 + 2 < V ? __ldg(row + v0 + 2) : -INFINITY;
+            x[k].w = v0 + 3 < V ? __ldg(row + v0 + 3) : -INFINITY;
         }
-        if (!hc) return;
-    }
-    const float *row = (kind == 0 ? target : draft) + (size_t)r * V;
-    float m = -INFINITY, s = 0.0f;
-    if ((V & 3) == 0) {
-        const float4 *row4 = reinterpret_cast<const float4 *>(row);
-        const int e4 = end >> 2;
-        int i = (beg >> 2) + tid;
-        for (; i + 3 * width < e4; i += 4 * width) {
-            const float4 a0 = __ldg(row4 + i);
-            const float4 a1 = __ldg(row4 + i + width);
-            const float4 a2 = __ldg(row4 + i + 2 * width);
-            const float4 a3 = __ldg(row4 + i + 3 * width);
-            ms_add4(m, s, a0);
-            ms_add4(m, s, a1);
-            ms_add4(m, s, a2);
-            ms_add4(m, s, a3);
-        }
-        for (; i < e4; i += width) ms_add4(m, s, __ldg(row4 + i));
-    } else {
-        for (int i = beg + tid; i < end; i += width) ms_add(m, s, __ldg(row + i));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        ms_merge(m, s, m2, s2);
-    }
-    float2 *dst = part + ((size_t)kind * rows + r) * nchunks + c;
-    if (WARP_PER_ROW) {
-        if (lane == 0) *dst = make_float2(m, s);
-        return;
-    }
-    __shared__ float sm[32], ss[32];
-    if (lane == 0) {
-        sm[warp] = m;
-        ss[warp] = s;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        m = lane < nw ? sm[lane] : -INFINITY;
-        s = lane < nw ? ss[lane] : 0.0f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-            ms_merge(m, s, m2, s2);
-        }
-        if (lane == 0) *dst = make_float2(m, s);
     }
 }
 
-// The residual (or target) distribution at one node, in closed form:
-// w_v = max(0, p_v - c q_v), p = softmax(target row), q = softmax(draft row).
-struct Residual {
-    const float *t;
-    const float *d;
-    float tl2, zt, dl2, zd;  // m log2 e and Z of each row
-    float c;                 // 0: plain target softmax (draft row not read)
-    __device__ __forceinline__ float w(float tv, float dv) const {
-        const float p = e2(tv, tl2) / zt;
-        if (c == 0.0f) return p;
-        return fmaxf(0.0f, fmaf(-c, e2(dv, dl2) / zd, p));
+// Replace the logits of a thread's slice by e^(l - m_t), m_t the thread's own
+// maximum; returns (m_t, sum). A thread with no element returns (-inf, 0).
+template <int E4>
+__device__ __forceinline__ float2 exp_in_place(float4 (&x)[E4]) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < E4; ++k) m = fmaxf(m, fmaxf(fmaxf(x[k].x, x[k].y), fmaxf(x[k].z, x[k].w)));
+    const float ml2 = m == -INFINITY ? 0.0f : m * acc::kLog2e;
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < E4; ++k) {
+        x[k].x = e2(x[k].x, ml2);
+        x[k].y = e2(x[k].y, ml2);
+        x[k].z = e2(x[k].z, ml2);
+        x[k].w = e2(x[k].w, ml2);
+        s += (x[k].x + x[k].y) + (x[k].z + x[k].w);
     }
+    return make_float2(m, s);
+}
+
+template <int E4>
+__device__ __forceinline__ void scale_in_place(float4 (&x)[E4], float f) {
+#pragma unroll
+    for (int k = 0; k < E4; ++k) {
+        x[k].x *= f;
+        x[k].y *= f;
+        x[k].z *= f;
+        x[k].w *= f;
+    }
+}
+
+// The current distribution at one element: the target softmax (c = 0) or the
+// residual numerator max(0, p - c q).
+__device__ __forceinline__ float resid(float p, float q, float c) {
+    return c == 0.0f ? p : fmaxf(0.0f, fmaf(-c, q, p));
+}
+
+// Double-float: a value hi + lo with |lo| <= ulp(hi) / 2, for residual masses
+// and CDF prefixes (about 44 significant bits on the fp32 pipes; this part's
+// fp64 units are far slower).
+struct DF {
+    float hi, lo;
 };
 
-// Four consecutive elements starting at v0 (zeros past V).
-template <bool VEC4>
-__device__ __forceinline__ void load4(const Residual &R, int v0, int V, float *w) {
-    if (VEC4) {
-        if (v0 < V) {
-            const float4 tv = __ldg(reinterpret_cast<const float4 *>(R.t + v0));
-            float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (R.c != 0.0f) dv = __ldg(reinterpret_cast<const float4 *>(R.d + v0));
-            w[0] = R.w(tv.x, dv.x);
-            w[1] = R.w(tv.y, dv.y);
-            w[2] = R.w(tv.z, dv.z);
-            w[3] = R.w(tv.w, dv.w);
-        } else {
-            w[0] = w[1] = w[2] = w[3] = 0.0f;
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int v = v0 + e;
-            w[e] = v < V ? R.w(__ldg(R.t + v), R.c != 0.0f ? __ldg(R.d + v) : 0.0f) : 0.0f;
-        }
-    }
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    float e = (a.hi - (s - bb)) + (b.hi - bb);
+    e += a.lo + b.lo;
+    const float hi = s + e;
+    return {hi, e - (hi - s)};
 }
 
-// Group sums over this CTA's slice of groups [g0, g1): G[g - g0] = sum of w
-// over elements [128 g, 128 g + 128) in fp32 (lanes add four elements, the
-// warp a butterfly). A warp keeps four groups' loads in flight. Returns the
-// slice total, added in fp64 in group order (same on every thread).
-template <int NT, bool VEC4>
-__device__ double slice_sums(const Residual &R, int V, int g0, int g1, float *G, double *sh_d) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int ng = g1 - g0;
-    __syncthreads();  // earlier readers of G are done
-    for (int k0 = warp * 4; k0 < ng; k0 += (NT / 32) * 4) {
-        float w[4][4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) load4<VEC4>(R, (g0 + k0 + k) * 128 + lane * 4, V, w[k]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float gs = warp_sum(((w[k][0] + w[k][1]) + w[k][2]) + w[k][3]);
-            if (lane == 0 && k0 + k < ng) G[k0 + k] = gs;
-        }
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // lane l adds a contiguous run of groups; the runs are then added in order
-        const int per = (ng + 31) / 32;
-        double part = 0.0;
-        for (int k = 0; k < per; ++k) {
-            const int gi = lane * per + k;
-            if (gi < ng) part += (double)G[gi];
-        }
-        double incl = part;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) sh_d[0] = incl;
-    }
-    __syncthreads();
-    const double tot = sh_d[0];
-    __syncthreads();
-    return tot;
+__device__ __forceinline__ DF df_mul(DF a, float u) {
+    const float p = a.hi * u;
+    float e = fmaf(a.hi, u, -p);
+    e = fmaf(a.lo, u, e);
+    const float hi = p + e;
+    return {hi, e - (hi - p)};
 }
 
-// Per-sequence shared state of the walk (one copy per CTA).
-struct WalkShared {
-    double slot[2];  // this CTA's slice total, exchanged (double-buffered by pass parity)
-    double scratch;
+__device__ __forceinline__ bool df_gt(DF a, DF b) {
+    return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+__device__ __forceinline__ DF df_shfl_up(DF a, int d) {
+    return {__shfl_up_sync(0xffffffffu, a.hi, d), __shfl_up_sync(0xffffffffu, a.lo, d)};
+}
+
+__device__ __forceinline__ DF df_shfl(DF a, int src) {
+    return {__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+
+// (max, sum e^(x - max)) of a warp: the maximum first, then every lane
+// rescales its own sum once. Butterflies leave the same value in every lane.
+__device__ __forceinline__ float2 warp_max_sum(float m, float s) {
+    float M = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float t = (m == -INFINITY) ? 0.0f : s * ex2_approx((m - M) * acc::kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return make_float2(M, t);
+}
+
+// Per-CTA shared state of the walk, next to the per-node arrays.
+struct WalkSmem {
+    float4 recv[2][acc::kMaxCluster];  // records pushed by every rank, by exchange parity
+    uint64_t bar[2];                   // completes when every rank's record has landed
+    float4 red[32];                    // per-warp partial statistics
+    DF run_incl[32];                   // warp 0: inclusive prefix of its lanes' group runs
     int bad;
+    int abort;
+    int gsel;                          // bonus search: group picked in this CTA (-1: none)
+    int gmode;                         // 1 when gsel holds the crossing, else the last group
+    DF gbase;                          // mass before gsel (gmode 1)
 };
 
-// Sum of the slice totals of the CTAs of this sequence, in rank order. Every
-// CTA computes the same fp64 value; *before_me gets the sum over lower ranks
-// and per_rank[] every rank's total.
-template <int CL>
-__device__ double cluster_total(WalkShared &ws, double mine, int pass, double *before_me,
-                                double *per_rank) {
-    if (CL == 1) {
-        *before_me = 0.0;
-        per_rank[0] = mine;
-        return mine;
-    }
-    cg::cluster_group cluster = cg::this_cluster();
-    const int slot = pass & 1;
-    if (threadIdx.x == 0) ws.slot[slot] = mine;
-    cluster.sync();
-    double total = 0.0, before = 0.0;
-    const unsigned me = cluster.block_rank();
-    double v[CL];
-#pragma unroll
-    for (int r = 0; r < CL; ++r) v[r] = *cluster.map_shared_rank(&ws.slot[slot], r);
-#pragma unroll
-    for (int r = 0; r < CL; ++r) {
-        per_rank[r] = v[r];
-        if ((unsigned)r < me) before += v[r];
-        total += v[r];
-    }
-    *before_me = before;
-    return total;
-}
-
-template <int NT, int CL, bool VEC4>
-__global__ void __launch_bounds__(NT) accept_walk_kernel(
+template <int NT, int E4, bool VEC, bool CLUSTER>
+__global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
     const float *__restrict__ target, const float *__restrict__ draft,
     const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
-    const float *__restrict__ u_accept, const float *__restrict__ u_bonus, int N, int V,
-    const float2 *__restrict__ part, int nchunks, long long rows,
+    const float *__restrict__ u_accept, const float *__restrict__ u_bonus, int N, int V, int CL,
     int32_t *__restrict__ accept_len, int32_t *__restrict__ path,
     int32_t *__restrict__ out_tokens, float *__restrict__ ratio, int32_t *__restrict__ status) {
-    extern __shared__ double dyn[];
-    const int ngroups = (V + 127) >> 7;
-    const int gper = (ngroups + CL - 1) / CL;
-    const int rank = CL > 1 ? (int)blockIdx.x % CL : 0;
-    const int b = CL > 1 ? (int)blockIdx.y : (int)blockIdx.x;
-    const int g0 = min(ngroups, rank * gper), g1 = min(ngroups, g0 + gper);
-    float2 *st_t = reinterpret_cast<float2 *>(dyn);          // [N] target (m log2 e, Z)
-    float2 *st_d = st_t + N;                                  // [N] draft
-    float2 *pq = st_d + N;                                    // [N] p_par(x_c), q_par(x_c)
-    float *su = reinterpret_cast<float *>(pq + N);            // [N] u_accept
-    int32_t *sp = reinterpret_cast<int32_t *>(su + N);        // [N] parent
-    int32_t *stok = sp + N;                                   // [N] tokens
-    int32_t *sch = stok + N;                                  // [N] has a child
-    float *G = reinterpret_cast<float *>(sch + N);            // [gper] group sums of the slice
-    __shared__ WalkShared ws;
-    __shared__ double per_rank[acc::kCluster];
+    constexpr int NW = NT / 32;
+    constexpr int NG = NW * E4;          // 128-element groups per CTA
+    constexpr int PER = (NG + 31) / 32;  // groups per lane in the CTA prefix
+    constexpr unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rank = CLUSTER ? (int)(blockIdx.x % (unsigned)CL) : 0;
+    const long long b = CLUSTER ? (long long)(blockIdx.x / (unsigned)CL) : (long long)blockIdx.x;
+    const int ncta = CLUSTER ? CL : 1;
+    const size_t base = (size_t)b * N;
+    const int g0 = (rank * NW + warp) * E4;  // first group of this warp's slice
     const bool lead = rank == 0;
 
-    const size_t base = (size_t)b * N;
-    if (threadIdx.x == 0) ws.bad = 0;
-    for (int i = threadIdx.x; i < N; i += NT) sch[i] = 0;
+    extern __shared__ __align__(16) unsigned char dyn[];
+    float2 *slx = reinterpret_cast<float2 *>(dyn);      // [N] (target, draft) logit of c's token
+    float *su = reinterpret_cast<float *>(slx + N);     // [N] u_accept
+    int32_t *sp = reinterpret_cast<int32_t *>(su + N);  // [N] parent
+    int32_t *stok = sp + N;                             // [N] token
+    int32_t *sfirst = stok + N;                         // [N] first child, -1 for a leaf
+    int32_t *snext = sfirst + N;                        // [N] next sibling, -1 for the last
+    float *G = reinterpret_cast<float *>(snext + N);    // [NG] group sums of the last pass
+    __shared__ WalkSmem ws;
+
+    // the root's rows go out first: their latency hides behind the set-up
+    float4 P[E4], Q[E4];
+    load_slice<E4, VEC>(target + base * V, V, g0, lane, P);
+    if (N > 1) {
+        load_slice<E4, VEC>(draft + base * V, V, g0, lane, Q);
+    } else {
+#pragma unroll
+        for (int k = 0; k < E4; ++k) Q[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    // ---- the tree: parents, tokens, uniforms; validity; child lists
+    if (threadIdx.x == 0) {
+        ws.bad = 0;
+        ws.abort = 0;
+    }
+    for (int i = threadIdx.x; i < N; i += NT) sfirst[i] = INT_MAX;
     __syncthreads();
     int bad = 0;
     for (int i = threadIdx.x; i < N; i += NT) {
@@ -336,180 +245,338 @@ __global__ void __launch_bounds__(NT) accept_walk_kernel(
         const int tk = tokens[base + i];
         sp[i] = pp;
         stok[i] = tk;
-        if (i == 0 ? pp != -1 : (pp < 0 || pp >= i)) bad |= SVF_DEV_BAD_PARENT;
+        su[i] = u_accept[base + i];
+        const bool pok = i == 0 ? pp == -1 : (pp >= 0 && pp < i);
+        if (!pok) bad |= SVF_DEV_BAD_PARENT;
         if (i > 0 && (tk < 0 || tk >= V)) bad |= SVF_DEV_BAD_TOKEN;
+        if (i > 0 && pok) atomicMin(&sfirst[pp], i);
         if (lead) {
             path[base + i] = -1;
             out_tokens[base + i] = -1;
             if (ratio) ratio[base + i] = __int_as_float(0x7fc00000);
         }
     }
-    for (int o = 16; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-    if ((threadIdx.x & 31) == 0 && bad) atomicOr(&ws.bad, bad);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad |= __shfl_xor_sync(FULL, bad, o);
+    if (lane == 0 && bad) atomicOr(&ws.bad, bad);
+    if (CLUSTER && threadIdx.x == 0) {
+        mbar_init(&ws.bar[0], 1);
+        mbar_init(&ws.bar[1], 1);
+        mbar_fence_init();
+    }
     __syncthreads();
     bad = ws.bad;
     if (lead && threadIdx.x == 0) {
         status[b] = bad;
         accept_len[b] = 0;
     }
-    if (bad) {
-        if (CL > 1) cg::this_cluster().sync();
-        return;
-    }
+    if (bad) return;  // every CTA of the cluster read the same tree and leaves here
+    // peers may push records once every CTA's barriers are initialised
+    if (CLUSTER) cluster_arrive();
 
-    // prologue: row statistics of every node, and every child's gathered
-    // probabilities under its parent's target and draft softmax
-    for (int i = 1 + threadIdx.x; i < N; i += NT) sch[sp[i]] = 1;
-    __syncthreads();
-    {
-        // one warp per row: lanes load chunks in parallel, a butterfly merges
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        for (int j = warp; j < N; j += NT / 32) {
-            float mt = -INFINITY, zt = 0.0f, md = -INFINITY, zd = 0.0f;
-            const bool internal = sch[j] != 0;
-            for (int c = lane; c < nchunks; c += 32) {
-                const float2 a = part[(base + j) * nchunks + c];
-                ms_merge(mt, zt, a.x, a.y);
-                if (internal) {
-                    const float2 d = part[(rows + base + j) * nchunks + c];
-                    ms_merge(md, zd, d.x, d.y);
+    // siblings in ascending index order; every child's token logits at its
+    // parent's rows (a parent's draft row is read because it has a child).
+    // Node threadIdx.x keeps its pair in registers until the first test, so
+    // those loads overlap the root's statistics.
+    float2 lx_mine = make_float2(0.0f, 0.0f);
+    for (int i = threadIdx.x; i < N; i += NT) {
+        if (sfirst[i] == INT_MAX) sfirst[i] = -1;
+        int nx = -1;
+        if (i > 0) {
+            const int pp = sp[i];
+            for (int c = i + 1; c < N; ++c)
+                if (sp[c] == pp) {
+                    nx = c;
+                    break;
                 }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, mt, o);
-                const float z2 = __shfl_xor_sync(0xffffffffu, zt, o);
-                ms_merge(mt, zt, m2, z2);
-                const float m3 = __shfl_xor_sync(0xffffffffu, md, o);
-                const float z3 = __shfl_xor_sync(0xffffffffu, zd, o);
-                ms_merge(md, zd, m3, z3);
-            }
-            if (lane == 0) {
-                st_t[j] = make_float2(mt * acc::kLog2e, zt);
-                st_d[j] = internal ? make_float2(md * acc::kLog2e, zd) : make_float2(0.0f, 1.0f);
+            const size_t row = (base + pp) * (size_t)V + stok[i];
+            if (i < NT) {
+                lx_mine = make_float2(__ldg(target + row), __ldg(draft + row));
+            } else {
+                slx[i] = make_float2(__ldg(target + row), __ldg(draft + row));
             }
         }
+        snext[i] = nx;
     }
-    __syncthreads();
-    for (int c = 1 + threadIdx.x; c < N; c += NT) {
-        const int j = sp[c], x = stok[c];
-        const float tv = target[(base + j) * V + x];
-        const float dv = draft[(base + j) * V + x];
-        pq[c] = make_float2(e2(tv, st_t[j].x) / st_t[j].y, e2(dv, st_d[j].x) / st_d[j].y);
-        su[c] = u_accept[base + c];
-    }
-    __syncthreads();
+    if (CLUSTER) cluster_wait();
 
-    // walk: every thread of every CTA takes the same decisions
-    int cur = 0, len = 0, pass = 0;
-    double coef = 0.0, mass = 1.0;
-    bool groups_hold_residual = false;
-    double slice_before = 0.0;
+    // One exchange: warp 0 pushes this CTA's record into slot `rank` of every
+    // CTA of the cluster and waits (bounded) until every rank's record has
+    // landed in its own slots; then the CTA's threads read them locally.
+    int ph = 0, last_ph = 0;
+    auto exchange = [&](float4 rec) {
+        const int s = ph & 1;
+        if (warp == 0) {
+            if (!CLUSTER) {
+                if (lane == 0) ws.recv[s][0] = rec;
+            } else {
+                if (lane == 0) mbar_arrive_expect_tx(&ws.bar[s], (uint32_t)ncta * 16u);
+                if (lane < ncta)
+                    st_async_v4(cluster_map(&ws.recv[s][rank], (uint32_t)lane), rec,
+                                cluster_map(&ws.bar[s], (uint32_t)lane));
+                const bool ok = __all_sync(FULL, mbar_wait_cluster(&ws.bar[s], (ph >> 1) & 1));
+                if (lane == 0 && !ok) ws.abort = 1;
+            }
+        }
+        __syncthreads();
+        last_ph = ph++;
+        return s;
+    };
+    // Sum of the ranks' masses of one exchange, as a fixed butterfly over the
+    // lanes (lane r holds rank r): the same value in every thread of every CTA.
+    auto rank_sum = [&](int s) -> DF {
+        DF t = lane < ncta ? DF{ws.recv[s][lane].x, ws.recv[s][lane].y} : DF{0.0f, 0.0f};
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const DF y = {__shfl_xor_sync(FULL, t.hi, o), __shfl_xor_sync(FULL, t.lo, o)};
+            t = (lane & o) ? df_add(y, t) : df_add(t, y);
+        }
+        return t;
+    };
+    // Mass of max(0, p - c q) (or of p for c = 0) over the vocabulary: group
+    // sums into G, this CTA's total over lane runs of PER groups, then the
+    // totals of all ranks in rank order.
+    auto mass_pass = [&](float c) -> DF {
+#pragma unroll
+        for (int k = 0; k < E4; ++k) {
+            const float w0 = resid(P[k].x, Q[k].x, c), w1 = resid(P[k].y, Q[k].y, c);
+            const float w2 = resid(P[k].z, Q[k].z, c), w3 = resid(P[k].w, Q[k].w, c);
+            const float gs = warp_sum(((w0 + w1) + w2) + w3);
+            if (lane == 0) G[warp * E4 + k] = gs;
+        }
+        __syncthreads();
+        float4 rec = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (warp == 0) {
+            DF part = {0.0f, 0.0f};
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int gi = lane * PER + i;
+                if (gi < NG) part = df_add(part, DF{G[gi], 0.0f});
+            }
+            DF incl = part;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const DF y = df_shfl_up(incl, o);
+                if (lane >= o) incl = df_add(incl, y);
+            }
+            ws.run_incl[lane] = incl;
+            const DF tot = df_shfl(incl, 31);
+            rec = make_float4(tot.hi, tot.lo, 0.f, 0.f);
+        }
+        const int s = exchange(rec);
+        return rank_sum(s);
+    };
+
+    // ---- the walk: every thread of every CTA takes the same decisions
+    int cur = 0, len = 0;
+    float coef = 0.0f;
+    DF mass = {1.0f, 0.0f};
+    bool hold = false;  // G and the last exchange hold the current distribution
+    bool aborted = false;
     if (lead && threadIdx.x == 0) path[base] = 0;
     for (;;) {
-        bool moved = false;
-        for (int c = cur + 1; c < N; ++c) {
-            if (sp[c] != cur) continue;
-            const double px = (double)pq[c].x, qx = (double)pq[c].y;
-            double r = px - coef * qx;
-            r = r > 0.0 ? r : 0.0;
-            const bool accepted = (double)su[c] * qx * mass < r;
-            if (lead && threadIdx.x == 0 && ratio) ratio[base + c] = (float)(r / (mass * qx));
+        const int c1 = sfirst[cur];
+        const bool kids = c1 >= 0;
+        if (VEC && kids && threadIdx.x == 0) {
+            // ask L2 for this CTA's slice of the first child's rows
+            const int s0 = rank * NG * 128;
+            if (s0 < V) {
+                const uint32_t bytes = (uint32_t)min(NG * 128, V - s0) * 4u;
+                prefetch_l2_bulk(target + (base + c1) * V + s0, bytes);
+                if (sfirst[c1] >= 0) prefetch_l2_bulk(draft + (base + c1) * V + s0, bytes);
+            }
+        }
+        // softmax statistics of the node's rows, identical in every CTA
+        const float2 tp = exp_in_place<E4>(P);
+        const float2 tq = kids ? exp_in_place<E4>(Q) : make_float2(-INFINITY, 0.0f);
+        const float2 wp = warp_max_sum(tp.x, tp.y);
+        const float2 wq = warp_max_sum(tq.x, tq.y);
+        if (lane == 0) ws.red[warp] = make_float4(wp.x, wp.y, wq.x, wq.y);
+        __syncthreads();
+        float4 rec = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        if (warp == 0) {
+            const float4 t = lane < NW ? ws.red[lane] : rec;
+            const float2 cp = warp_max_sum(t.x, t.y);
+            const float2 cq = warp_max_sum(t.z, t.w);
+            rec = make_float4(cp.x, cp.y, cq.x, cq.y);
+        }
+        const int s = exchange(rec);
+        if (ws.abort) {
+            aborted = true;
+            break;
+        }
+        // lane r of every warp takes rank r's record; the same butterflies
+        // run in every CTA, so every CTA gets the same (m, Z)
+        const float4 rr = lane < ncta ? ws.recv[s][lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        const float2 gp = warp_max_sum(rr.x, rr.y);
+        const float2 gq = warp_max_sum(rr.z, rr.w);
+        const float mp = gp.x, zp = gp.y, mq = gq.x, zq = gq.y;
+        if (cur == 0) {
+            if (threadIdx.x > 0 && (int)threadIdx.x < N) slx[threadIdx.x] = lx_mine;  // i < NT above
+            __syncthreads();
+        }
+        // registers -> probabilities: e^(l - m_t) * e^(m_t - m) / Z
+        const float apl2 = mp * acc::kLog2e, inv_zp = 1.0f / zp;
+        scale_in_place<E4>(P, tp.x == -INFINITY ? 0.0f : e2(tp.x, apl2) * inv_zp);
+        float aql2 = 0.0f, inv_zq = 1.0f;
+        if (kids) {
+            aql2 = mq * acc::kLog2e;
+            inv_zq = 1.0f / zq;
+            scale_in_place<E4>(Q, tq.x == -INFINITY ? 0.0f : e2(tq.x, aql2) * inv_zq);
+        }
+
+        // the children, in ascending index order
+        int next = -1;
+        for (int c = c1; c >= 0; c = snext[c]) {
+            const float2 lx = slx[c];
+            const float px = e2(lx.x, apl2) * inv_zp;
+            const float qx = e2(lx.y, aql2) * inv_zq;
+            const float r = fmaxf(0.0f, fmaf(-coef, qx, px));
+            const bool accepted = su[c] * qx * mass.hi < r;
+            if (lead && threadIdx.x == 0 && ratio) ratio[base + c] = r / (mass.hi * qx);
             if (accepted) {
-                ++len;
-                if (lead && threadIdx.x == 0) {
-                    path[base + len] = c;
-                    out_tokens[base + len - 1] = stok[c];
-                }
-                cur = c;
-                coef = 0.0;
-                mass = 1.0;
-                groups_hold_residual = false;
-                moved = true;
+                next = c;
                 break;
             }
-            // rejected: mass of max(0, p - (coef + mass) q) over the vocabulary
-            Residual R;
-            R.t = target + (base + cur) * V;
-            R.d = draft + (base + cur) * V;
-            R.tl2 = st_t[cur].x; R.zt = st_t[cur].y; R.dl2 = st_d[cur].x; R.zd = st_d[cur].y;
-            R.c = (float)(coef + mass);
-            const double mine = slice_sums<NT, VEC4>(R, V, g0, g1, G, &ws.scratch);
-            double before;
-            const double S = cluster_total<CL>(ws, mine, pass++, &before, per_rank);
-            if (S > 0.0) {
-                coef = (double)R.c;
+            // rejected: the residual max(0, p - (coef + mass) q) and its mass
+            const float cn = df_add(DF{coef, 0.0f}, mass).hi;
+            const DF S = mass_pass(cn);
+            if (ws.abort) {
+                aborted = true;
+                break;
+            }
+            if (S.hi > 0.0f) {
+                coef = cn;
                 mass = S;
-                groups_hold_residual = true;
-                slice_before = before;
+                hold = true;
             } else {
-                groups_hold_residual = false;
+                hold = false;  // no mass: the distribution stays as it was
             }
         }
-        if (!moved) break;
+        if (aborted || next < 0) break;
+        ++len;
+        if (lead && threadIdx.x == 0) {
+            path[base + len] = next;
+            out_tokens[base + len - 1] = stok[next];
+        }
+        cur = next;
+        coef = 0.0f;
+        mass = DF{1.0f, 0.0f};
+        hold = false;
+        load_slice<E4, VEC>(target + (base + cur) * V, V, g0, lane, P);
+        if (sfirst[cur] >= 0) load_slice<E4, VEC>(draft + (base + cur) * V, V, g0, lane, Q);
     }
 
-    // bonus token at the last node, from its target softmax or its residual
-    Residual R;
-    R.t = target + (base + cur) * V;
-    R.tl2 = st_t[cur].x;
-    R.zt = st_t[cur].y;
-    R.c = (float)coef;
-    R.d = coef != 0.0 ? draft + (base + cur) * V : R.t;
-    R.dl2 = coef != 0.0 ? st_d[cur].x : 0.0f;
-    R.zd = coef != 0.0 ? st_d[cur].y : 1.0f;
-    double total;
-    if (groups_hold_residual) {
-        total = mass;
-    } else {
-        const double mine = slice_sums<NT, VEC4>(R, V, g0, g1, G, &ws.scratch);
-        total = cluster_total<CL>(ws, mine, pass++, &slice_before, per_rank);
+    // ---- bonus token at the last node, from its target softmax or its residual
+    DF total = mass;
+    if (!aborted && !hold) {
+        total = mass_pass(coef);
+        aborted = ws.abort != 0;
     }
-    const double thr = (double)u_bonus[b] * total;
-    // the CTA whose slice holds the crossing, else (rounding) the last one with mass
-    int owner = -1, last_pos = -1;
-    {
-        double acc_before = 0.0;
-        for (int r2 = 0; r2 < CL; ++r2) {
-            const double v = per_rank[r2];
-            if (owner < 0 && acc_before + v > thr) owner = r2;
-            if (v > 0.0) last_pos = r2;
-            acc_before += v;
+    if (aborted) {
+        // a peer stopped answering: report it. Every wait above is bounded, so
+        // every CTA of the cluster reaches the closing barrier.
+        if (lead && threadIdx.x == 0) {
+            accept_len[b] = len;
+            atomicOr(&status[b], SVF_DEV_TIMEOUT);
         }
+        if (CLUSTER) {
+            cluster_arrive();
+            cluster_wait();
+        }
+        return;
     }
+    const int lp = last_ph & 1;
+    const DF thr = df_mul(total, u_bonus[b]);
+    // the rank whose slice holds the crossing, else (rounding) the last one with mass
+    int owner = -1, last_pos = -1;
+    DF owner_before = {0.0f, 0.0f};
+    {
+        const DF v = lane < ncta ? DF{ws.recv[lp][lane].x, ws.recv[lp][lane].y} : DF{0.0f, 0.0f};
+        DF incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const DF y = df_shfl_up(incl, o);
+            if (lane >= o) incl = df_add(y, incl);
+        }
+        DF excl = df_shfl_up(incl, 1);
+        if (lane == 0) excl = DF{0.0f, 0.0f};
+        const unsigned hit = __ballot_sync(FULL, lane < ncta && df_gt(incl, thr));
+        const unsigned pos = __ballot_sync(FULL, lane < ncta && v.hi > 0.0f);
+        if (hit) {
+            owner = __ffs(hit) - 1;
+            owner_before = df_shfl(excl, owner);
+        }
+        if (pos) last_pos = 31 - __clz(pos);
+    }
+    if (CLUSTER) cluster_arrive();  // no more traffic between the CTAs
     const bool crossing = owner >= 0;
     if (!crossing) owner = last_pos;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (owner == rank && warp == 0) {
-        const int ng = g1 - g0;
-        // group of the crossing: running fp64 sum over the slice's groups
-        int gsel = -1;
-        double gb = slice_before;
-        if (lane == 0) {
+    if (owner == rank) {
+        if (warp == 0) {
+            // the group of the crossing: the first lane run whose prefix passes
+            // thr, then that run group by group
+            int gsel = -1, mode = 0;
+            DF gb = {0.0f, 0.0f};
             if (crossing) {
-                for (int k = 0; k < ng; ++k) {
-                    if (gb + (double)G[k] > thr) {
-                        gsel = k;
-                        break;
+                const DF incl = ws.run_incl[lane];
+                DF excl = df_shfl_up(incl, 1);
+                if (lane == 0) excl = DF{0.0f, 0.0f};
+                const unsigned hit = __ballot_sync(FULL, df_gt(df_add(owner_before, incl), thr));
+                if (hit) {
+                    const int l0 = __ffs(hit) - 1;
+                    if (lane == l0) {
+                        DF run = df_add(owner_before, excl);
+                        for (int i = l0 * PER; i < min(NG, (l0 + 1) * PER); ++i) {
+                            const DF nx = df_add(run, DF{G[i], 0.0f});
+                            if (df_gt(nx, thr)) {
+                                gsel = i;
+                                break;
+                            }
+                            run = nx;
+                        }
+                        gb = run;
                     }
-                    gb += (double)G[k];
+                    gsel = __shfl_sync(FULL, gsel, l0);
+                    gb = df_shfl(gb, l0);
+                    mode = gsel >= 0 ? 1 : 0;
                 }
             }
-            if (gsel < 0) {  // no crossing found: last group with mass
-                for (int k = ng - 1; k >= 0; --k)
-                    if (G[k] > 0.0f) {
-                        gsel = k;
+            if (gsel < 0) {
+                // no crossing (rounding): the last group with mass
+                int lastg = -1;
+                for (int i = min(NG, (lane + 1) * PER) - 1; i >= lane * PER; --i)
+                    if (G[i] > 0.0f) {
+                        lastg = i;
                         break;
                     }
-                gb = 0.0;
+                const unsigned has = __ballot_sync(FULL, lastg >= 0);
+                if (has) gsel = __shfl_sync(FULL, lastg, 31 - __clz(has));
+                gb = DF{0.0f, 0.0f};
+                mode = 0;
+            }
+            if (lane == 0) {
+                ws.gsel = gsel;
+                ws.gbase = gb;
+                ws.gmode = mode;
             }
         }
-        gsel = __shfl_sync(0xffffffffu, gsel, 0);
-        gb = __shfl_sync(0xffffffffu, gb, 0);
-        int pick = -1;
-        if (gsel >= 0) {
-            float w[4];
-            load4<VEC4>(R, (g0 + gsel) * 128 + lane * 4, V, w);
+        __syncthreads();
+        const int gsel = ws.gsel;
+        if (gsel < 0) {
+            if (threadIdx.x == 0) out_tokens[base + len] = -1;
+        } else if (warp == gsel / E4) {
+            const int ks = gsel - warp * E4;
+            float4 pp = P[0], qq = Q[0];
+#pragma unroll
+            for (int k = 1; k < E4; ++k)
+                if (k == ks) {
+                    pp = P[k];
+                    qq = Q[k];
+                }
+            const bool by_crossing = ws.gmode != 0;
+            const float w[4] = {resid(pp.x, qq.x, coef), resid(pp.y, qq.y, coef),
+                                resid(pp.z, qq.z, coef), resid(pp.w, qq.w, coef)};
             float a[4];
             a[0] = w[0];
             a[1] = a[0] + w[1];
@@ -518,127 +585,168 @@ __global__ void __launch_bounds__(NT) accept_walk_kernel(
             float incl = a[3];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                const float y = __shfl_up_sync(FULL, incl, o);
                 if (lane >= o) incl += y;
             }
-            const double lbase = gb + (double)(incl - a[3]);
+            const DF lbase = df_add(ws.gbase, DF{incl - a[3], 0.0f});
             int hit = -1, lastw = -1;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (crossing && hit < 0 && lbase + (double)a[e] > thr) hit = e;
+                if (by_crossing && hit < 0 && df_gt(df_add(lbase, DF{a[e], 0.0f}), thr)) hit = e;
                 if (w[e] > 0.0f) lastw = e;
             }
-            const unsigned bh = __ballot_sync(0xffffffffu, hit >= 0);
-            const unsigned bl = __ballot_sync(0xffffffffu, lastw >= 0);
+            const unsigned bh = __ballot_sync(FULL, hit >= 0);
+            const unsigned bl = __ballot_sync(FULL, lastw >= 0);
+            const int v0 = (rank * NG + gsel) * 128;
+            int pick = -1;
             if (bh) {
                 const int src = __ffs(bh) - 1;
-                pick = (g0 + gsel) * 128 + src * 4 + __shfl_sync(0xffffffffu, hit, src);
+                pick = v0 + src * 4 + __shfl_sync(FULL, hit, src);
             } else if (bl) {
                 const int src = 31 - __clz(bl);
-                pick = (g0 + gsel) * 128 + src * 4 + __shfl_sync(0xffffffffu, lastw, src);
+                pick = v0 + src * 4 + __shfl_sync(FULL, lastw, src);
             }
+            if (lane == 0) out_tokens[base + len] = pick;
         }
-        if (lane == 0) out_tokens[base + len] = pick;
     }
     if (lead && threadIdx.x == 0) accept_len[b] = len;
-    if (CL > 1) cg::this_cluster().sync();  // peers may still read this CTA's slots
+    if (CLUSTER) cluster_wait();
 }
 
-static int stat_chunks(long long rows, int V, int *chunk) {
-    if (V <= acc::kSmallV) {
-        *chunk = V;
-        return 1;
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+struct WalkCfg {
+    int nt, e4, cl;
+};
+
+constexpr int kLargeCap = acc::kLargeThreads / 32 * 128;  // elements per CTA per float4 slot
+static_assert(kLargeCap * 8 * acc::kMaxCluster == kMaxOnChipVocab,
+              "the largest on-chip configuration holds exactly kMaxOnChipVocab elements");
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Threads, float4 slots per lane and CTAs per sequence for a vocabulary of V.
+bool walk_config(int B, int V, WalkCfg *cfg) {
+    if (V <= 128) *cfg = {32, 1, 1};
+    else if (V <= 512) *cfg = {32, 4, 1};
+    else if (V <= 1024) *cfg = {128, 2, 1};
+    else if (V <= 4096) *cfg = {128, 8, 1};
+    else {
+        int e4 = 1;
+        while (e4 < 8 && ceil_div(V, (long long)kLargeCap * e4) > acc::kMaxCluster) e4 *= 2;
+        int cl = ceil_div(V, (long long)kLargeCap * e4);
+        if (cl > acc::kMaxCluster) return false;
+        // many sequences: fewer, fuller CTAs per sequence
+        while (e4 < 8 && (long long)B * cl > num_sms()) {
+            e4 *= 2;
+            cl = ceil_div(V, (long long)kLargeCap * e4);
+        }
+        *cfg = {acc::kLargeThreads, e4, cl};
     }
-    const long long want = 4LL * num_sms();
-    long long n = (want + 2 * rows - 1) / (2 * rows);
-    const long long maxn = (V + 4095) / 4096;
-    if (n > maxn) n = maxn;
-    if (n < 1) n = 1;
-    if (n > 64) n = 64;
-    int ch = (int)((V + n - 1) / n);
-    ch = (ch + 1023) / 1024 * 1024;
-    *chunk = ch;
-    return (V + ch - 1) / ch;
+    return true;
 }
 
-size_t accept_workspace_bytes(int B, int N, int V) {
-    int chunk;
-    const int n = stat_chunks((long long)B * N, V, &chunk);
-    return (size_t)2 * B * N * n * sizeof(float2) + 256;
+size_t walk_smem(int N, const WalkCfg &c) {
+    return (size_t)N * (sizeof(float2) + sizeof(float) + 4 * sizeof(int32_t)) +
+           (size_t)(c.nt / 32) * c.e4 * sizeof(float) + 16;
 }
 
-template <int NT, int CL, bool VEC4>
-static cudaError_t launch_walk(const float *target, const float *draft, const int32_t *tokens,
-                               const int32_t *parent, const float *u_accept,
-                               const float *u_bonus, int B, int N, int V, const float2 *part,
-                               int nchunks, int32_t *accept_len, int32_t *path,
-                               int32_t *out_tokens, float *ratio, int32_t *status,
-                               cudaStream_t stream) {
-    const int ngroups = (V + 127) >> 7;
-    const int gper = (ngroups + CL - 1) / CL;
-    const size_t smem = (size_t)N * (3 * sizeof(float2) + sizeof(float) + 3 * sizeof(int32_t)) +
-                        (size_t)gper * sizeof(float) + 16;
-    auto kern = accept_walk_kernel<NT, CL, VEC4>;
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    const long long rows = (long long)B * N;
-    if (CL == 1) {
-        kern<<<B, NT, smem, stream>>>(target, draft, tokens, parent, u_accept, u_bonus, N, V, part,
-                                      nchunks, rows, accept_len, path, out_tokens, ratio, status);
+template <int NT, int E4, bool VEC, bool CLUSTER>
+cudaError_t launch_walk(const WalkCfg &c, const float *target, const float *draft,
+                        const int32_t *tokens, const int32_t *parent, const float *u_accept,
+                        const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                        int32_t *path, int32_t *out_tokens, float *ratio, int32_t *status,
+                        cudaStream_t stream) {
+    auto kern = accept_walk_kernel<NT, E4, VEC, CLUSTER>;
+    const size_t smem = walk_smem(N, c);
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    if (!CLUSTER) {
+        kern<<<(unsigned)B, NT, smem, stream>>>(target, draft, tokens, parent, u_accept, u_bonus,
+                                                 N, V, 1, accept_len, path, out_tokens, ratio,
+                                                 status);
         return cudaGetLastError();
     }
+    if (c.cl > 8) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CL, B, 1);
+    cfg.gridDim = dim3((unsigned)((long long)B * c.cl), 1, 1);
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.x = (unsigned)c.cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, target, draft, tokens, parent, u_accept, u_bonus, N, V,
-                              part, nchunks, rows, accept_len, path, out_tokens, ratio, status);
+                              c.cl, accept_len, path, out_tokens, ratio, status);
+}
+
+template <bool VEC>
+cudaError_t dispatch_walk(const WalkCfg &c, const float *target, const float *draft,
+                          const int32_t *tokens, const int32_t *parent, const float *u_accept,
+                          const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                          int32_t *path, int32_t *out_tokens, float *ratio, int32_t *status,
+                          cudaStream_t stream) {
+#define SVF_WALK(NT_, E4_, CL_)                                                                  \
+    return launch_walk<NT_, E4_, VEC, CL_>(c, target, draft, tokens, parent, u_accept, u_bonus, \
+                                           B, N, V, accept_len, path, out_tokens, ratio, status, \
+                                           stream)
+    if (c.nt == 32) {
+        if (c.e4 == 1) SVF_WALK(32, 1, false);
+        SVF_WALK(32, 4, false);
+    }
+    if (c.nt == 128) {
+        if (c.e4 == 2) SVF_WALK(128, 2, false);
+        SVF_WALK(128, 8, false);
+    }
+    switch (c.e4) {
+        case 1: SVF_WALK(acc::kLargeThreads, 1, true);
+        case 2: SVF_WALK(acc::kLargeThreads, 2, true);
+        case 4: SVF_WALK(acc::kLargeThreads, 4, true);
+        default: SVF_WALK(acc::kLargeThreads, 8, true);
+    }
+#undef SVF_WALK
+}
+
+}  // namespace
+
+bool accept_supported(int V) { return V >= 1 && V <= kMaxStreamVocab; }
+
+bool accept_on_chip(int V) {
+    WalkCfg c;
+    return walk_config(1, V, &c);
+}
+
+size_t accept_workspace_bytes(int B, int N, int V) {
+    return accept_on_chip(V) ? 0 : accept_stream_workspace_bytes(B, N, V);
 }
 
 cudaError_t launch_accept(const float *target, const float *draft, const int32_t *tokens,
                           const int32_t *parent, const float *u_accept, const float *u_bonus, int B,
                           int N, int V, int32_t *accept_len, int32_t *path, int32_t *out_tokens,
                           float *ratio, void *workspace, int32_t *status, cudaStream_t stream) {
-    float2 *part = reinterpret_cast<float2 *>(
-        (reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
-    const long long rows = (long long)B * N;
-    int chunk;
-    const int nchunks = stat_chunks(rows, V, &chunk);
-    if (V <= acc::kSmallV) {
-        dim3 grid((unsigned)((rows + 7) / 8), 2);
-        accept_rowstats_kernel<true><<<grid, 256, 0, stream>>>(target, draft, parent, B, N, V, 1,
-                                                               V, part);
-    } else {
-        dim3 grid((unsigned)(rows * nchunks), 2);
-        accept_rowstats_kernel<false><<<grid, 256, 0, stream>>>(target, draft, parent, B, N, V,
-                                                                nchunks, chunk, part);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const bool vec4 = (V & 3) == 0;
-    if (V <= acc::kSmallV) {
-        return vec4 ? launch_walk<32, 1, true>(target, draft, tokens, parent, u_accept, u_bonus, B,
-                                              N, V, part, nchunks, accept_len, path, out_tokens,
-                                              ratio, status, stream)
-                    : launch_walk<32, 1, false>(target, draft, tokens, parent, u_accept, u_bonus,
-                                               B, N, V, part, nchunks, accept_len, path,
-                                               out_tokens, ratio, status, stream);
-    }
-    constexpr int NT = acc::kWalkThreads, CL = acc::kCluster;
-    return vec4 ? launch_walk<NT, CL, true>(target, draft, tokens, parent, u_accept, u_bonus, B, N,
-                                           V, part, nchunks, accept_len, path, out_tokens, ratio,
-                                           status, stream)
-                : launch_walk<NT, CL, false>(target, draft, tokens, parent, u_accept, u_bonus, B,
-                                            N, V, part, nchunks, accept_len, path, out_tokens,
-                                            ratio, status, stream);
+    WalkCfg c;
+    if (!walk_config(B, V, &c))
+        return launch_accept_stream(target, draft, tokens, parent, u_accept, u_bonus, B, N, V,
+                                    accept_len, path, out_tokens, ratio, workspace, status,
+                                    stream);
+    return (V & 3) == 0 ? dispatch_walk<true>(c, target, draft, tokens, parent, u_accept, u_bonus,
+                                              B, N, V, accept_len, path, out_tokens, ratio,
+                                              status, stream)
+                        : dispatch_walk<false>(c, target, draft, tokens, parent, u_accept,
+                                               u_bonus, B, N, V, accept_len, path, out_tokens,
+                                               ratio, status, stream);
 }
 
 }  // namespace svf

@@ -6,7 +6,8 @@
 // input and output buffers, a serving loop that reserved every byte of HBM
 // up front and forbids allocation afterwards, or host code that must not
 // risk the implicit synchronisation an allocation can bring. This entry
-// point runs the same two kernels as svf_spec_accept, but their scratch (the
+// point runs the same kernels as svf_spec_accept. Vocabularies up to 262144
+// need no scratch; for larger ones the streaming kernels' scratch (the
 // per-row, per-chunk softmax statistics) lives in a fixed array that the
 // library itself defines in device memory. Every GPU that loads the library
 // holds that array until the process exits.

@@ -127,11 +127,11 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
     if (!target_logits || !draft_logits || !tokens || !parent || !u_accept || !u_bonus ||
         !accept_len || !path || !out_tokens || !status)
         return SVF_ERR_ARG;
-    if (N < 1 || N > 1024 || V < 1 || V > 786432) return SVF_ERR_UNSUPPORTED;
+    if (N < 1 || N > 1024 || V < 1 || !accept_supported(V)) return SVF_ERR_UNSUPPORTED;
     if ((V & 3) == 0 && (!aligned16(target_logits) || !aligned16(draft_logits)))
         return SVF_ERR_ARG;
     const size_t need = accept_workspace_bytes(B, N, V);
-    if (!workspace || workspace_bytes < need) return SVF_ERR_WORKSPACE;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return SVF_ERR_WORKSPACE;
     cudaError_t e = launch_accept(target_logits, draft_logits, tokens, parent, u_accept, u_bonus,
                                   B, N, V, accept_len, path, out_tokens, ratio, workspace, status,
                                   reinterpret_cast<cudaStream_t>(stream));

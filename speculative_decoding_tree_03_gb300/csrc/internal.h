@@ -38,12 +38,24 @@ size_t attn_tc_workspace_bytes(int B, int N, int Hq, int Hkv, int max_pages, int
 int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size);
 int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream);
 
-// Acceptance walk (accept.cu).
+// Acceptance walk (accept.cu): rows of the visited nodes held in the registers
+// of one CTA cluster up to kMaxOnChipVocab, streamed from memory beyond that
+// (accept_stream.cu, with a statistics pre-pass into the workspace).
+constexpr int kMaxOnChipVocab = 262144;
+constexpr int kMaxStreamVocab = 786432;
+bool accept_supported(int V);
+bool accept_on_chip(int V);
 size_t accept_workspace_bytes(int B, int N, int V);
 cudaError_t launch_accept(const float *target, const float *draft, const int32_t *tokens,
                           const int32_t *parent, const float *u_accept, const float *u_bonus, int B,
                           int N, int V, int32_t *accept_len, int32_t *path, int32_t *out_tokens,
                           float *ratio, void *workspace, int32_t *status, cudaStream_t stream);
+size_t accept_stream_workspace_bytes(int B, int N, int V);
+cudaError_t launch_accept_stream(const float *target, const float *draft, const int32_t *tokens,
+                                 const int32_t *parent, const float *u_accept,
+                                 const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                                 int32_t *path, int32_t *out_tokens, float *ratio, void *workspace,
+                                 int32_t *status, cudaStream_t stream);
 
 int num_sms();
 

@@ -475,3 +475,4 @@ def algorithmic_bytes(w: Workload, seq_lens: np.ndarray, parent: np.ndarray) -> 
     flops = 4 * int(T.sum()) * w.N * w.Hq * w.D
     return {"attn_bytes": attn, "accept_bytes": accept, "attn_flops": flops,
             "internal_rows": internal}
+

@@ -92,9 +92,13 @@ def test_accept_argument_checks(lib):
     assert call(t=None) == -1
     assert call(N=0) == -2 and call(N=1025) == -2
     assert call(V=786433) == -2
-    assert call(ws=None) == -4
-    assert call(wsb=8) == -4
-    assert lib.svf_spec_accept_workspace_size(2, 3, 100) > 0
+    # vocabularies held on chip need no workspace; larger ones stream from
+    # memory with a statistics pre-pass that does
+    assert lib.svf_spec_accept_workspace_size(2, 3, 100) == 0
+    assert lib.svf_spec_accept_workspace_size(64, 31, 262144) == 0
+    assert lib.svf_spec_accept_workspace_size(2, 3, 262145) > 0
+    assert call(V=300000, ws=None) == -4
+    assert call(V=300000, wsb=8) == -4
 
 
 def test_workspace_sizes_without_gpu(lib):

@@ -323,6 +323,16 @@ def test_accept_vocab_sizes(sv, V):
     print(V, stats)
 
 
+def test_accept_streaming_vocabulary(sv):
+    """A vocabulary above what one cluster holds on chip (262144) takes the
+    streaming kernels with their statistics pre-pass."""
+    V = 300000
+    arrs = _synthetic_accept(31, 3, 7, V, [-1, 0, 0, 1, 1, 2, 2], sigma=2.0, noise=0.7)
+    assert sv.spec_accept_workspace_size(3, 7, V) > 0
+    gpu = _accept_gpu(sv, arrs)
+    compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
+
+
 def test_accept_root_only_and_chain(sv):
     arrs = _synthetic_accept(21, 32, 1, 500, [-1])
     gpu = _accept_gpu(sv, arrs)
