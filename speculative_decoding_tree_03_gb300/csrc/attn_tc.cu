@@ -7,21 +7,31 @@
 // (D.2), so the kernel is a KV-streaming decode kernel: every query row of one
 // (sequence, KV head) -- N nodes x G grouped heads -- shares each K/V tile.
 //
-// One CTA = (KV split, KV head [x row block], sequence). Roles:
-//   warp 0      TMA producer: K and V tiles of 128 tokens, page by page
-//               (128-byte swizzle), into a 2-stage ring.
-//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma:
-//                 S_h  = Q_h K^T  (A, B from shared memory, M=128, N=128)
-//                 O_h += P_h V    (A = P from tensor memory, B = V MN-major)
-//   warps 2..   softmax: one thread per query row (= TMEM lane). Reads S
-//               from TMEM, applies the ancestor mask on the tile(s) that
-//               reach the tree, keeps a lazily-updated running max (O is
-//               rescaled only when the max grows by more than 2^8), writes
-//               P as bf16 into the S columns, and finally reads O.
-// With more than 128 rows (N*G > 128) the rows form two halves with their own
-// S/O accumulators; the halves interleave on the tensor pipe.
+// One CTA = (KV head [x row block], KV chunk, sequence); up to 128 rows form
+// one half (NH = 1), up to 256 rows two halves (NH = 2). Roles:
+//   warp 0        producer: K and V tiles of 64 tokens, one TMA box per page
+//                 (16 tokens at most) and 64-dim half, 128-byte swizzle,
+//                 issued by several lanes at once into two rings (K and V).
+//                 Every box's coordinate is computed once, at kernel start,
+//                 into shared memory. It also zeroes V rows past the
+//                 sequence end in the last tile.
+//   warp 1 + h    QK issuer of half h: S_h,b = Q_h K^T (A, B from shared
+//                 memory, M=128, N=64) into S buffer b = tile parity, once
+//                 the PV that read that buffer is done. Warp 1 also owns the
+//                 tensor-memory allocation.
+//   warp 1+NH+h   PV issuer of half h: O_h += P_h,b V (A = P from tensor
+//                 memory, B = V MN-major) once the softmax wrote P.
+//                 A thread issuing tcgen05.mma sustains about one MMA per 100
+//                 cycles; separate issuing warps overlap, so every chain gets
+//                 its own.
+//   4 warps per h softmax: one thread per query row (= TMEM lane). Reads the
+//                 64 S columns of a tile, applies the ancestor mask on the
+//                 tiles that reach the tree, keeps a lazily-updated running
+//                 max (O is rescaled only when the max grows by more than
+//                 2^8), writes P as bf16 over the first 32 S columns, and
+//                 finally reads O.
 //
-// Splits of the KV range write normalised partial outputs and their
+// Chunks of the KV range (splits) write normalised partial outputs and their
 // log-sum-exp to the workspace; attn_combine_kernel merges them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -34,21 +44,29 @@
 namespace svf {
 
 namespace tc {
-constexpr int BN = 128;                  // KV tokens per tile
-constexpr int HD = 128;                  // head_dim
-// Ring depths for K and V tiles (32 KB each). One 128-row half (32 KB of Q)
-// fits 3 + 3 stages; two halves (64 KB of Q) fit 5 stages. There K frees as
-// soon as the QK^T that reads it completes, early enough for 2 stages, while
-// V waits for its PV, the last use of a tile, and gets the third stage.
-__host__ __device__ constexpr int kstages_for(int NH) { return NH == 1 ? 3 : 2; }
-__host__ __device__ constexpr int vstages_for(int NH) { return 3; }
-constexpr int CRING = 16;  // page coordinates kept for tiles ahead of the V ring
-constexpr int HALF_BYTES = 128 * HD * 2;  // 32 KB: 128 rows x 128 bf16
-constexpr int ATOM_COL_BYTES = 128 * 128;  // one 64-element column block of a 128-row tile
-constexpr int TILE_BYTES = BN * HD * 2;   // 32 KB per K or V tile
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int PREFETCH = 3;               // tiles pulled into L2 ahead of the smem ring
-constexpr int MAX_BOX_ROWS = 32;          // TMA box height (tokens) for large pages
+constexpr int BN = 64;                      // KV tokens per tile
+constexpr int HD = 128;                     // head_dim
+constexpr int SB = 2;                       // S buffers per row half
+constexpr int HALF_BYTES = 128 * HD * 2;    // 32 KB of Q per 128-row half
+constexpr int Q_COL_BYTES = 128 * 128;      // one 64-dim block of 128 Q rows
+constexpr int TILE_BYTES = BN * HD * 2;     // 16 KB per K or V tile
+constexpr int KV_COL_BYTES = BN * 128;      // one 64-dim block of a 64-token tile
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr int MAX_BOX_ROWS = 64;            // TMA box height (tokens)
+constexpr int CMAX_TILES = 256;             // tiles of one CTA (coordinates in smem)
+constexpr int MAX_BOXES = CMAX_TILES * (BN / 16);
+// K/V ring depths: two halves of Q (64 KB) leave room for 9 stages of 16 KB,
+// one half for 11. A V stage is held two tiles longer than a K stage (its PV
+// comes after the next tile's QK), so V gets the extra stage.
+__host__ __device__ constexpr int kstages_for(int NH) { return NH == 1 ? 5 : 4; }
+__host__ __device__ constexpr int vstages_for(int NH) { return NH == 1 ? 6 : 5; }
+constexpr int kFixedTiles = 3;              // prologue + epilogue cost, in tiles
+// Warps: a K and a V producer, a QK issuer and a PV issuer per half, four
+// softmax warps per half. One thread issuing tcgen05.mma (or TMA copies)
+// sustains about one instruction per 100 cycles; several issuing warps
+// overlap, so each stream gets its own warp.
+__host__ __device__ constexpr int first_softmax_warp(int NH) { return 2 + 2 * NH; }
+__host__ __device__ constexpr int threads_for(int NH) { return 32 * (2 + 6 * NH); }
 }  // namespace tc
 
 struct TcParams {
@@ -58,7 +76,7 @@ struct TcParams {
     const uint64_t *anc;
     int B, N, Hq, Hkv, G, M;
     int num_pages, page_size, max_pages;
-    int splits, row_blocks;
+    int splits, chunk, row_blocks;
     int q_tma;        // 1: Q arrives by TMA (G a power of two <= 128)
     float scale_log2;
     __nv_bfloat16 *out;
@@ -70,16 +88,18 @@ struct TcParams {
 
 template <int NH>
 struct TcSmem {
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + NH * tc::HALF_BYTES;
     static constexpr int kKS = tc::kstages_for(NH);
     static constexpr int kVS = tc::vstages_for(NH);
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + NH * tc::HALF_BYTES;
     static constexpr int kV = kK + kKS * tc::TILE_BYTES;
-    static constexpr int kBar = kV + kVS * tc::TILE_BYTES;
-    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 3 * 2 + 1;
+    static constexpr int kCrd = kV + kVS * tc::TILE_BYTES;
+    static constexpr int kBar = kCrd + tc::MAX_BOXES * 4;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 3 * NH * tc::SB + 2;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kDynamic = kBytes + 1024;  // slack to align the base to 1 KB
+    static_assert(kDynamic <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -101,149 +121,114 @@ __device__ __forceinline__ uint32_t visible_bits(long long off, uint64_t anc) {
 }
 
 template <int NH>
-__global__ void __launch_bounds__(64 + 128 * NH, 1)
+__global__ void __launch_bounds__(tc::threads_for(NH), 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmq, TcParams p) {
     using S = TcSmem<NH>;
     using namespace tc;
     constexpr int KS = S::kKS;
     constexpr int VS = S::kVS;
+    constexpr int NTHREADS = threads_for(NH);
+    constexpr int SW0 = first_softmax_warp(NH);
+    constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = smem + S::kQ;
     uint8_t *sK = smem + S::kK;
     uint8_t *sV = smem + S::kV;
+    int32_t *crd = reinterpret_cast<int32_t *>(smem + S::kCrd);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
     uint64_t *k_full = bars;
     uint64_t *k_empty = k_full + KS;
     uint64_t *v_full = k_empty + KS;
     uint64_t *v_empty = v_full + VS;
-    // S slots: the two row halves (NH = 2), or two buffers of one half (NH = 1)
-    uint64_t *s_full = v_empty + VS;
-    uint64_t *p_full = s_full + 2;
-    uint64_t *o_done = p_full + 2;
-    uint64_t *q_full = o_done + 2;
+    uint64_t *s_full = v_empty + VS;      // [NH][SB]: QK of the tile in S buffer b done
+    uint64_t *p_full = s_full + NH * SB;  // [NH][SB]: P of the tile written over S buffer b
+    uint64_t *o_done = p_full + NH * SB;  // [NH][SB]: PV that read S buffer b done
+    uint64_t *q_full = o_done + NH * SB;
+    uint64_t *v_tail = q_full + 1;       // last V tile with its rows past the end zeroed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
     int *err_flag = reinterpret_cast<int *>(smem + S::kMisc + 8);
 
-    // tensor memory: S slot k at columns [128 k, 128 k + 128), O of half h at
-    // [256 + 128 h, ...); P is written over the first 64 columns of its S slot
+    // tensor memory: S buffer (h, b) at columns [64 (SB h + b), +64); O of
+    // half h at [256 + 128 h, +128); P goes over the first 32 columns of its S
     constexpr uint32_t kTmemCols = 512;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int split = blockIdx.x;
-    const int g = blockIdx.y / p.row_blocks;
-    const int rb = blockIdx.y % p.row_blocks;
+    // KV heads vary fastest: the CTAs of one token range start together, so
+    // the heads' slices of each token row are read from DRAM close in time
+    const int g = blockIdx.x / p.row_blocks;
+    const int rb = blockIdx.x % p.row_blocks;
+    const int split = blockIdx.y;
     const int b = blockIdx.z;
 
     const int L = p.seq_lens[b];
     const long long T = (long long)L + p.N;
     const bool len_ok = L >= 0 && T <= (long long)p.max_pages * p.page_size;
     const int ntiles = len_ok ? (int)((T + BN - 1) / BN) : 0;
-    const int chunk = (ntiles + p.splits - 1) / p.splits;
-    const int j0 = split * chunk;
-    const int j1 = min(j0 + chunk, ntiles);
+    const int j0 = split * p.chunk;
+    const int j1 = min(j0 + p.chunk, ntiles);
+    const int n = j1 - j0;
+    if (n <= 0) {
+        // No tile here. The first chunk reports a bad length; with a single
+        // chunk this CTA owns final outputs, which are zeros then.
+        if (split == 0 && !len_ok && threadIdx.x == 0 && rb == 0 && g == 0)
+            atomicOr(&p.status[b], SVF_DEV_BAD_LENGTH);
+        if (p.splits == 1 && threadIdx.x < 128 * NH) {
+            const int R = rb * 128 * NH + threadIdx.x;
+            if (R < p.M) {
+                const size_t row = ((size_t)b * p.N + R / p.G) * p.Hq + g * p.G + R % p.G;
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < HD / 8; ++k)
+                    *reinterpret_cast<uint4 *>(p.out + row * HD + 8 * k) = z;
+                if (p.lse) p.lse[row] = 0.0f;
+            }
+        }
+        return;
+    }
 
-    // Page-table lookup of one tile, one box per lane of the producer warp:
-    // the starting slot of box `lane` (a slot past the cache, zero-filled by
-    // TMA, for boxes past the sequence or with a page id outside the cache).
-    // Every index fits in 32 bits (num_pages * page_size <= INT_MAX).
+    // ---- set-up: barriers, Q, tensor memory, box coordinates
     const int ps = p.page_size;
     const int box_rows = ps < MAX_BOX_ROWS ? ps : MAX_BOX_ROWS;
-    const int boxes = BN / box_rows;
-    const int oob = p.num_pages * ps;
-    const int Ti = (int)T;
-    const int32_t *__restrict__ pt = p.page_table + (size_t)b * p.max_pages;
-    auto lane_coord = [&](int j, int &bad) -> int {
-        if (lane >= boxes || j >= j1) return oob;
-        const int t0 = j * BN + lane * box_rows;
-        if (t0 >= Ti) return oob;
-        const int page = t0 / ps;
-        const int id = __ldg(pt + page);
-        if (id < 0 || id >= p.num_pages) {
-            bad = 1;
-            return oob;
+    const int bpt = BN / box_rows;  // TMA boxes per tile and 64-dim half
+    if (threadIdx.x == 0) {
+        for (int s2 = 0; s2 < KS; ++s2) {
+            mbar_init(&k_full[s2], 1);
+            mbar_init(&k_empty[s2], NH);
         }
-        return id * ps + (t0 - page * ps);
-    };
-    // Lane 0 issues the K (or V) boxes of one tile into one stage; lane x's
-    // coordinate is broadcast by shuffle (all lanes of warp 0 take part).
-    auto issue_boxes = [&](const CUtensorMap *map, uint8_t *dst, uint64_t *bar, int my_coord) {
-        int cs[BN / 16];
-        for (int x = 0; x < boxes; ++x) cs[x] = __shfl_sync(0xffffffffu, my_coord, x);
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar, TILE_BYTES);
-            for (int x = 0; x < boxes; ++x)
+        for (int s2 = 0; s2 < VS; ++s2) {
+            mbar_init(&v_full[s2], 1);
+            mbar_init(&v_empty[s2], NH);
+        }
+        for (int k = 0; k < NH * SB; ++k) {
+            mbar_init(&s_full[k], 1);
+            mbar_init(&p_full[k], 128);
+            mbar_init(&o_done[k], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(v_tail, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        if (p.q_tma) {
+            // rows (node, head) of this block: box = 64 dims x G heads x 128/G nodes
+            mbar_arrive_expect_tx(q_full, NH * HALF_BYTES);
+            const int nodes = 128 / p.G;
+            for (int hh = 0; hh < NH; ++hh)
                 for (int dh = 0; dh < 2; ++dh)
-                    tma_load_3d(dst + dh * ATOM_COL_BYTES + x * box_rows * 128, map, dh * 64, g,
-                                cs[x], bar);
-        }
-    };
-    auto prefetch_coord = [&](int c) {
-        if (lane < boxes && c != oob) {
-            for (int dh = 0; dh < 2; ++dh) {
-                tma_prefetch_l2_3d(&tmk, dh * 64, g, c);
-                tma_prefetch_l2_3d(&tmv, dh * 64, g, c);
-            }
-        }
-    };
-    // page coordinates of upcoming tiles, kept in a ring indexed by tile
-    int ring[CRING];
-    int bad_pages = 0;
-    int filled = j0;  // tiles [j0, filled) have their coordinates in the ring
-    if (warp == 0) {
-#pragma unroll
-        for (int k = 0; k <= PREFETCH; ++k) ring[(j0 + k) % CRING] = lane_coord(j0 + k, bad_pages);
-        filled = j0 + PREFETCH + 1;
-        const int bad0 = __reduce_or_sync(0xffffffffu, bad_pages);
-        if (lane == 0) {
-            *err_flag = bad0;
-            for (int s2 = 0; s2 < KS; ++s2) {
-                mbar_init(&k_full[s2], 1);
-                mbar_init(&k_empty[s2], 1);
-            }
-            for (int s2 = 0; s2 < VS; ++s2) {
-                mbar_init(&v_full[s2], 1);
-                mbar_init(&v_empty[s2], 1);
-            }
-            for (int k = 0; k < 2; ++k) {
-                mbar_init(&s_full[k], 1);
-                mbar_init(&p_full[k], 128);
-                mbar_init(&o_done[k], 1);
-            }
-            mbar_init(q_full, 1);
-            *abort_flag = 0;
-            mbar_fence_init();
-            if (!len_ok) atomicOr(&p.status[b], SVF_DEV_BAD_LENGTH);
-            if (j0 < j1 && p.q_tma) {
-                // rows (node, head) of this block: box = 64 dims x G heads x 128/G nodes
-                mbar_arrive_expect_tx(q_full, NH * HALF_BYTES);
-                const int nodes = 128 / p.G;
-                for (int hh = 0; hh < NH; ++hh)
-                    for (int dh = 0; dh < 2; ++dh)
-                        tma_load_4d(sQ + hh * HALF_BYTES + dh * ATOM_COL_BYTES, &tmq, dh * 64,
-                                    g * p.G, (rb * NH + hh) * nodes, b, q_full);
-            }
-        }
-        __syncwarp();
-        if (j0 < j1) {
-            const int c0 = ring[j0 % CRING];
-            issue_boxes(&tmk, sK, &k_full[0], c0);
-            issue_boxes(&tmv, sV, &v_full[0], c0);
-#pragma unroll
-            for (int k = 1; k <= PREFETCH; ++k) prefetch_coord(ring[(j0 + k) % CRING]);
+                    tma_load_4d(sQ + hh * HALF_BYTES + dh * Q_COL_BYTES, &tmq, dh * 64, g * p.G,
+                                (rb * NH + hh) * nodes, b, q_full);
         }
     }
-    if (warp == 1) {
+    if (warp == 2) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (!p.q_tma && threadIdx.x >= 64) {
+    if (!p.q_tma && warp >= SW0) {
         // Q rows -> shared memory by the softmax threads (K-major, 128-byte
         // swizzle: 16-byte chunk c of row r lands at chunk c ^ (r % 8)).
-        const int tid = threadIdx.x - 64;
+        const int tid = threadIdx.x - 32 * SW0;
         constexpr int kIters = 16;
         uint4 v[kIters];
 #pragma unroll
@@ -263,179 +248,153 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
             const int idx = tid + k * 128 * NH;
             const int row = idx >> 4, c = idx & 15;
             const int hh = row >> 7, r = row & 127, dh = c >> 3, c8 = c & 7;
-            *reinterpret_cast<uint4 *>(sQ + hh * HALF_BYTES + dh * ATOM_COL_BYTES + r * 128 +
+            *reinterpret_cast<uint4 *>(sQ + hh * HALF_BYTES + dh * Q_COL_BYTES + r * 128 +
                                        ((c8 ^ (r & 7)) << 4)) = v[k];
         }
         fence_proxy_async_smem();
     }
+    // Starting slot of every box of this chunk: a slot past the cache (which
+    // TMA fills with zeros) for boxes past the sequence or with a page id
+    // outside the cache. Every index fits in 32 bits (num_pages * page_size
+    // <= INT_MAX).
+    int bad = 0;
+    {
+        const int oob = p.num_pages * ps;
+        const int32_t *__restrict__ pt = p.page_table + (size_t)b * p.max_pages;
+        for (int idx = threadIdx.x; idx < n * bpt; idx += NTHREADS) {
+            const long long t0 = (long long)(j0 + idx / bpt) * BN + (idx % bpt) * box_rows;
+            int c = oob;
+            if (t0 < T) {
+                const int page = (int)(t0 / ps);
+                const int id = __ldg(pt + page);
+                if (id < 0 || id >= p.num_pages) bad = 1;
+                else c = id * ps + (int)(t0 - (long long)page * ps);
+            }
+            crd[idx] = c;
+        }
+    }
     tc_fence_before();
-    __syncthreads();
+    bad = __syncthreads_or(bad);
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (j0 < j1 && warp == 0) {
-        // ------------------------------------------------------------ producer
-        // K and V of every tile, each into its own ring as soon as a stage is
-        // free (polling both, K first), the page coordinates PREFETCH tiles
-        // ahead of the next K tile, and those tiles pulled into L2.
-        int kj = j0 + 1, vj = j0 + 1;  // next tiles to issue
-        int bad = bad_pages;
-        // one page-table load in flight: its coordinate is stored (and its
-        // boxes prefetched) at the next K issue, when the load has landed
-        int pending_tile = -1, pending = oob;
-        unsigned long long t_last = globaltimer_ns();
-        while ((kj < j1 || vj < j1) && !*abort_flag) {
-            bool progressed = false;
-            if (kj < j1) {
-                const int it = kj - j0, st = it % KS, use = it / KS;
-                bool free_ = use == 0 || mbar_test_wait(&k_empty[st], (use - 1) & 1);
-                free_ = __shfl_sync(0xffffffffu, free_, 0);
-                if (free_) {
-                    issue_boxes(&tmk, sK + st * TILE_BYTES, &k_full[st], ring[kj % CRING]);
-                    ++kj;
-                    if (pending_tile >= 0) {
-                        ring[pending_tile % CRING] = pending;
-                        prefetch_coord(pending);
-                    }
-                    pending_tile = filled;
-                    pending = lane_coord(filled, bad);
-                    ++filled;
-                    progressed = true;
-                }
+    if (warp <= 1) {
+        // ------------------------------------------------------------ producers
+        // Warp 0 streams K, warp 1 streams V, each into its ring as soon as a
+        // stage is free; lane x < bpt issues box x of both 64-dim halves.
+        const bool is_k = warp == 0;
+        const CUtensorMap *map = is_k ? &tmk : &tmv;
+        uint8_t *ring = is_k ? sK : sV;
+        uint64_t *full = is_k ? k_full : v_full;
+        uint64_t *empty = is_k ? k_empty : v_empty;
+        const int stages = is_k ? KS : VS;
+        int j = 0;  // tiles issued
+        for (; j < n; ++j) {
+            const int st = j % stages, use = j / stages;
+            if (use > 0 && !warp_wait(&empty[st], (uint32_t)((use - 1) & 1), abort_flag)) break;
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], TILE_BYTES);
+            if (lane < bpt) {
+                const int c = crd[j * bpt + lane];
+#pragma unroll
+                for (int dh = 0; dh < 2; ++dh)
+                    tma_load_3d(ring + st * TILE_BYTES + dh * KV_COL_BYTES + lane * box_rows * 128,
+                                map, dh * 64, g, c, &full[st]);
             }
-            if (vj < kj && vj < j1) {
-                const int it = vj - j0, st = it % VS, use = it / VS;
-                bool free_ = use == 0 || mbar_test_wait(&v_empty[st], (use - 1) & 1);
-                free_ = __shfl_sync(0xffffffffu, free_, 0);
-                if (free_) {
-                    issue_boxes(&tmv, sV + st * TILE_BYTES, &v_full[st], ring[vj % CRING]);
-                    ++vj;
-                    progressed = true;
+            __syncwarp();
+        }
+        const int kj = is_k ? j : 0, vj = is_k ? 0 : j;
+        // V rows past the sequence end may hold anything (NaN included, and
+        // P = 0 does not cancel NaN): zero them in the last tile, then let the
+        // PV issuers in through v_tail.
+        const long long tbl = (long long)(j0 + n - 1) * BN;
+        if (!is_k && tbl + BN > T && vj == n) {
+            const int jl = n - 1;
+            if (warp_wait(&v_full[jl % VS], (uint32_t)((jl / VS) & 1), abort_flag)) {
+                const int r0 = (int)(T - tbl);
+                uint8_t *vs = sV + (jl % VS) * TILE_BYTES;
+                for (int idx = lane; idx < (BN - r0) * 16; idx += 32) {
+                    const int r = r0 + (idx >> 4), c = idx & 15;
+                    *reinterpret_cast<uint4 *>(vs + (c >> 3) * KV_COL_BYTES + r * 128 +
+                                               (c & 7) * 16) = make_uint4(0, 0, 0, 0);
                 }
-            }
-            if (progressed) {
-                t_last = globaltimer_ns();
-            } else {
-                __nanosleep(64);
-                if (globaltimer_ns() - t_last > kWaitDeadlineNs) {
-                    if (lane == 0) *abort_flag = 1;
-                    break;
-                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(v_tail);
             }
         }
-        bad = __reduce_or_sync(0xffffffffu, bad);
         if (lane == 0) {
-            if (bad || *err_flag) {
-                *err_flag = 1;
-                atomicOr(&p.status[b], SVF_DEV_BAD_PAGE);
-            }
             // Never leave with copies in flight: wait (bounded, ignoring the
-            // abort flag) for the last use of every stage that was loaded.
+            // abort flag) for the last fill of every stage that was loaded.
             volatile int never = 0;
-            const int nk = kj - j0, nv = vj - j0;
-            for (int st = 0; st < KS && st < nk; ++st)
-                mbar_wait(&k_full[st], ((nk - 1 - st) / KS) & 1, &never);
-            for (int st = 0; st < VS && st < nv; ++st)
-                mbar_wait(&v_full[st], ((nv - 1 - st) / VS) & 1, &never);
-            if (p.q_tma) mbar_wait(q_full, 0, &never);
+            for (int st = 0; st < KS && st < kj; ++st)
+                mbar_wait(&k_full[st], ((kj - 1 - st) / KS) & 1, &never);
+            for (int st = 0; st < VS && st < vj; ++st)
+                mbar_wait(&v_full[st], ((vj - 1 - st) / VS) & 1, &never);
+            if (is_k && p.q_tma) mbar_wait(q_full, 0, &never);
         }
-    } else if (j0 < j1 && warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
-            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-            // S_slot = Q_h K^T
-            auto issue_qk = [&](int stage, int h, int slot) {
-                const uint32_t d = tmem + slot * 128;
+    } else if (warp <= 1 + NH) {
+        // ------------------------------------------------------------ QK issuer, half h
+        // S_h,b = Q_h K^T for every tile, into the buffer whose previous PV is done.
+        const int h = warp - 2;
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, false, false);
+        const uint32_t aQ = smem_u32(sQ) + h * HALF_BYTES, aK = smem_u32(sK);
+        bool ok = !p.q_tma || warp_wait(q_full, 0, abort_flag);
+        for (int t = 0; ok && t < n; ++t) {
+            const int bb = t % SB;
+            if (!(ok = warp_wait(&k_full[t % KS], (uint32_t)((t / KS) & 1), abort_flag))) break;
+            if (t >= SB) {
+                // PV(t - SB) of this half read P from this S buffer
+                const int pj = t - SB;
+                if (!(ok = warp_wait(&o_done[h * SB + bb], (uint32_t)((pj / SB) & 1), abort_flag)))
+                    break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t d = tmem + (uint32_t)((h * SB + bb) * BN);
+                const uint32_t kst = aK + (t % KS) * TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * ATOM_COL_BYTES + (kk & 3) * 32;
-                    umma_ss(d, smem_desc_sw128(aQ + h * HALF_BYTES + off, 16, 1024),
-                            smem_desc_sw128(aK + stage * TILE_BYTES + off, 16, 1024), idesc_qk,
-                            kk > 0);
+                    const uint32_t oq = (kk >> 2) * Q_COL_BYTES + (kk & 3) * 32;
+                    const uint32_t ok_ = (kk >> 2) * KV_COL_BYTES + (kk & 3) * 32;
+                    umma_ss(d, smem_desc_sw128(aQ + oq, 16, 1024),
+                            smem_desc_sw128(kst + ok_, 16, 1024), idesc_qk, kk > 0);
                 }
-                umma_commit(&s_full[slot]);
-            };
-            // O_h += P_slot V
-            auto issue_pv = [&](int stage, int h, int slot, bool first) {
+                umma_commit(&s_full[h * SB + bb]);
+                umma_commit(&k_empty[t % KS]);
+            }
+            __syncwarp();
+        }
+    } else if (warp <= 1 + 2 * NH) {
+        // ------------------------------------------------------------ PV issuer, half h
+        // O_h += P_h,b V for every tile once its softmax is done.
+        const int h = warp - 2 - NH;
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+        const uint32_t aV = smem_u32(sV);
+        bool ok = true;
+        for (int j = 0; ok && j < n; ++j) {
+            const int bb = j % SB;
+            const bool tail = (long long)(j0 + j) * BN + BN > T;  // the sequence's last tile
+            ok = tail ? warp_wait(v_tail, 0, abort_flag)
+                      : warp_wait(&v_full[j % VS], (uint32_t)((j / VS) & 1), abort_flag);
+            if (!ok) break;
+            if (!(ok = warp_wait(&p_full[h * SB + bb], (uint32_t)((j / SB) & 1), abort_flag))) break;
+            tc_fence_after();
+            if (lane == 0) {
                 const uint32_t d = tmem + 256 + h * 128;
-                const uint32_t a = tmem + slot * 128;
+                const uint32_t a = tmem + (uint32_t)((h * SB + bb) * BN);
+                const uint32_t vst = aV + (j % VS) * TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ts(d, a + kk * 8,
-                            smem_desc_sw128(aV + stage * TILE_BYTES + kk * 2048, ATOM_COL_BYTES,
-                                            1024),
-                            idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                umma_commit(&o_done[slot]);
-            };
-            auto kst = [&](int it) { return it % KS; };
-            auto kph = [&](int it) { return (uint32_t)((it / KS) & 1); };
-            auto vst = [&](int it) { return it % VS; };
-            auto vph = [&](int it) { return (uint32_t)((it / VS) & 1); };
-            bool ok = !p.q_tma || mbar_wait(q_full, 0, abort_flag);
-            if (NH == 2) {
-                // Ping-pong: PV(h0, j), QK(h0, j+1), PV(h1, j), QK(h1, j+1), so
-                // one half's softmax overlaps the other half's MMAs. A slot's S
-                // (and the P written over it) is reused only after its PV is done.
-                ok = ok && mbar_wait(&k_full[kst(0)], kph(0), abort_flag);
-                if (ok) {
-                    tc_fence_after();
-                    issue_qk(kst(0), 0, 0);
-                    issue_qk(kst(0), 1, 1);
-                    umma_commit(&k_empty[kst(0)]);
-                }
-                for (int j = j0; ok && j < j1; ++j) {
-                    const int it = j - j0;
-                    const bool more = j + 1 < j1;
-                    if (!(ok = mbar_wait(&v_full[vst(it)], vph(it), abort_flag))) break;
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        if (!(ok = mbar_wait(&p_full[h], it & 1, abort_flag))) break;
-                        tc_fence_after();
-                        issue_pv(vst(it), h, h, it == 0);
-                        if (h == 1) umma_commit(&v_empty[vst(it)]);
-                        if (more) {
-                            if (h == 0 &&
-                                !(ok = mbar_wait(&k_full[kst(it + 1)], kph(it + 1), abort_flag)))
-                                break;
-                            if (!(ok = mbar_wait(&o_done[h], it & 1, abort_flag))) break;
-                            tc_fence_after();
-                            issue_qk(kst(it + 1), h, h);
-                            if (h == 1) umma_commit(&k_empty[kst(it + 1)]);
-                        }
-                    }
-                }
-            } else {
-                // One half, S double-buffered: QK(j + 2) goes into the slot PV(j)
-                // has just finished reading, while the softmax works on tile j + 1.
-                for (int k = 0; k < 2 && ok && j0 + k < j1; ++k) {
-                    if (!(ok = mbar_wait(&k_full[kst(k)], kph(k), abort_flag))) break;
-                    tc_fence_after();
-                    issue_qk(kst(k), 0, k);
-                    umma_commit(&k_empty[kst(k)]);
-                }
-                for (int j = j0; ok && j < j1; ++j) {
-                    const int it = j - j0, slot = it & 1;
-                    const uint32_t sph = (uint32_t)((it >> 1) & 1);
-                    if (!(ok = mbar_wait(&v_full[vst(it)], vph(it), abort_flag))) break;
-                    if (!(ok = mbar_wait(&p_full[slot], sph, abort_flag))) break;
-                    tc_fence_after();
-                    issue_pv(vst(it), 0, slot, it == 0);
-                    umma_commit(&v_empty[vst(it)]);
-                    if (j + 2 < j1) {
-                        if (!(ok = mbar_wait(&k_full[kst(it + 2)], kph(it + 2), abort_flag)))
-                            break;
-                        if (!(ok = mbar_wait(&o_done[slot], sph, abort_flag))) break;
-                        tc_fence_after();
-                        issue_qk(kst(it + 2), 0, slot);
-                        umma_commit(&k_empty[kst(it + 2)]);
-                    }
-                }
+                    umma_ts(d, a + kk * 8, smem_desc_sw128(vst + kk * 2048, KV_COL_BYTES, 1024),
+                            idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&o_done[h * SB + bb]);
+                umma_commit(&v_empty[j % VS]);
             }
+            __syncwarp();
         }
-    } else if (warp >= 2) {
+    } else {
         // ------------------------------------------------------------ softmax
-        const int h = (warp - 2) >> 2;
+        const int h = (warp - SW0) >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const int R = rb * 128 * NH + h * 128 + r;
@@ -448,59 +407,51 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY, l = 0.0f;
         bool ok = true;
-        for (int j = j0; j < j1; ++j) {
-            const int it = j - j0, s = it % VS, use = it / VS;
-            // S slot of this tile and the parity of its barriers
-            const int slot = NH == 2 ? h : (it & 1);
-            const uint32_t sph = NH == 2 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
-            const uint32_t tS = tmem + lane_off + slot * 128;
-            if (!(ok = warp_wait(&s_full[slot], sph, abort_flag))) break;
+        for (int j = 0; j < n; ++j) {
+            const int bb = j % SB;
+            const uint32_t bph = (uint32_t)((j / SB) & 1);
+            const uint32_t tS = tmem + lane_off + (uint32_t)((h * SB + bb) * BN);
+            if (!(ok = warp_wait(&s_full[h * SB + bb], bph, abort_flag))) break;
             tc_fence_after();
-            const long long tbase = (long long)j * BN;
-            const bool masked_tile = tbase + BN > L;  // this tile reaches the tree
-            // pass 1: row max of the visible scores, two 64-column halves
+            uint32_t v[BN];
+            tmem_ld32(tS, v);
+            tmem_ld32(tS + 32, v + 32);
+            tmem_wait_ld();
+            const long long tbase = (long long)(j0 + j) * BN;
+            if (tbase + BN > L) {
+                // this tile reaches the tree: ancestors only
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const uint32_t vis = visible_bits(tbase + 32 * c2 - L, anc);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        v[32 * c2 + c] = ((vis >> c) & 1u) ? v[32 * c2 + c] : 0xff800000u;
+                }
+            }
             float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll 1
-            for (int c64 = 0; c64 < 2; ++c64) {
-                uint32_t v[64];
-                tmem_ld32(tS + c64 * 64, v);
-                tmem_ld32(tS + c64 * 64 + 32, v + 32);
-                tmem_wait_ld();
-                if (masked_tile) {
 #pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        const uint32_t vis = visible_bits(tbase + 64 * c64 + 32 * c2 - L, anc);
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            v[32 * c2 + c] = ((vis >> c) & 1u) ? v[32 * c2 + c] : 0xff800000u;
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 64; c += 4) {
-                    m0 = fmaxf(m0, __uint_as_float(v[c]));
-                    m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
-                    m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
-                    m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
-                }
+            for (int c = 0; c < BN; c += 4) {
+                m0 = fmaxf(m0, __uint_as_float(v[c]));
+                m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
+                m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
+                m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
             }
             const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
             // lazy rescale: move the reference max only when it grows by > 2^8
             const bool need = mx > m_ref + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
+            if (__any_sync(FULL, need)) {
                 const float alpha = need ? ex2_approx(m_ref - mx) : 1.0f;
                 if (need) {
                     l *= alpha;
                     m_ref = mx;
                 }
-                if (it > 0) {
-                    if (NH == 1) {
-                        // O is being accumulated by PV(j - 1) on the other slot
-                        const int pit = it - 1;
-                        if (!(ok = warp_wait(&o_done[pit & 1], (uint32_t)((pit >> 1) & 1),
-                                             abort_flag)))
-                            break;
-                        tc_fence_after();
-                    }
+                if (j > 0) {
+                    // O is final up to PV(j - 1) of this half
+                    const int pj = j - 1;
+                    if (!(ok = warp_wait(&o_done[h * SB + pj % SB], (uint32_t)((pj / SB) & 1),
+                                         abort_flag)))
+                        break;
+                    tc_fence_after();
 #pragma unroll 1
                     for (int c4 = 0; c4 < 4; ++c4) {
                         uint32_t o[32];
@@ -514,70 +465,35 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
                     tmem_wait_st();
                 }
             }
-            // pass 2: P = 2^(s*scale - m_ref) as bf16 pairs; the 32 packed
-            // columns of half c64 go over S columns [32 c64, 32 c64 + 32),
-            // which pass 2 has already read
+            // P = 2^(s*scale - m_ref) as bf16 pairs over the first 32 S columns
             const float mneg = m_ref == -INFINITY ? 0.0f : -m_ref;
             float r0 = 0.0f, r1 = 0.0f;
-#pragma unroll 1
-            for (int c64 = 0; c64 < 2; ++c64) {
-                uint32_t v[64];
-                tmem_ld32(tS + c64 * 64, v);
-                tmem_ld32(tS + c64 * 64 + 32, v + 32);
-                tmem_wait_ld();
-                if (masked_tile) {
+            uint32_t pk[BN / 2];
 #pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        const uint32_t vis = visible_bits(tbase + 64 * c64 + 32 * c2 - L, anc);
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            v[32 * c2 + c] = ((vis >> c) & 1u) ? v[32 * c2 + c] : 0xff800000u;
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * c]), sl2, mneg));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * c + 1]), sl2, mneg));
-                    r0 += p0;
-                    r1 += p1;
-                    v[c] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(tS + c64 * 32, v);
+            for (int c = 0; c < BN / 2; ++c) {
+                const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * c]), sl2, mneg));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * c + 1]), sl2, mneg));
+                r0 += p0;
+                r1 += p1;
+                pk[c] = pack_bf16x2(p0, p1);
             }
+            tmem_st32(tS, pk);
             tmem_wait_st();
             l += r0 + r1;
-            // V rows past the sequence end may hold anything: zero them before PV.
-            if (h == 0 && tbase + BN > T) {
-                if (!(ok = warp_wait(&v_full[s], use & 1, abort_flag))) break;
-                if (tbase + r >= T) {
-                    uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int dh = 0; dh < 2; ++dh)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(sV + s * TILE_BYTES + dh * ATOM_COL_BYTES +
-                                                       r * 128 + c * 16) = z;
-                }
-                fence_proxy_async_smem();
-            }
             tc_fence_before();
-            mbar_arrive(&p_full[slot]);
+            mbar_arrive(&p_full[h * SB + bb]);
         }
-        // epilogue
-        if (ok && j0 < j1) {
-            const int lit = j1 - j0 - 1;  // the last PV of this half
-            ok = NH == 2 ? warp_wait(&o_done[h], (uint32_t)(lit & 1), abort_flag)
-                         : warp_wait(&o_done[lit & 1], (uint32_t)((lit >> 1) & 1), abort_flag);
-        }
+        // epilogue: O of this half after its last PV
+        if (ok) ok = warp_wait(&o_done[h * SB + (n - 1) % SB], (uint32_t)(((n - 1) / SB) & 1),
+                               abort_flag);
         tc_fence_after();
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const float lse_v =
-            l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        const float lse_v = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         const size_t row = ((size_t)b * p.N + node) * p.Hq + hq;
 #pragma unroll 1
         for (int c64 = 0; c64 < 2; ++c64) {
             uint32_t o[64];
-            if (j0 < j1 && ok) {
+            if (ok) {
                 tmem_ld32(tO + c64 * 64, o);
                 tmem_ld32(tO + c64 * 64 + 32, o + 32);
                 tmem_wait_ld();
@@ -609,42 +525,49 @@ __global__ void __launch_bounds__(64 + 128 * NH, 1)
         }
         if (row_valid) {
             if (p.splits == 1) {
-                if (p.lse) p.lse[row] = (j0 < j1) ? lse_v : 0.0f;
+                if (p.lse) p.lse[row] = lse_v;
             } else {
-                p.part_lse[(size_t)split * p.B * p.N * p.Hq + row] = (j0 < j1) ? lse_v : -INFINITY;
+                p.part_lse[(size_t)split * p.B * p.N * p.Hq + row] = lse_v;
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 0 && *abort_flag) atomicOr(&p.status[b], SVF_DEV_TIMEOUT);
-    // With a single split this CTA wrote final outputs: a sequence with a bad
+    if (threadIdx.x == 0) {
+        if (*abort_flag) atomicOr(&p.status[b], SVF_DEV_TIMEOUT);
+        if (bad) atomicOr(&p.status[b], SVF_DEV_BAD_PAGE);
+    }
+    // With a single chunk this CTA wrote final outputs: a sequence with a bad
     // page gets zeros (every CTA of the sequence saw the same page table).
-    if (p.splits == 1 && *err_flag && warp >= 2) {
-        const int h = (warp - 2) >> 2;
+    if (p.splits == 1 && bad && warp >= SW0) {
+        const int h = (warp - SW0) >> 2;
         const int R = rb * 128 * NH + h * 128 + (warp & 3) * 32 + lane;
         if (R < p.M) {
             const size_t row = ((size_t)b * p.N + R / p.G) * p.Hq + g * p.G + R % p.G;
-            uint4 z = make_uint4(0, 0, 0, 0);
+            const uint4 z = make_uint4(0, 0, 0, 0);
             for (int k = 0; k < HD / 8; ++k)
                 *reinterpret_cast<uint4 *>(p.out + row * HD + 8 * k) = z;
             if (p.lse) p.lse[row] = 0.0f;
         }
     }
+    (void)err_flag;
 }
 
-// Merge split partials: lse = log sum_s e^{lse_s}, out = sum_s e^{lse_s - lse} o_s.
-// One warp per (sequence, node, head) row; lane s holds split s's lse (and
-// s + 32's), and the partial rows are loaded eight splits at a time so their
-// latencies overlap. A sequence with any status bit set gets zeros.
+// Merge chunk partials: lse = log sum_s e^{lse_s}, out = sum_s e^{lse_s - lse} o_s,
+// over the chunks that hold tiles of the sequence (ceil(tiles / chunk) of
+// them). One warp per (sequence, node, head) row; lane s holds chunk s's lse
+// (and s + 32's), and the partial rows are loaded eight chunks at a time so
+// their latencies overlap. A sequence with any status bit set gets zeros.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restrict__ part_o,
                                                            const float *__restrict__ part_lse,
-                                                           int splits, long long rows, int per_b,
+                                                           long long rows, int per_b, int N,
+                                                           int chunk,
+                                                           const int32_t *__restrict__ seq_lens,
                                                            const int32_t *__restrict__ status,
                                                            __nv_bfloat16 *__restrict__ out,
                                                            float *__restrict__ lse) {
@@ -655,6 +578,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restri
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lse_out = 0.0f;
     if (status[b] == 0) {
+        const long long T = (long long)seq_lens[b] + N;
+        const int tiles = (int)((T + tc::BN - 1) / tc::BN);
+        const int splits = (tiles + chunk - 1) / chunk;
         const float l0 = lane < splits ? part_lse[(size_t)lane * rows + row] : -INFINITY;
         const float l1 = lane + 32 < splits ? part_lse[(size_t)(lane + 32) * rows + row] : -INFINITY;
         const float mx = warp_max(fmaxf(l0, l1));
@@ -740,6 +666,10 @@ static bool make_q_map(CUtensorMap *map, const void *q, int B, int N, int Hq, in
 
 static int row_halves(int M) { return M > 128 ? 2 : 1; }
 
+// Chunk count of the KV range per (sequence, KV head, row block): minimises
+// max(waves x (tiles per chunk + fixed cost), total bytes / bandwidth), where
+// the bytes count the partial outputs written and read back, with at most
+// CMAX_TILES tiles per chunk.
 int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) {
     const int G = Hq / Hkv;
     const int M = N * G;
@@ -749,15 +679,16 @@ int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) 
     const long long kv_max = (long long)max_pages * page_size;
     const int tiles = (int)((kv_max + tc::BN - 1) / tc::BN);
     const int C = num_sms();
-    // partial output write + read per split and unit, in units of one KV tile
+    // partial output write + read per chunk and unit, in units of one K+V tile
     const double part_tiles = (double)(128 * NH) * (tc::HD + 1) * 4 * 2 / (2.0 * tc::TILE_BYTES);
     double best = 1e300;
     int best_s = 1;
     const int smax = tiles < 64 ? tiles : 64;
     for (int s = 1; s <= smax; ++s) {
-        const long long waves = (units * s + C - 1) / C;
         const int per_cta = (tiles + s - 1) / s;
-        const double t_chain = (double)waves * (per_cta + 1.0) + (s > 1 ? 0.5 : 0.0);
+        if (per_cta > tc::CMAX_TILES) continue;
+        const long long waves = (units * s + C - 1) / C;
+        const double t_chain = (double)waves * (per_cta + tc::kFixedTiles);
         const double t_bytes = (double)units * (tiles + (s > 1 ? s * part_tiles : 0.0)) / C;
         const double t = t_chain > t_bytes ? t_chain : t_bytes;
         if (t < best - 1e-9) {
@@ -766,6 +697,18 @@ int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) 
         }
     }
     return best_s;
+}
+
+static int attn_tc_chunk(int splits, int max_pages, int page_size) {
+    const long long kv_max = (long long)max_pages * page_size;
+    const int tiles = (int)((kv_max + tc::BN - 1) / tc::BN);
+    return (tiles + splits - 1) / splits;
+}
+
+bool attn_tc_supported(int max_pages, int page_size) {
+    const long long kv_max = (long long)max_pages * page_size;
+    const int tiles = (int)((kv_max + tc::BN - 1) / tc::BN);
+    return tiles <= 64 * tc::CMAX_TILES;
 }
 
 size_t attn_tc_workspace_bytes(int B, int N, int Hq, int Hkv, int max_pages, int page_size) {
@@ -780,7 +723,9 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
     const int M = a.N * G;
     const int NH = row_halves(M);
     const int row_blocks = (M + 128 * NH - 1) / (128 * NH);
+    if (!attn_tc_supported(a.max_pages, a.page_size)) return SVF_ERR_UNSUPPORTED;
     const int splits = attn_tc_splits(a.B, a.N, a.Hq, a.Hkv, a.max_pages, a.page_size);
+    const int chunk = attn_tc_chunk(splits, a.max_pages, a.page_size);
     const size_t need = attn_tc_workspace_bytes(a.B, a.N, a.Hq, a.Hkv, a.max_pages, a.page_size);
     if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SVF_ERR_WORKSPACE;
 
@@ -804,6 +749,7 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
     p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.M = M;
     p.num_pages = a.num_pages; p.page_size = a.page_size; p.max_pages = a.max_pages;
     p.splits = splits;
+    p.chunk = chunk;
     p.row_blocks = row_blocks;
     p.q_tma = q_tma ? 1 : 0;
     const float scale = a.sm_scale > 0.0f ? a.sm_scale : 1.0f / sqrtf((float)a.D);
@@ -821,22 +767,23 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
     }
     p.status = a.status;
 
-    dim3 grid(splits, a.Hkv * row_blocks, a.B);
+    dim3 grid(a.Hkv * row_blocks, splits, a.B);
     if (NH == 1) {
         const int smem = TcSmem<1>::kDynamic;
         cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        attn_tc_kernel<1><<<grid, 64 + 128, smem, stream>>>(tmk, tmv, tmq, p);
+        attn_tc_kernel<1><<<grid, tc::threads_for(1), smem, stream>>>(tmk, tmv, tmq, p);
     } else {
         const int smem = TcSmem<2>::kDynamic;
         cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        attn_tc_kernel<2><<<grid, 64 + 256, smem, stream>>>(tmk, tmv, tmq, p);
+        attn_tc_kernel<2><<<grid, tc::threads_for(2), smem, stream>>>(tmk, tmv, tmq, p);
     }
     if (cudaGetLastError() != cudaSuccess) return SVF_ERR_LAUNCH;
     if (splits > 1) {
         const long long threads = (long long)rows * 32;
         const int blocks = (int)((threads + 255) / 256);
-        attn_combine_kernel<<<blocks, 256, 0, stream>>>(
-            p.part_o, p.part_lse, splits, (long long)rows, a.N * a.Hq, a.status, p.out, a.lse);
+        attn_combine_kernel<<<blocks, 256, 0, stream>>>(p.part_o, p.part_lse, (long long)rows,
+                                                        a.N * a.Hq, a.N, chunk, a.seq_lens,
+                                                        a.status, p.out, a.lse);
         if (cudaGetLastError() != cudaSuccess) return SVF_ERR_LAUNCH;
     }
     return SVF_OK;

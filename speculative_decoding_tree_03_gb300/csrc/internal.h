@@ -36,6 +36,7 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t stream);
 // Tensor-core path for bf16 (attn_tc.cu).
 size_t attn_tc_workspace_bytes(int B, int N, int Hq, int Hkv, int max_pages, int page_size);
 int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size);
+bool attn_tc_supported(int max_pages, int page_size);
 int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 // Acceptance walk (accept.cu): rows of the visited nodes held in the registers
