@@ -222,6 +222,8 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
     float *G = reinterpret_cast<float *>(snext + N);    // [NG] group sums of the last pass
     __shared__ WalkSmem ws;
 
+    pdl_wait();
+    pdl_launch_dependents();
     // the root's rows go out first: their latency hides behind the set-up
     float4 P[E4], Q[E4];
     load_slice<E4, VEC>(target + base * V, V, g0, lane, P);
@@ -666,30 +668,14 @@ cudaError_t launch_walk(const WalkCfg &c, const float *target, const float *draf
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    if (!CLUSTER) {
-        kern<<<(unsigned)B, NT, smem, stream>>>(target, draft, tokens, parent, u_accept, u_bonus,
-                                                 N, V, 1, accept_len, path, out_tokens, ratio,
-                                                 status);
-        return cudaGetLastError();
-    }
-    if (c.cl > 8) {
+    if (CLUSTER && c.cl > 8) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((long long)B * c.cl), 1, 1);
-    cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)c.cl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, target, draft, tokens, parent, u_accept, u_bonus, N, V,
-                              c.cl, accept_len, path, out_tokens, ratio, status);
+    const unsigned blocks = (unsigned)((long long)B * (CLUSTER ? c.cl : 1));
+    return launch_pdl(kern, dim3(blocks), dim3(NT), smem, stream, CLUSTER ? (unsigned)c.cl : 0u,
+                      target, draft, tokens, parent, u_accept, u_bonus, N, V, CLUSTER ? c.cl : 1,
+                      accept_len, path, out_tokens, ratio, status);
 }
 
 template <bool VEC>

@@ -107,8 +107,7 @@ int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache
     if (D != 128 || !tc_page_size_ok(page_size)) return SVF_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return SVF_ERR_ARG;
-    if (cudaMemsetAsync(status, 0, sizeof(int32_t) * (size_t)B, s) != cudaSuccess)
-        return SVF_ERR_LAUNCH;
+    // the kernel stores every sequence's status word itself
     return launch_attn_tc(a, workspace, workspace_bytes, s);
 }
 

@@ -163,6 +163,11 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     const int rb = blockIdx.x % p.row_blocks;
     const int split = blockIdx.y;
     const int b = blockIdx.z;
+    // One CTA per sequence owns its status word and stores it whole; other
+    // CTAs only add SVF_DEV_TIMEOUT, which takes seconds to arise.
+    const bool designated = g == 0 && rb == 0 && split == 0;
+    pdl_wait();
+    pdl_launch_dependents();
 
     const int L = p.seq_lens[b];
     const long long T = (long long)L + p.N;
@@ -174,8 +179,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     if (n <= 0) {
         // No tile here. The first chunk reports a bad length; with a single
         // chunk this CTA owns final outputs, which are zeros then.
-        if (split == 0 && !len_ok && threadIdx.x == 0 && rb == 0 && g == 0)
-            atomicOr(&p.status[b], SVF_DEV_BAD_LENGTH);
+        if (designated && threadIdx.x == 0) p.status[b] = SVF_DEV_BAD_LENGTH;
         if (p.splits == 1 && threadIdx.x < 128 * NH) {
             const int R = rb * 128 * NH + threadIdx.x;
             if (R < p.M) {
@@ -257,10 +261,18 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     // TMA fills with zeros) for boxes past the sequence or with a page id
     // outside the cache. Every index fits in 32 bits (num_pages * page_size
     // <= INT_MAX).
-    int bad = 0;
+    int bad = 0, bad_seq = 0;
     {
         const int oob = p.num_pages * ps;
         const int32_t *__restrict__ pt = p.page_table + (size_t)b * p.max_pages;
+        if (designated) {
+            // every page the sequence uses, for its status word
+            const int npg = (int)((T + ps - 1) / ps);
+            for (int i = threadIdx.x; i < npg; i += NTHREADS) {
+                const int id = __ldg(pt + i);
+                if (id < 0 || id >= p.num_pages) bad_seq = 1;
+            }
+        }
         for (int idx = threadIdx.x; idx < n * bpt; idx += NTHREADS) {
             const long long t0 = (long long)(j0 + idx / bpt) * BN + (idx % bpt) * box_rows;
             int c = oob;
@@ -273,6 +285,8 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
             crd[idx] = c;
         }
     }
+    bad_seq = __syncthreads_or(bad_seq);
+    if (designated && threadIdx.x == 0) p.status[b] = bad_seq ? SVF_DEV_BAD_PAGE : 0;
     tc_fence_before();
     bad = __syncthreads_or(bad);
     tc_fence_after();
@@ -538,10 +552,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 0) {
-        if (*abort_flag) atomicOr(&p.status[b], SVF_DEV_TIMEOUT);
-        if (bad) atomicOr(&p.status[b], SVF_DEV_BAD_PAGE);
-    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&p.status[b], SVF_DEV_TIMEOUT);
     // With a single chunk this CTA wrote final outputs: a sequence with a bad
     // page gets zeros (every CTA of the sequence saw the same page table).
     if (p.splits == 1 && bad && warp >= SW0) {
@@ -571,6 +582,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restri
                                                            const int32_t *__restrict__ status,
                                                            __nv_bfloat16 *__restrict__ out,
                                                            float *__restrict__ lse) {
+    pdl_wait();
+    pdl_launch_dependents();
     const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -771,20 +784,25 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
     if (NH == 1) {
         const int smem = TcSmem<1>::kDynamic;
         cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        attn_tc_kernel<1><<<grid, tc::threads_for(1), smem, stream>>>(tmk, tmv, tmq, p);
+        if (launch_pdl(attn_tc_kernel<1>, grid, dim3(tc::threads_for(1)), smem, stream, 0u, tmk,
+                       tmv, tmq, p) != cudaSuccess)
+            return SVF_ERR_LAUNCH;
     } else {
         const int smem = TcSmem<2>::kDynamic;
         cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        attn_tc_kernel<2><<<grid, tc::threads_for(2), smem, stream>>>(tmk, tmv, tmq, p);
+        if (launch_pdl(attn_tc_kernel<2>, grid, dim3(tc::threads_for(2)), smem, stream, 0u, tmk,
+                       tmv, tmq, p) != cudaSuccess)
+            return SVF_ERR_LAUNCH;
     }
     if (cudaGetLastError() != cudaSuccess) return SVF_ERR_LAUNCH;
     if (splits > 1) {
         const long long threads = (long long)rows * 32;
         const int blocks = (int)((threads + 255) / 256);
-        attn_combine_kernel<<<blocks, 256, 0, stream>>>(p.part_o, p.part_lse, (long long)rows,
-                                                        a.N * a.Hq, a.N, chunk, a.seq_lens,
-                                                        a.status, p.out, a.lse);
-        if (cudaGetLastError() != cudaSuccess) return SVF_ERR_LAUNCH;
+        if (launch_pdl(attn_combine_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, 0u,
+                       (const float *)p.part_o, (const float *)p.part_lse, (long long)rows,
+                       a.N * a.Hq, a.N, chunk, a.seq_lens, (const int32_t *)a.status, p.out,
+                       a.lse) != cudaSuccess)
+            return SVF_ERR_LAUNCH;
     }
     return SVF_OK;
 }

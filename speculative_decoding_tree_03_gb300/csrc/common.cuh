@@ -138,6 +138,17 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Kernels of this library are launched with programmatic stream
+// serialization: a kernel may start while the previous kernel on the stream
+// finishes. Each one waits (griddepcontrol.wait) before its first access to
+// global memory, which returns once the previous grid has completed and its
+// writes are visible, and lets the next kernel start launching early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(1024) tree_mask_kernel(const int32_t *__restri
                                                          int32_t *__restrict__ status) {
     extern __shared__ int32_t sp[];
     const int b = blockIdx.x;
+    pdl_wait();
+    pdl_launch_dependents();
     const int32_t *par = parent + (size_t)b * N;
     int bad = 0;
     for (int i = threadIdx.x; i < N; i += blockDim.x) {
@@ -53,9 +55,8 @@ cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint64_t *anc,
     const int W = (N + 63) / 64;
     int threads = ((N + 31) / 32) * 32;
     if (threads > 1024) threads = 1024;
-    tree_mask_kernel<<<B, threads, N * sizeof(int32_t), stream>>>(parent, N, W, anc, depth,
-                                                                  status);
-    return cudaGetLastError();
+    return launch_pdl(tree_mask_kernel, dim3((unsigned)B), dim3((unsigned)threads),
+                      N * sizeof(int32_t), stream, 0u, parent, N, W, anc, depth, status);
 }
 
 }  // namespace svf
