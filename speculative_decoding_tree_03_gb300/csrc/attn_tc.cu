@@ -46,7 +46,6 @@ namespace svf {
 namespace tc {
 constexpr int BN = 64;                      // KV tokens per tile
 constexpr int HD = 128;                     // head_dim
-constexpr int SB = 2;                       // S buffers per row half
 constexpr int HALF_BYTES = 128 * HD * 2;    // 32 KB of Q per 128-row half
 constexpr int Q_COL_BYTES = 128 * 128;      // one 64-dim block of 128 Q rows
 constexpr int TILE_BYTES = BN * HD * 2;     // 16 KB per K or V tile
@@ -60,6 +59,9 @@ constexpr int MAX_BOXES = CMAX_TILES * (BN / 16);
 // comes after the next tile's QK), so V gets the extra stage.
 __host__ __device__ constexpr int kstages_for(int NH) { return NH == 1 ? 5 : 4; }
 __host__ __device__ constexpr int vstages_for(int NH) { return NH == 1 ? 6 : 5; }
+// S buffers per row half: 2 x 2 x 64 columns of S plus 2 x 128 of O fill the
+// 512 TMEM columns with two halves; one half has room for four.
+__host__ __device__ constexpr int sbuffers_for(int NH) { return NH == 1 ? 4 : 2; }
 constexpr int kFixedTiles = 3;              // prologue + epilogue cost, in tiles
 // Warps: a K and a V producer, a QK issuer and a PV issuer per half, four
 // softmax warps per half. One thread issuing tcgen05.mma (or TMA copies)
@@ -95,7 +97,7 @@ struct TcSmem {
     static constexpr int kV = kK + kKS * tc::TILE_BYTES;
     static constexpr int kCrd = kV + kVS * tc::TILE_BYTES;
     static constexpr int kBar = kCrd + tc::MAX_BOXES * 4;
-    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 3 * NH * tc::SB + 2;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 3 * NH * tc::sbuffers_for(NH) + 2;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kDynamic = kBytes + 1024;  // slack to align the base to 1 KB
@@ -129,6 +131,8 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     constexpr int KS = S::kKS;
     constexpr int VS = S::kVS;
     constexpr int NTHREADS = threads_for(NH);
+    constexpr int SB = sbuffers_for(NH);
+    static_assert(NH * SB * BN + NH * 128 <= 512, "tensor memory budget");
     constexpr int SW0 = first_softmax_warp(NH);
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ uint8_t smem_raw[];
@@ -166,6 +170,35 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     // One CTA per sequence owns its status word and stores it whole; other
     // CTAs only add SVF_DEV_TIMEOUT, which takes seconds to arise.
     const bool designated = g == 0 && rb == 0 && split == 0;
+    // On-chip set-up first: it overlaps the previous kernel's tail.
+    if (threadIdx.x == 0) {
+        for (int s2 = 0; s2 < KS; ++s2) {
+            mbar_init(&k_full[s2], 1);
+            mbar_init(&k_empty[s2], NH);
+        }
+        for (int s2 = 0; s2 < VS; ++s2) {
+            mbar_init(&v_full[s2], 1);
+            mbar_init(&v_empty[s2], NH);
+        }
+        for (int k = 0; k < NH * SB; ++k) {
+            mbar_init(&s_full[k], 1);
+            mbar_init(&p_full[k], 128);
+            mbar_init(&o_done[k], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(v_tail, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1 && lane == 0) {
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        if (p.q_tma) tma_prefetch_desc(&tmq);
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
     pdl_wait();
     pdl_launch_dependents();
 
@@ -179,6 +212,12 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     if (n <= 0) {
         // No tile here. The first chunk reports a bad length; with a single
         // chunk this CTA owns final outputs, which are zeros then.
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 2) {
+            tc_fence_after();
+            tmem_dealloc(*tmem_slot, kTmemCols);
+        }
         if (designated && threadIdx.x == 0) p.status[b] = SVF_DEV_BAD_LENGTH;
         if (p.splits == 1 && threadIdx.x < 128 * NH) {
             const int R = rb * 128 * NH + threadIdx.x;
@@ -198,23 +237,6 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     const int box_rows = ps < MAX_BOX_ROWS ? ps : MAX_BOX_ROWS;
     const int bpt = BN / box_rows;  // TMA boxes per tile and 64-dim half
     if (threadIdx.x == 0) {
-        for (int s2 = 0; s2 < KS; ++s2) {
-            mbar_init(&k_full[s2], 1);
-            mbar_init(&k_empty[s2], NH);
-        }
-        for (int s2 = 0; s2 < VS; ++s2) {
-            mbar_init(&v_full[s2], 1);
-            mbar_init(&v_empty[s2], NH);
-        }
-        for (int k = 0; k < NH * SB; ++k) {
-            mbar_init(&s_full[k], 1);
-            mbar_init(&p_full[k], 128);
-            mbar_init(&o_done[k], 1);
-        }
-        mbar_init(q_full, 1);
-        mbar_init(v_tail, 1);
-        *abort_flag = 0;
-        mbar_fence_init();
         if (p.q_tma) {
             // rows (node, head) of this block: box = 64 dims x G heads x 128/G nodes
             mbar_arrive_expect_tx(q_full, NH * HALF_BYTES);
@@ -224,10 +246,6 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
                     tma_load_4d(sQ + hh * HALF_BYTES + dh * Q_COL_BYTES, &tmq, dh * 64, g * p.G,
                                 (rb * NH + hh) * nodes, b, q_full);
         }
-    }
-    if (warp == 2) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
     }
     if (!p.q_tma && warp >= SW0) {
         // Q rows -> shared memory by the softmax threads (K-major, 128-byte
@@ -677,6 +695,9 @@ static bool make_q_map(CUtensorMap *map, const void *q, int B, int N, int Hq, in
     return r == CUDA_SUCCESS;
 }
 
+// Rows per CTA: one half of up to 128 rows, or two halves of up to 256. Two
+// halves per CTA beat two one-half CTAs per KV head (which read every K/V
+// tile twice, from L2 or by multicast) on this part.
 static int row_halves(int M) { return M > 128 ? 2 : 1; }
 
 // Chunk count of the KV range per (sequence, KV head, row block): minimises
