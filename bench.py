@@ -378,6 +378,28 @@ def run_ours(args, w, idx):
     attn_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     acc_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
 
+    # ---- KV commit of the accepted path (one layer), timed on its own after
+    # the step: it rewrites tree rows of the cache in place, which later
+    # replays of the step read as ordinary (finite) K/V
+    commit_out = {}
+
+    def commit_call(s):
+        sv.kv_commit(s["k"], s["v"], s["page_table"], s["seq_lens"], acc_out["path"],
+                     acc_out["accept_len"], outputs=commit_out)
+
+    commit_call(sets[0])
+    barrier()
+    g_commit = [capture(commit_call, s) for s in sets]
+    barrier()
+    cevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        cevs[i][0].record(stream)
+        g_commit[i % nsets].replay()
+        cevs[i][1].record(stream)
+    barrier()
+    commit_ms = sum(e[0].elapsed_time(e[1]) for e in cevs) / args.steps
+    assert int(commit_out["status"].abs().sum()) == 0
+
     def rmax(x):
         if world == 1:
             return x
@@ -443,6 +465,12 @@ def run_ours(args, w, idx):
     acc_bytes = walk_bytes(w, inp.parent, acc_out["path"].cpu().numpy(),
                            acc_out["accept_len"].cpu().numpy())
     acc_gbs = acc_bytes / (acc_ms / 1e3) / 1e9
+    path_h = acc_out["path"].cpu().numpy()
+    alen_h = acc_out["accept_len"].cpu().numpy()
+    rows_moved = int(sum(int((path_h[b, 1: alen_h[b] + 1] != np.arange(1, alen_h[b] + 1)).sum())
+                         for b in range(B)))
+    commit_bytes = rows_moved * w.Hkv * D * (2 if bf else 4) * 2 * 2
+    commit_gbs = commit_bytes / (commit_ms / 1e3) / 1e9
     acc_ws_need = sv.spec_accept_workspace_size(B, N, w.V)
     launches_per_step = 1 + 1 + (1 if ws_need > 0 else 0) + (2 if acc_ws_need > 0 else 1)
     line = {
@@ -476,6 +504,10 @@ def run_ours(args, w, idx):
                             "bytes_all_rows": nb["accept_bytes"],
                             "bytes_note": "rows of the visited nodes; bytes_all_rows counts "
                                           "every row a walk could test"},
+            "kv_commit": {"ms": commit_ms, "bytes": commit_bytes, "gbs": commit_gbs,
+                          "frac_of_hbm": commit_gbs / peak, "rows_moved": rows_moved,
+                          "bytes_note": "K and V rows of accepted nodes not yet in place, "
+                                        "read and written, one layer"},
         },
         "roofline": {
             "bound": "hbm",

@@ -66,7 +66,8 @@ enum svf_device_status {
     SVF_DEV_BAD_TOKEN = 2,  /* a draft token (node >= 1) outside [0, V) */
     SVF_DEV_BAD_PAGE = 4,   /* a needed page id outside [0, num_pages) */
     SVF_DEV_BAD_LENGTH = 8, /* seq_lens[b] < 0 or the sequence overflows its page table */
-    SVF_DEV_TIMEOUT = 16    /* an internal wait gave up (the outputs of b are undefined) */
+    SVF_DEV_TIMEOUT = 16,   /* an internal wait gave up (the outputs of b are undefined) */
+    SVF_DEV_BAD_PATH = 32   /* accept_len or path[b] is not a root path in BFS order */
 };
 
 /* ------------------------------------------------------------------------
@@ -216,6 +217,55 @@ int svf_spec_accept_noalloc(const float *target_logits, const float *draft_logit
                             const float *u_bonus, int B, int N, int V, int32_t *accept_len,
                             int32_t *path, int32_t *out_tokens, float *ratio, int32_t *status,
                             svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * svf_kv_commit -- keep the accepted path's K/V and roll back the rejected
+ * nodes' entries.
+ *
+ * Follows "EAGLE-4 Technical Deepdive", § EAGLE-4 verification trees and
+ * harness (after verification the accepted continuation is kept and the
+ * KV-cache entries of rejected nodes are freed) and "EAGLE 演化史", § D.2
+ * (every tree node writes its own K/V in the verification pass; entries of
+ * nodes that fail must not stay in the cache, which is rolled back page by
+ * page). For every layer l, sequence b and k = 0 .. accept_len[b]:
+ *   token L_b + k  <-  token L_b + path[b][k]     (K and V, all heads)
+ * with every source read before its destination is written, so tokens
+ * L_b .. L_b + accept_len[b] hold the root and the accepted nodes in path
+ * order. Tokens before L_b and past L_b + accept_len[b] are not written.
+ *
+ *   k_cache,    layer l at k_cache + l * layer_stride elements, each layer
+ *   v_cache     [num_pages, page_size, Hkv, D] dtype, paged as in
+ *               svf_tree_verify_attn (token t of b in page
+ *               page_table[b][t / page_size], slot t % page_size); 16-byte
+ *               aligned; updated in place
+ *   layer_stride  elements between layers, >= num_pages * page_size * Hkv * D
+ *               when num_layers > 1 (ignored for one layer)
+ *   seq_lens   [B] int32    L_b, the prefix length before the tree
+ *   path       [B, N] int32, accept_len [B] int32: svf_spec_accept's outputs
+ *   new_seq_lens [B] int32  out: L_b + accept_len[b] + 1 (root + accepted)
+ *   freed_pages [B, max_free] int32  out, may be NULL when max_free is 0: ids
+ *               of the pages that held tree entries and hold no committed
+ *               token now (page-table indices ceil(new_len / page_size) ..
+ *               ceil((L_b + N) / page_size) - 1, in order), -1 after them;
+ *               max_free >= ceil(N / page_size) holds every case
+ *   n_freed    [B] int32    out, may be NULL: that count
+ *   status     [B] int32    out; SVF_DEV_BAD_PATH (accept_len outside
+ *               [0, N-1], path[0] != 0, or path not strictly increasing
+ *               inside [0, N)), SVF_DEV_BAD_LENGTH (L_b < 0 or L_b + N past
+ *               the page table), SVF_DEV_BAD_PAGE (a page of tokens
+ *               [L_b, L_b + N) outside [0, num_pages)). A flagged sequence's
+ *               cache is not written, new_seq_lens[b] = L_b and nothing is
+ *               freed.
+ * The pages of tokens [L_b, L_b + N) must be distinct and belong to b alone;
+ * otherwise the cache contents are undefined (nothing faults).
+ * Limits: 1 <= N <= 1024, 1 <= num_layers <= 65535, Hkv * D * element size a
+ * multiple of 16 bytes, dtype SVF_F32 or SVF_BF16.
+ * ---------------------------------------------------------------------- */
+int svf_kv_commit(void *k_cache, void *v_cache, int num_layers, long long layer_stride,
+                  int num_pages, int page_size, const int32_t *page_table, int max_pages,
+                  const int32_t *seq_lens, const int32_t *path, const int32_t *accept_len, int B,
+                  int N, int Hkv, int D, int dtype, int32_t *new_seq_lens, int32_t *freed_pages,
+                  int max_free, int32_t *n_freed, int32_t *status, svf_stream_t stream);
 
 /* Human-readable name of a host return code or of one device status bit. */
 const char *svf_status_string(int code);

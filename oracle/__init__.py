@@ -10,6 +10,7 @@ Functions (the C file cites the passage each one follows):
   tree_mask(parent)                      -> anc [B,N,W] uint64, depth [B,N], status [B]
   tree_attn(q, k, v, seq_lens, parent, scale, rows=None) -> out [R,D] f64, lse [R] f64
   spec_accept(target, draft, tokens, parent, u_accept, u_bonus) -> dict
+  kv_commit(k_cache, v_cache, page_table, seq_lens, path, accept_len, N) -> dict
 """
 
 from __future__ import annotations
@@ -56,6 +57,9 @@ def _load():
             lib.oracle_tree_attn.restype = I
             lib.oracle_spec_accept.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P, P, P, P, P]
             lib.oracle_spec_accept.restype = I
+            lib.oracle_kv_commit.argtypes = [P, P, I, I, ctypes.c_longlong, I, I, P, I, P, P, P,
+                                             I, I, I, I, P, P, I, P, P]
+            lib.oracle_kv_commit.restype = I
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = I
             lib.oracle_set_threads.argtypes = [I]
@@ -149,4 +153,42 @@ def spec_accept(target, draft, tokens, parent, u_accept, u_bonus, probe_token=No
         _p(out["accept_margin"]), _p(out["bonus_margin"]), _p(out["n_rejects"]), _p(out["status"]),
         _p(probe_token), _p(out["probe_cdf"]) if probe_token is not None else None)
     assert rc == 0
+    return out
+
+
+def kv_commit(k_cache, v_cache, page_table, seq_lens, path, accept_len, N, max_free=None):
+    """Commit the accepted path's K/V in place on copies of the caches.
+
+    k_cache, v_cache: [layers, num_pages, page_size, Hkv, D] (or without the
+    layer axis) numpy arrays of 2- or 4-byte elements (bf16 as uint16). Returns
+    a dict with the committed caches ``k``, ``v`` and ``new_seq_lens``,
+    ``freed`` [B, max_free], ``n_freed``, ``status``."""
+    k = np.array(k_cache, copy=True, order="C")
+    v = np.array(v_cache, copy=True, order="C")
+    assert k.shape == v.shape and k.dtype == v.dtype and k.itemsize in (2, 4)
+    shp = k.shape if k.ndim == 5 else (1,) + k.shape
+    layers, num_pages, page_size, Hkv, D = shp
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    path = np.ascontiguousarray(path, dtype=np.int32)
+    accept_len = np.ascontiguousarray(accept_len, dtype=np.int32)
+    B, max_pages = page_table.shape
+    assert path.shape == (B, N) and accept_len.shape == (B,) and seq_lens.shape == (B,)
+    if max_free is None:
+        max_free = (N + page_size - 1) // page_size
+    out = {
+        "new_seq_lens": np.zeros((B,), np.int32),
+        "freed": np.zeros((B, max_free), np.int32),
+        "n_freed": np.zeros((B,), np.int32),
+        "status": np.zeros((B,), np.int32),
+    }
+    stride = num_pages * page_size * Hkv * D
+    rc = _load().oracle_kv_commit(
+        _p(k), _p(v), k.itemsize, layers, stride, num_pages, page_size, _p(page_table), max_pages,
+        _p(seq_lens), _p(path), _p(accept_len), B, N, Hkv, D, _p(out["new_seq_lens"]),
+        _p(out["freed"]), max_free, _p(out["n_freed"]), _p(out["status"]))
+    if rc != 0:
+        raise ValueError("oracle_kv_commit: bad arguments")
+    out["k"] = k
+    out["v"] = v
     return out

@@ -14,6 +14,12 @@
  *                      tree; each node attends to the prefix, its ancestors and
  *                      itself; its output equals running prompt + root->node
  *                      path as an ordinary causal sequence).
+ *   oracle_kv_commit   "EAGLE-4 Technical Deepdive", § EAGLE-4 verification
+ *                      trees and harness (after verification keep the
+ *                      accepted continuation, free the rejected KV entries)
+ *                      and "EAGLE 演化史", § D.2 (every tree node writes its
+ *                      own K/V; rejected nodes' entries must not stay in the
+ *                      cache, which is rolled back page by page).
  *   oracle_spec_accept "Eagle vs DFlash", speculative sampling rule (accept
  *                      x with probability min(1, p(x)/q(x)); on rejection
  *                      sample from normalize(max(0, p - q))); "EAGLE 演化史"
@@ -46,6 +52,9 @@
 
 #define ORACLE_BAD_PARENT 1
 #define ORACLE_BAD_TOKEN 2
+#define ORACLE_BAD_PAGE 4
+#define ORACLE_BAD_LENGTH 8
+#define ORACLE_BAD_PATH 32
 
 int oracle_max_threads(void) {
 #ifdef _OPENMP
@@ -330,6 +339,98 @@ int oracle_spec_accept(const float *target, const float *draft, const int32_t *t
         free(pt);
         free(qd);
         free(res);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O5: commit the accepted path's K/V (rollback of the rejected nodes).     */
+/*   k_cache, v_cache: num_layers caches of [num_pages, page_size, Hkv, D]   */
+/*     elements of elem_size bytes, layer l starting layer_stride elements   */
+/*     after layer l-1. Token t of sequence b sits in page                   */
+/*     page_table[b][t / page_size], slot t % page_size; the tree's node j   */
+/*     is token L_b + j.                                                     */
+/*   path [B, N], accept_len [B]: the acceptance walk's result (root first). */
+/* For each layer and each sequence, the K/V rows of tokens                  */
+/*   L_b + path[0], L_b + path[1], ..., L_b + path[accept_len]              */
+/* are read, and then written to tokens L_b, L_b + 1, ..., L_b + accept_len. */
+/* new_seq_lens[b] = L_b + accept_len + 1. The pages at table indices        */
+/* ceil(new_len / ps) .. ceil((L_b + N) / ps) - 1 held only rejected nodes;  */
+/* their ids go to freed[b][0..] in that order (-1 after them), the count to */
+/* n_freed[b].                                                               */
+/* A sequence with a bad path (accept_len outside [0, N-1], path[0] != 0, or */
+/* a path index outside (path[k-1], N)), a bad length (L_b < 0 or           */
+/* L_b + N beyond its page table) or a bad page (a page of tokens            */
+/* [L_b, L_b + N) outside [0, num_pages)) is left untouched: status bits,    */
+/* new_seq_lens[b] = L_b, no freed pages.                                    */
+/* ------------------------------------------------------------------------ */
+int oracle_kv_commit(uint8_t *k_cache, uint8_t *v_cache, int elem_size, int num_layers,
+                     long long layer_stride, int num_pages, int page_size,
+                     const int32_t *page_table, int max_pages, const int32_t *seq_lens,
+                     const int32_t *path, const int32_t *accept_len, int B, int N, int Hkv,
+                     int D, int32_t *new_seq_lens, int32_t *freed, int max_free,
+                     int32_t *n_freed, int32_t *status) {
+    if (B < 0 || N < 1 || Hkv < 1 || D < 1 || page_size < 1 || max_pages < 1 || num_layers < 1 ||
+        (elem_size != 2 && elem_size != 4))
+        return -1;
+    const size_t row_bytes = (size_t)Hkv * D * elem_size;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b];
+        const int32_t *pt = page_table + (size_t)b * max_pages;
+        const int32_t *pb = path + (size_t)b * N;
+        const int len = accept_len[b];
+        int st = 0;
+        if (len < 0 || len > N - 1 || pb[0] != 0) {
+            st |= ORACLE_BAD_PATH;
+        } else {
+            for (int k = 1; k <= len; ++k)
+                if (pb[k] <= pb[k - 1] || pb[k] >= N) st |= ORACLE_BAD_PATH;
+        }
+        if (L < 0 || (long long)L + N > (long long)max_pages * page_size) {
+            st |= ORACLE_BAD_LENGTH;
+        } else {
+            for (long long t = L; t < (long long)L + N; ++t) {
+                const int page = pt[t / page_size];
+                if (page < 0 || page >= num_pages) st |= ORACLE_BAD_PAGE;
+            }
+        }
+        status[b] = st;
+        if (freed)
+            for (int i = 0; i < max_free; ++i) freed[(size_t)b * max_free + i] = -1;
+        if (n_freed) n_freed[b] = 0;
+        if (st) {
+            new_seq_lens[b] = L;
+            continue;
+        }
+        const int new_len = L + len + 1;
+        new_seq_lens[b] = new_len;
+        /* read every source row first, then write the destinations */
+        uint8_t *buf = (uint8_t *)malloc(row_bytes * (size_t)(len + 1) * 2);
+        for (int l = 0; l < num_layers; ++l) {
+            uint8_t *kl = k_cache + (size_t)l * layer_stride * elem_size;
+            uint8_t *vl = v_cache + (size_t)l * layer_stride * elem_size;
+            for (int k = 0; k <= len; ++k) {
+                const long long t = (long long)L + pb[k];
+                const size_t off = ((size_t)pt[t / page_size] * page_size + t % page_size) * row_bytes;
+                memcpy(buf + (size_t)(2 * k) * row_bytes, kl + off, row_bytes);
+                memcpy(buf + (size_t)(2 * k + 1) * row_bytes, vl + off, row_bytes);
+            }
+            for (int k = 0; k <= len; ++k) {
+                const long long t = (long long)L + k;
+                const size_t off = ((size_t)pt[t / page_size] * page_size + t % page_size) * row_bytes;
+                memcpy(kl + off, buf + (size_t)(2 * k) * row_bytes, row_bytes);
+                memcpy(vl + off, buf + (size_t)(2 * k + 1) * row_bytes, row_bytes);
+            }
+        }
+        free(buf);
+        const int first = (new_len + page_size - 1) / page_size;
+        const int end = (int)(((long long)L + N + page_size - 1) / page_size);
+        int cnt = 0;
+        for (int i = first; i < end; ++i) {
+            if (freed && cnt < max_free) freed[(size_t)b * max_free + cnt] = pt[i];
+            ++cnt;
+        }
+        if (n_freed) n_freed[b] = cnt;
     }
     return 0;
 }

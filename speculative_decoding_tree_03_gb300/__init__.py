@@ -37,6 +37,7 @@ EXPORTED = [
     "svf_spec_accept_workspace_size",
     "svf_spec_accept",
     "svf_spec_accept_noalloc",
+    "svf_kv_commit",
     "svf_status_string",
     "svf_version",
 ]
@@ -71,6 +72,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_spec_accept.restype = I
     lib.svf_spec_accept_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P]
     lib.svf_spec_accept_noalloc.restype = I
+    lib.svf_kv_commit.argtypes = [P, P, I, ctypes.c_longlong, I, I, P, I, P, P, P, I, I, I, I,
+                                  I, P, P, I, P, P, P]
+    lib.svf_kv_commit.restype = I
     lib.svf_status_string.argtypes = [I]
     lib.svf_status_string.restype = ctypes.c_char_p
     lib.svf_version.argtypes = []
@@ -250,6 +254,62 @@ def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor, tokens:
         _ptr(u_bonus), B, N, V, _ptr(o["accept_len"]), _ptr(o["path"]), _ptr(o["out_tokens"]),
         _ptr(o.get("ratio")), _ptr(workspace), ws_bytes, _ptr(o["status"]), _stream(stream))
     _check(rc, "svf_spec_accept")
+    return o
+
+
+# ---------------------------------------------------------------------------
+# kv_commit
+# ---------------------------------------------------------------------------
+
+def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+              seq_lens: torch.Tensor, path: torch.Tensor, accept_len: torch.Tensor,
+              max_free: Optional[int] = None, outputs: Optional[dict] = None,
+              stream=None) -> dict:
+    """Keep the accepted path's K/V in place, in path order after the prefix.
+
+    k_cache, v_cache [layers, num_pages, page_size, Hkv, D] (or without the
+    layer axis), float32 or bfloat16, each layer contiguous; page_table
+    [B, max_pages], seq_lens [B], path [B, N], accept_len [B] int32. Returns a
+    dict of device tensors: new_seq_lens [B], freed [B, max_free] (page ids, -1
+    padded), n_freed [B], status [B]."""
+    lib = load_library()
+    _dev(k_cache, "k_cache")
+    if k_cache.dim() == 4:
+        layers, (num_pages, page_size, Hkv, D) = 1, k_cache.shape
+        stride = 0
+    elif k_cache.dim() == 5:
+        layers, num_pages, page_size, Hkv, D = k_cache.shape
+        stride = k_cache.stride(0)
+    else:
+        raise SpecVerifyError("k_cache must be [layers,] num_pages, page_size, Hkv, D")
+    if not (k_cache[0] if k_cache.dim() == 5 else k_cache).is_contiguous():
+        raise SpecVerifyError("each layer of k_cache must be contiguous")
+    _dev(v_cache, "v_cache", k_cache.dtype, k_cache.shape)
+    if v_cache.stride() != k_cache.stride():
+        raise SpecVerifyError("v_cache must have k_cache's strides")
+    _dev(page_table, "page_table", torch.int32)
+    B, max_pages = page_table.shape
+    _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    _dev(path, "path", torch.int32)
+    if path.dim() != 2 or path.shape[0] != B:
+        raise SpecVerifyError("path must be [B, N]")
+    N = path.shape[1]
+    _dev(accept_len, "accept_len", torch.int32, (B,))
+    if max_free is None:
+        max_free = (N + page_size - 1) // page_size
+    dev = k_cache.device
+    o = outputs if outputs is not None else {}
+    if "status" not in o:
+        o["new_seq_lens"] = torch.empty((B,), dtype=torch.int32, device=dev)
+        o["freed"] = torch.empty((B, max(max_free, 1)), dtype=torch.int32, device=dev)
+        o["n_freed"] = torch.empty((B,), dtype=torch.int32, device=dev)
+        o["status"] = torch.empty((B,), dtype=torch.int32, device=dev)
+    rc = lib.svf_kv_commit(
+        _ptr(k_cache), _ptr(v_cache), layers, stride, num_pages, page_size, _ptr(page_table),
+        max_pages, _ptr(seq_lens), _ptr(path), _ptr(accept_len), B, N, Hkv, D,
+        _dtype_code(k_cache.dtype), _ptr(o["new_seq_lens"]), _ptr(o["freed"]), max_free,
+        _ptr(o["n_freed"]), _ptr(o["status"]), _stream(stream))
+    _check(rc, "svf_kv_commit")
     return o
 
 

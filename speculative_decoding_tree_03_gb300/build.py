@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libspecverify.so")
-SOURCES = ["mask.cu", "attn_simt.cu", "attn_tc.cu", "accept.cu", "accept_stream.cu", "accept_noalloc.cu", "api.cu"]
+SOURCES = ["mask.cu", "attn_simt.cu", "attn_tc.cu", "accept.cu", "accept_stream.cu",
+           "accept_noalloc.cu", "kv_commit.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -50,6 +50,7 @@ const char *svf_status_string(int code) {
         case SVF_DEV_BAD_PAGE: return "device: page id outside the cache";
         case SVF_DEV_BAD_LENGTH: return "device: sequence length outside its page table";
         case SVF_DEV_TIMEOUT: return "device: an internal wait timed out";
+        case SVF_DEV_BAD_PATH: return "device: accepted path is not a root path in BFS order";
         default: return "unknown status";
     }
 }
@@ -134,6 +135,40 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
     cudaError_t e = launch_accept(target_logits, draft_logits, tokens, parent, u_accept, u_bonus,
                                   B, N, V, accept_len, path, out_tokens, ratio, workspace, status,
                                   reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+int svf_kv_commit(void *k_cache, void *v_cache, int num_layers, long long layer_stride,
+                  int num_pages, int page_size, const int32_t *page_table, int max_pages,
+                  const int32_t *seq_lens, const int32_t *path, const int32_t *accept_len, int B,
+                  int N, int Hkv, int D, int dtype, int32_t *new_seq_lens, int32_t *freed_pages,
+                  int max_free, int32_t *n_freed, int32_t *status, svf_stream_t stream) {
+    if (B < 0 || N < 0 || num_layers < 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 ||
+        page_size <= 0 || max_pages <= 0 || max_free < 0 || layer_stride < 0)
+        return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (!k_cache || !v_cache || !page_table || !seq_lens || !path || !accept_len ||
+        !new_seq_lens || !status || (max_free > 0 && !freed_pages))
+        return SVF_ERR_ARG;
+    if (N < 1 || N > 1024 || num_layers < 1 || num_layers > 65535) return SVF_ERR_UNSUPPORTED;
+    const int elem = dtype == SVF_BF16 ? 2 : dtype == SVF_F32 ? 4 : 0;
+    if (elem == 0 || ((long long)Hkv * D * elem) % 16 != 0) return SVF_ERR_UNSUPPORTED;
+    if ((long long)num_pages * page_size > INT_MAX || (long long)max_pages * page_size > INT_MAX)
+        return SVF_ERR_UNSUPPORTED;
+    const long long layer_elems = (long long)num_pages * page_size * Hkv * D;
+    if (num_layers > 1 && layer_stride < layer_elems) return SVF_ERR_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || (layer_stride * elem) % 16 != 0)
+        return SVF_ERR_ARG;
+    KvCommitArgs a;
+    a.k_cache = k_cache; a.v_cache = v_cache;
+    a.num_layers = num_layers; a.layer_stride = num_layers > 1 ? layer_stride : 0;
+    a.num_pages = num_pages; a.page_size = page_size;
+    a.page_table = page_table; a.max_pages = max_pages;
+    a.seq_lens = seq_lens; a.path = path; a.accept_len = accept_len;
+    a.B = B; a.N = N; a.Hkv = Hkv; a.D = D; a.elem_size = elem;
+    a.new_seq_lens = new_seq_lens; a.freed_pages = max_free > 0 ? freed_pages : nullptr;
+    a.max_free = max_free; a.n_freed = n_freed; a.status = status;
+    cudaError_t e = launch_kv_commit(a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 

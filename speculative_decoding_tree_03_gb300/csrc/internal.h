@@ -13,6 +13,28 @@ namespace svf {
 cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint64_t *anc, int32_t *depth,
                              int32_t *status, cudaStream_t stream);
 
+// Arguments of one KV commit call (kv_commit.cu).
+struct KvCommitArgs {
+    void *k_cache;
+    void *v_cache;
+    int num_layers;
+    long long layer_stride;  // elements
+    int num_pages;
+    int page_size;
+    const int32_t *page_table;
+    int max_pages;
+    const int32_t *seq_lens;
+    const int32_t *path;
+    const int32_t *accept_len;
+    int B, N, Hkv, D, elem_size;
+    int32_t *new_seq_lens;
+    int32_t *freed_pages;
+    int max_free;
+    int32_t *n_freed;
+    int32_t *status;
+};
+cudaError_t launch_kv_commit(const KvCommitArgs &a, cudaStream_t stream);
+
 // Arguments of one tree-attention call, shared by both attention kernels.
 struct AttnArgs {
     const void *q;

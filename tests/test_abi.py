@@ -101,6 +101,22 @@ def test_accept_argument_checks(lib):
     assert call(V=300000, wsb=8) == -4
 
 
+def test_kv_commit_argument_checks(lib):
+    def call(B=2, N=7, layers=1, stride=0, num_pages=8, ps=4, max_pages=4, Hkv=2, D=64,
+             dtype=1, max_free=2, freed=P, k=P):
+        return lib.svf_kv_commit(k, P, layers, stride, num_pages, ps, P, max_pages, P, P, P, B, N,
+                                 Hkv, D, dtype, P, freed, max_free, None, P, None)
+    assert call(B=-1) == -1
+    assert call(B=0, k=None) == 0
+    assert call(k=None) == -1
+    assert call(max_free=2, freed=None) == -1          # freed_pages needed when max_free > 0
+    assert call(N=0) == -2 and call(N=1025) == -2
+    assert call(dtype=5) == -2
+    assert call(Hkv=1, D=4) == -2                       # a row of 8 bytes is not 16-byte sized
+    assert call(layers=2, stride=100) == -1             # layers overlap
+    assert call(k=ctypes.c_void_p(264)) == -1           # not 16-byte aligned
+
+
 def test_workspace_sizes_without_gpu(lib):
     # bf16 attention with many KV tiles per (sequence, head) splits the KV range
     n = lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 1, 1, 2176)
