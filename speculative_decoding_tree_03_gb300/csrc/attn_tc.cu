@@ -97,7 +97,7 @@ struct TcSmem {
     static constexpr int kV = kK + kKS * tc::TILE_BYTES;
     static constexpr int kCrd = kV + kVS * tc::TILE_BYTES;
     static constexpr int kBar = kCrd + tc::MAX_BOXES * 4;
-    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 3 * NH * tc::sbuffers_for(NH) + 2;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 4 * NH * tc::sbuffers_for(NH) + 2;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kBytes = kMisc + 64;
     static constexpr int kDynamic = kBytes + 1024;  // slack to align the base to 1 KB
@@ -150,7 +150,8 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     uint64_t *s_full = v_empty + VS;      // [NH][SB]: QK of the tile in S buffer b done
     uint64_t *p_full = s_full + NH * SB;  // [NH][SB]: P of the tile written over S buffer b
     uint64_t *o_done = p_full + NH * SB;  // [NH][SB]: PV that read S buffer b done
-    uint64_t *q_full = o_done + NH * SB;
+    uint64_t *p_half = o_done + NH * SB;  // [NH][SB]: first half of that P written
+    uint64_t *q_full = p_half + NH * SB;
     uint64_t *v_tail = q_full + 1;       // last V tile with its rows past the end zeroed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
             mbar_init(&s_full[k], 1);
             mbar_init(&p_full[k], 128);
             mbar_init(&o_done[k], 1);
+            mbar_init(&p_half[k], 128);
         }
         mbar_init(q_full, 1);
         mbar_init(v_tail, 1);
@@ -409,16 +411,28 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
             ok = tail ? warp_wait(v_tail, 0, abort_flag)
                       : warp_wait(&v_full[j % VS], (uint32_t)((j / VS) & 1), abort_flag);
             if (!ok) break;
-            if (!(ok = warp_wait(&p_full[h * SB + bb], (uint32_t)((j / SB) & 1), abort_flag))) break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t d = tmem + 256 + h * 128;
-                const uint32_t a = tmem + (uint32_t)((h * SB + bb) * BN);
-                const uint32_t vst = aV + (j % VS) * TILE_BYTES;
+            // P arrives in two halves of 32 tokens; the first half's K-steps
+            // go in while the softmax still computes the second
+            const uint32_t d = tmem + 256 + h * 128;
+            const uint32_t a = tmem + (uint32_t)((h * SB + bb) * BN);
+            const uint32_t vst = aV + (j % VS) * TILE_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ts(d, a + kk * 8, smem_desc_sw128(vst + kk * 2048, KV_COL_BYTES, 1024),
-                            idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int part = 0; part < 2; ++part) {
+                uint64_t *pb = part == 0 ? &p_half[h * SB + bb] : &p_full[h * SB + bb];
+                if (!(ok = warp_wait(pb, (uint32_t)((j / SB) & 1), abort_flag))) break;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int k2 = 0; k2 < BN / 32; ++k2) {
+                        const int kk = part * (BN / 32) + k2;
+                        umma_ts(d, a + kk * 8, smem_desc_sw128(vst + kk * 2048, KV_COL_BYTES, 1024),
+                                idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) {
                 umma_commit(&o_done[h * SB + bb]);
                 umma_commit(&v_empty[j % VS]);
             }
@@ -462,13 +476,13 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
             }
             float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < BN; c += 4) {
-                m0 = fmaxf(m0, __uint_as_float(v[c]));
-                m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
-                m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
-                m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
+            for (int c = 0; c < BN; c += 8) {
+                m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+                m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+                m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+                m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
             }
-            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sl2;
+            const float mx = fmax3(m0, m1, fmaxf(m2, m3)) * sl2;
             // lazy rescale: move the reference max only when it grows by > 2^8
             const bool need = mx > m_ref + kRescaleThreshold;
             if (__any_sync(FULL, need)) {
@@ -497,21 +511,30 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
                     tmem_wait_st();
                 }
             }
-            // P = 2^(s*scale - m_ref) as bf16 pairs over the first 32 S columns
+            // P = 2^(s*scale - m_ref) as bf16 pairs over the first 32 S
+            // columns, in two halves of 32 tokens (the PV issuer starts on the
+            // first); even and odd columns are summed in the two lanes of r
             const float mneg = m_ref == -INFINITY ? 0.0f : -m_ref;
-            float r0 = 0.0f, r1 = 0.0f;
+            const float2 sc2 = make_float2(sl2, sl2), mn2 = make_float2(mneg, mneg);
+            float2 r = make_float2(0.0f, 0.0f);
             uint32_t pk[BN / 2];
 #pragma unroll
             for (int c = 0; c < BN / 2; ++c) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * c]), sl2, mneg));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * c + 1]), sl2, mneg));
-                r0 += p0;
-                r1 += p1;
-                pk[c] = pack_bf16x2(p0, p1);
+                const float2 x = ffma2(make_float2(__uint_as_float(v[2 * c]),
+                                                   __uint_as_float(v[2 * c + 1])), sc2, mn2);
+                const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                r = fadd2(r, pp);
+                pk[c] = pack_bf16x2(pp.x, pp.y);
+                if (c == BN / 4 - 1) {
+                    tmem_st16(tS, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&p_half[h * SB + bb]);
+                }
             }
-            tmem_st32(tS, pk);
+            tmem_st16(tS + BN / 4, pk + BN / 4);
             tmem_wait_st();
-            l += r0 + r1;
+            l += r.x + r.y;
             tc_fence_before();
             mbar_arrive(&p_full[h * SB + bb]);
         }
