@@ -400,6 +400,56 @@ def run_ours(args, w, idx):
     commit_ms = sum(e[0].elapsed_time(e[1]) for e in cevs) / args.steps
     assert int(commit_out["status"].abs().sum()) == 0
 
+    # ---- the target-only acceptance variants on the same inputs, each timed
+    # on its own (greedy argmax matching; one-hot candidate sampling)
+    var_out = {"greedy": {}, "onehot": {}}
+
+    def greedy_call(s):
+        sv.spec_accept_greedy(s["target"], s["tokens"], s["parent"], outputs=var_out["greedy"])
+
+    def onehot_call(s):
+        sv.spec_accept_onehot(s["target"], s["tokens"], s["parent"], s["u_accept"],
+                              s["u_bonus"], outputs=var_out["onehot"])
+
+    # ---- EAGLE-2 tree construction for this workload's batch and vocabulary:
+    # k = 8 per round, 6 rounds, N nodes kept, from seeded synthetic draft rows
+    e2k, e2rounds = 8, 6
+    e2gen = torch.Generator(device=dev)
+    e2gen.manual_seed(1234)
+    e2rows = [torch.randn((B, 1 if r == 0 else e2k, w.V), generator=e2gen, device=dev) * 2.0
+              for r in range(e2rounds)]
+    e2roots = torch.zeros((B,), dtype=torch.int32, device=dev)
+    e2cap = 1 + e2k + (e2rounds - 1) * e2k * e2k
+    e2pool = sv.eagle2_pool(e2roots, e2cap)
+    e2f0 = torch.zeros((B, 1), dtype=torch.int32, device=dev)
+    e2fr = [torch.empty((B, e2k), dtype=torch.int32, device=dev) for _ in range(e2rounds)]
+
+    def eagle2_call(s):
+        sv.eagle2_init(e2pool, e2roots)
+        f = e2f0
+        for r in range(e2rounds):
+            f = sv.eagle2_expand(e2pool, e2rows[r], f, e2k, next_frontier=e2fr[r])
+        return sv.eagle2_finalize(e2pool, N, outputs=e2out)
+
+    e2out = {}
+    var_ms = {}
+    for name, fn in (("greedy", greedy_call), ("onehot", onehot_call), ("eagle2", eagle2_call)):
+        fn(sets[0])
+        barrier()
+        graphs = [capture(fn, s) for s in sets]
+        barrier()
+        vev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            vev[i][0].record(stream)
+            graphs[i % nsets].replay()
+            vev[i][1].record(stream)
+        barrier()
+        var_ms[name] = sum(e[0].elapsed_time(e[1]) for e in vev) / args.steps
+        if name != "eagle2":
+            assert int(var_out[name]["status"].abs().sum()) == 0
+    assert int(e2out["n_out"].min()) == min(N, e2cap)
+
     def rmax(x):
         if world == 1:
             return x
@@ -471,6 +521,23 @@ def run_ours(args, w, idx):
                          for b in range(B)))
     commit_bytes = rows_moved * w.Hkv * D * (2 if bf else 4) * 2 * 2
     commit_gbs = commit_bytes / (commit_ms / 1e3) / 1e9
+    e2bytes = (1 + (e2rounds - 1) * e2k) * B * w.V * 4
+    var_kernels = {"eagle2_build": {
+        "ms": var_ms["eagle2"], "bytes": e2bytes, "gbs": e2bytes / (var_ms["eagle2"] / 1e3) / 1e9,
+        "frac_of_hbm": e2bytes / (var_ms["eagle2"] / 1e3) / 1e9 / peak,
+        "config": f"k={e2k}, {e2rounds} rounds, N={N}, B={B}, V={w.V}: init, {e2rounds} "
+                  f"expansions, rerank",
+        "bytes_note": "draft rows read by the expansions"}}
+    for name in ("greedy", "onehot"):
+        vp = var_out[name]["path"].cpu().numpy()
+        vl = var_out[name]["accept_len"].cpu().numpy()
+        vb = sum(int(vl[b]) + 1 for b in range(B)) * w.V * 4
+        var_kernels["spec_accept_" + name] = {
+            "ms": var_ms[name], "bytes": vb, "gbs": vb / (var_ms[name] / 1e3) / 1e9,
+            "frac_of_hbm": vb / (var_ms[name] / 1e3) / 1e9 / peak,
+            "mean_accept_len": float(vl.mean()),
+            "bytes_note": "target rows of the visited nodes"}
+        assert (vp[:, 0] == 0).all()
     acc_ws_need = sv.spec_accept_workspace_size(B, N, w.V)
     launches_per_step = 1 + 1 + (1 if ws_need > 0 else 0) + (2 if acc_ws_need > 0 else 1)
     line = {
@@ -508,6 +575,7 @@ def run_ours(args, w, idx):
                           "frac_of_hbm": commit_gbs / peak, "rows_moved": rows_moved,
                           "bytes_note": "K and V rows of accepted nodes not yet in place, "
                                         "read and written, one layer"},
+            **var_kernels,
         },
         "roofline": {
             "bound": "hbm",

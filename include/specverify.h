@@ -219,6 +219,110 @@ int svf_spec_accept_noalloc(const float *target_logits, const float *draft_logit
                             svf_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * svf_spec_accept_greedy -- temperature-0 acceptance over the tree.
+ *
+ * "Eagle vs DFlash", § A fair evaluation protocol: greedy speculative
+ * decoding must reproduce a target-only greedy run. From the root, let a be
+ * the argmax of the current node's target logits (equal maxima: the lowest
+ * token id); accept the first child, in ascending node index, whose token is
+ * a and continue there; stop when no child carries a. The bonus token is the
+ * last a. Only the target rows of visited nodes are read.
+ *   target_logits [B, N, V] float32, tokens / parent [B, N] int32 (as for
+ *   svf_spec_accept); outputs accept_len [B], path [B, N], out_tokens [B, N]
+ *   and status [B] as for svf_spec_accept (same status bits and "no result"
+ *   values).
+ * Limits: 1 <= N <= 1024, 1 <= V <= 262144; target_logits 16-byte aligned
+ * when V % 4 == 0.
+ * ---------------------------------------------------------------------- */
+int svf_spec_accept_greedy(const float *target_logits, const int32_t *tokens,
+                           const int32_t *parent, int B, int N, int V, int32_t *accept_len,
+                           int32_t *path, int32_t *out_tokens, int32_t *status,
+                           svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * svf_spec_accept_onehot -- the sampling rule with one-hot draft
+ * distributions, for deterministic (top-k) sibling candidates.
+ *
+ * "Eagle vs DFlash" gives the rule (accept x with probability
+ * min(1, p(x)/q(x)); on rejection continue from normalize(max(0, p - q))).
+ * With the draft's q shared by siblings it is exact only when the siblings
+ * are independent draws from q; this call takes q = one-hot(candidate) for
+ * every child instead, which keeps the output distributed as the target's
+ * for any fixed candidate set. Child c with token x is accepted iff
+ * u_accept[b][c] < p~(x); a rejection gives p~ <- normalize(max(0, p~ -
+ * one-hot(x))), i.e. x loses its mass; when every child of the current node
+ * is rejected, or at a leaf, the bonus token is the inverse CDF of p~ at
+ * u_bonus[b] (smallest k whose cumulative p~ exceeds u * sum p~). Only the
+ * target rows of visited nodes are read.
+ *   Arguments and outputs as for svf_spec_accept without draft_logits and
+ *   workspace; ratio [B, N] (may be NULL) gets p~(x) = p~(x)/q(x) for every
+ *   tested child, NaN otherwise.
+ * Limits: 1 <= N <= 1024, 1 <= V <= 262144; target_logits 16-byte aligned
+ * when V % 4 == 0.
+ * ---------------------------------------------------------------------- */
+int svf_spec_accept_onehot(const float *target_logits, const int32_t *tokens,
+                           const int32_t *parent, const float *u_accept, const float *u_bonus,
+                           int B, int N, int V, int32_t *accept_len, int32_t *path,
+                           int32_t *out_tokens, float *ratio, int32_t *status,
+                           svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * EAGLE-2 dynamic draft-tree construction.
+ *
+ * "EAGLE 演化史", § E.2-E.3, and "The EAGLE Family" (EAGLE-2): a node's value
+ * is the product of the draft confidences on its root path, a confidence
+ * being the draft softmax probability of the node's own token. Each round
+ * expands the k most valuable nodes of the previous round into their k most
+ * probable draft tokens; rerank keeps the N most valuable nodes (a connected
+ * subtree) and flattens them in BFS order for verification. The drafter runs
+ * between rounds, so the build is a sequence of calls on a node pool per
+ * sequence, all on one stream:
+ *   svf_eagle2_init      root (pool id 0, value 1, depth 0); count = 1
+ *   svf_eagle2_expand    one round; round 1 expands frontier {0}
+ *   svf_eagle2_finalize  rerank + BFS numbering -> parent[] / tokens
+ *
+ * Pool (device, caller-owned, [B, capacity] each, row b for sequence b;
+ * capacity >= 1 + k + (rounds - 1) k^2 holds every node; the node with pool
+ * id c is "creation id" c): pool_parent int32 (parent's id, -1 for the root),
+ * pool_depth int32, pool_token int32, pool_value float64; pool_count [B]
+ * int32 = nodes created so far.
+ *
+ * svf_eagle2_expand: draft_rows [B, R, V] float32, row r = the drafter's
+ * logits at node frontier[b][r] (frontier [B, R] int32 pool ids, -1 entries
+ * only after the valid ones; their rows are not read). For every valid
+ * frontier node f, in order, its k most probable tokens (ties to the lower
+ * id) become children with ids pool_count[b] + r k + i (i = rank), value
+ * value(f) * softmax(row)[token]; pool_count advances by k per valid row
+ * (capped at capacity; children past it are dropped). next_frontier [B, k]
+ * int32 gets the ids of the k most valuable new children (value desc, id
+ * asc), -1 padded: the nodes to draft from next.
+ *
+ * svf_eagle2_finalize: keeps the root and the n_nodes - 1 most valuable other
+ * nodes (value desc, depth asc, id asc) and numbers them level by level, a
+ * level ordered by (parent's new index, value desc, id asc). Outputs
+ * [B, n_nodes]: parent (new indices, -1 for the root), tokens, values
+ * (float64), cids (pool ids); entries past n_out[b] (when the pool holds
+ * fewer nodes) are -1 / 0.
+ *
+ * Limits: 1 <= k <= 16, k <= V; capacity <= 2048; 1 <= n_nodes <= 1024.
+ * Confidences are computed in fp32 statistics with an fp64 final step; values
+ * within ~1e-6 relative of each other may order differently from an exact
+ * computation.
+ * ---------------------------------------------------------------------- */
+int svf_eagle2_init(const int32_t *root_tokens, int B, int capacity, int32_t *pool_parent,
+                    int32_t *pool_depth, int32_t *pool_token, double *pool_value,
+                    int32_t *pool_count, svf_stream_t stream);
+int svf_eagle2_expand(const float *draft_rows, int B, int R, int V, int k,
+                      const int32_t *frontier, int capacity, int32_t *pool_parent,
+                      int32_t *pool_depth, int32_t *pool_token, double *pool_value,
+                      int32_t *pool_count, int32_t *next_frontier, svf_stream_t stream);
+int svf_eagle2_finalize(int B, int capacity, const int32_t *pool_parent,
+                        const int32_t *pool_depth, const int32_t *pool_token,
+                        const double *pool_value, const int32_t *pool_count, int n_nodes,
+                        int32_t *parent, int32_t *tokens, double *values, int32_t *cids,
+                        int32_t *n_out, svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * svf_kv_commit -- keep the accepted path's K/V and roll back the rejected
  * nodes' entries.
  *

@@ -11,6 +11,9 @@ Functions (the C file cites the passage each one follows):
   tree_attn(q, k, v, seq_lens, parent, scale, rows=None) -> out [R,D] f64, lse [R] f64
   spec_accept(target, draft, tokens, parent, u_accept, u_bonus) -> dict
   kv_commit(k_cache, v_cache, page_table, seq_lens, path, accept_len, N) -> dict
+  spec_accept_greedy(target, tokens, parent) -> dict
+  eagle2_pool / eagle2_expand / eagle2_finalize: EAGLE-2 tree construction
+  spec_accept_onehot(target, tokens, parent, u_accept, u_bonus) -> dict
 """
 
 from __future__ import annotations
@@ -60,6 +63,14 @@ def _load():
             lib.oracle_kv_commit.argtypes = [P, P, I, I, ctypes.c_longlong, I, I, P, I, P, P, P,
                                              I, I, I, I, P, P, I, P, P]
             lib.oracle_kv_commit.restype = I
+            lib.oracle_spec_accept_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P]
+            lib.oracle_spec_accept_greedy.restype = I
+            lib.oracle_spec_accept_onehot.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P, P, P, P]
+            lib.oracle_spec_accept_onehot.restype = I
+            lib.oracle_eagle2_expand.argtypes = [P, I, I, I, I, P, I, P, P, P, P, P, P, P]
+            lib.oracle_eagle2_expand.restype = I
+            lib.oracle_eagle2_finalize.argtypes = [I, I, P, P, P, P, P, I, P, P, P, P, P, P, P]
+            lib.oracle_eagle2_finalize.restype = I
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = I
             lib.oracle_set_threads.argtypes = [I]
@@ -191,4 +202,91 @@ def kv_commit(k_cache, v_cache, page_table, seq_lens, path, accept_len, N, max_f
         raise ValueError("oracle_kv_commit: bad arguments")
     out["k"] = k
     out["v"] = v
+    return out
+
+
+def _variant_inputs(target, tokens, parent):
+    target = np.ascontiguousarray(target, dtype=np.float32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    B, N, V = target.shape
+    assert tokens.shape == (B, N) and parent.shape == (B, N)
+    return target, tokens, parent, B, N, V
+
+
+def spec_accept_greedy(target, tokens, parent):
+    """Temperature-0 acceptance: argmax matching along the tree."""
+    target, tokens, parent, B, N, V = _variant_inputs(target, tokens, parent)
+    out = {"accept_len": np.zeros((B,), np.int32), "path": np.zeros((B, N), np.int32),
+           "out_tokens": np.zeros((B, N), np.int32), "status": np.zeros((B,), np.int32)}
+    rc = _load().oracle_spec_accept_greedy(
+        _p(target), _p(tokens), _p(parent), B, N, V, _p(out["accept_len"]), _p(out["path"]),
+        _p(out["out_tokens"]), _p(out["status"]))
+    assert rc == 0
+    return out
+
+
+def spec_accept_onehot(target, tokens, parent, u_accept, u_bonus):
+    """The sampling rule with q = one-hot(candidate) for every child."""
+    target, tokens, parent, B, N, V = _variant_inputs(target, tokens, parent)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32)
+    u_bonus = np.ascontiguousarray(u_bonus, dtype=np.float32)
+    assert u_accept.shape == (B, N) and u_bonus.shape == (B,)
+    out = {"accept_len": np.zeros((B,), np.int32), "path": np.zeros((B, N), np.int32),
+           "out_tokens": np.zeros((B, N), np.int32), "ratio": np.zeros((B, N), np.float64),
+           "accept_margin": np.zeros((B, N), np.float64),
+           "bonus_margin": np.zeros((B,), np.float64), "status": np.zeros((B,), np.int32)}
+    rc = _load().oracle_spec_accept_onehot(
+        _p(target), _p(tokens), _p(parent), _p(u_accept), _p(u_bonus), B, N, V,
+        _p(out["accept_len"]), _p(out["path"]), _p(out["out_tokens"]), _p(out["ratio"]),
+        _p(out["accept_margin"]), _p(out["bonus_margin"]), _p(out["status"]))
+    assert rc == 0
+    return out
+
+
+def eagle2_pool(root_tokens, capacity):
+    """A fresh node pool per sequence holding only the root (cid 0, value 1)."""
+    root_tokens = np.asarray(root_tokens, dtype=np.int32)
+    B = root_tokens.shape[0]
+    pool = {"parent": np.full((B, capacity), -1, np.int32),
+            "depth": np.zeros((B, capacity), np.int32),
+            "token": np.full((B, capacity), -1, np.int32),
+            "value": np.zeros((B, capacity), np.float64),
+            "count": np.ones((B,), np.int32)}
+    pool["token"][:, 0] = root_tokens
+    pool["value"][:, 0] = 1.0
+    return pool
+
+
+def eagle2_expand(pool, rows, frontier, k):
+    """One expansion round in place on ``pool``. rows [B, R, V] are the draft
+    logits at the frontier nodes frontier [B, R] (cids, -1 padded at the end).
+    Returns (next_frontier [B, k], select_gap [B])."""
+    rows = np.ascontiguousarray(rows, dtype=np.float32)
+    frontier = np.ascontiguousarray(frontier, dtype=np.int32)
+    B, R, V = rows.shape
+    C = pool["parent"].shape[1]
+    nxt = np.zeros((B, k), np.int32)
+    gap = np.zeros((B,), np.float64)
+    rc = _load().oracle_eagle2_expand(_p(rows), B, R, V, k, _p(frontier), C, _p(pool["parent"]),
+                                      _p(pool["depth"]), _p(pool["token"]), _p(pool["value"]),
+                                      _p(pool["count"]), _p(nxt), _p(gap))
+    if rc != 0:
+        raise ValueError("oracle_eagle2_expand: bad arguments")
+    return nxt, gap
+
+
+def eagle2_finalize(pool, n_nodes):
+    """Rerank the pool and flatten the kept subtree in BFS order."""
+    B, C = pool["parent"].shape
+    out = {"parent": np.zeros((B, n_nodes), np.int32), "token": np.zeros((B, n_nodes), np.int32),
+           "value": np.zeros((B, n_nodes), np.float64), "cid": np.zeros((B, n_nodes), np.int32),
+           "n_out": np.zeros((B,), np.int32), "cut_gap": np.zeros((B,), np.float64),
+           "connected": np.zeros((B,), np.int32)}
+    rc = _load().oracle_eagle2_finalize(
+        B, C, _p(pool["parent"]), _p(pool["depth"]), _p(pool["token"]), _p(pool["value"]),
+        _p(pool["count"]), n_nodes, _p(out["parent"]), _p(out["token"]), _p(out["value"]),
+        _p(out["cid"]), _p(out["n_out"]), _p(out["cut_gap"]), _p(out["connected"]))
+    if rc != 0:
+        raise ValueError("oracle_eagle2_finalize: bad arguments")
     return out

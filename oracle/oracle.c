@@ -20,6 +20,22 @@
  *                      and "EAGLE 演化史", § D.2 (every tree node writes its
  *                      own K/V; rejected nodes' entries must not stay in the
  *                      cache, which is rolled back page by page).
+ *   oracle_spec_accept_greedy  "Eagle vs DFlash", § A fair evaluation
+ *                      protocol (greedy decoding must reproduce a target-only
+ *                      run): at temperature 0 the target emits its argmax, so
+ *                      a draft node is accepted iff its token is the argmax of
+ *                      its parent's target row, and the bonus token is the
+ *                      argmax at the last accepted node.
+ *   oracle_spec_accept_onehot  the sampling rule of oracle_spec_accept with
+ *                      q = one-hot(candidate token) for every child, the form
+ *                      that stays lossless for deterministic (top-k) siblings.
+ *   oracle_eagle2_*    "EAGLE 演化史", § E.2 (a node's value is the product
+ *                      of draft confidences on its root path; expand the
+ *                      top-k frontier nodes by value into their top-k draft
+ *                      tokens each round; rerank all nodes by value and keep
+ *                      the top N, a connected subtree) and § E.3 (one worked
+ *                      expansion step); "The EAGLE Family", EAGLE-2 (expand,
+ *                      then rerank and flatten for verification).
  *   oracle_spec_accept "Eagle vs DFlash", speculative sampling rule (accept
  *                      x with probability min(1, p(x)/q(x)); on rejection
  *                      sample from normalize(max(0, p - q))); "EAGLE 演化史"
@@ -431,6 +447,339 @@ int oracle_kv_commit(uint8_t *k_cache, uint8_t *v_cache, int elem_size, int num_
             ++cnt;
         }
         if (n_freed) n_freed[b] = cnt;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O6: acceptance variants that read only target rows.                      */
+/* ------------------------------------------------------------------------ */
+
+/* Validity of one sequence, as for oracle_spec_accept; resets its outputs. */
+static int variant_reset(const int32_t *par, const int32_t *tok, int N, int V, int32_t *path,
+                         int32_t *out_tokens, double *ratio, double *accept_margin) {
+    int st = 0;
+    if (!tree_is_valid(par, N)) st |= ORACLE_BAD_PARENT;
+    for (int c = 1; c < N; ++c)
+        if (tok[c] < 0 || tok[c] >= V) st |= ORACLE_BAD_TOKEN;
+    for (int c = 0; c < N; ++c) {
+        path[c] = -1;
+        out_tokens[c] = -1;
+        if (ratio) ratio[c] = NAN;
+        if (accept_margin) accept_margin[c] = NAN;
+    }
+    return st;
+}
+
+/* Greedy: a = argmax of the current node's target logits (the lowest index
+ * among equal maxima); accept the first child (ascending index) whose token
+ * is a and continue there; stop when no child carries a. The bonus token is
+ * the last a. Outputs as for oracle_spec_accept. */
+int oracle_spec_accept_greedy(const float *target, const int32_t *tokens, const int32_t *parent,
+                              int B, int N, int V, int32_t *accept_len, int32_t *path,
+                              int32_t *out_tokens, int32_t *status) {
+    if (B < 0 || N < 1 || V <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parent + (size_t)b * N;
+        const int32_t *tok = tokens + (size_t)b * N;
+        int32_t *pb = path + (size_t)b * N, *ob = out_tokens + (size_t)b * N;
+        const int st = variant_reset(par, tok, N, V, pb, ob, NULL, NULL);
+        status[b] = st;
+        accept_len[b] = 0;
+        if (st) continue;
+        int cur = 0, len = 0;
+        pb[0] = 0;
+        for (;;) {
+            const float *row = target + ((size_t)b * N + cur) * V;
+            int a = 0;
+            for (int v = 1; v < V; ++v)
+                if (row[v] > row[a]) a = v;
+            int next = -1;
+            for (int c = cur + 1; c < N; ++c)
+                if (par[c] == cur && tok[c] == a) {
+                    next = c;
+                    break;
+                }
+            if (next < 0) {
+                ob[len] = a;
+                break;
+            }
+            ++len;
+            pb[len] = next;
+            ob[len - 1] = a;
+            cur = next;
+        }
+        accept_len[b] = len;
+    }
+    return 0;
+}
+
+/* One-hot candidates: the sampling rule with q_c = one-hot(x_c) for child c.
+ * With p~ the current target distribution (softmax of the node's row, then
+ * residuals), child c is accepted iff u_c * q_c(x_c) = u_c < p~(x_c); on a
+ * rejection p~ <- normalize(max(0, p~ - one-hot(x_c))), i.e. x_c loses its
+ * mass; when every child is rejected, or at a leaf, the bonus token is the
+ * inverse CDF of p~ at u_bonus (smallest k whose cumulative p~ exceeds
+ * u * sum(p~), else the last k with p~(k) > 0). ratio = p~(x)/q(x) = p~(x);
+ * margins as for oracle_spec_accept. */
+int oracle_spec_accept_onehot(const float *target, const int32_t *tokens, const int32_t *parent,
+                              const float *u_accept, const float *u_bonus, int B, int N, int V,
+                              int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                              double *ratio, double *accept_margin, double *bonus_margin,
+                              int32_t *status) {
+    if (B < 0 || N < 1 || V <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parent + (size_t)b * N;
+        const int32_t *tok = tokens + (size_t)b * N;
+        int32_t *pb = path + (size_t)b * N, *ob = out_tokens + (size_t)b * N;
+        double *rb = ratio ? ratio + (size_t)b * N : NULL;
+        double *mb = accept_margin ? accept_margin + (size_t)b * N : NULL;
+        const int st = variant_reset(par, tok, N, V, pb, ob, rb, mb);
+        status[b] = st;
+        accept_len[b] = 0;
+        if (bonus_margin) bonus_margin[b] = NAN;
+        if (st) continue;
+        double *pt = (double *)malloc(sizeof(double) * V);
+        int cur = 0, len = 0;
+        pb[0] = 0;
+        softmax64(target + ((size_t)b * N + cur) * V, V, pt);
+        for (;;) {
+            int moved = 0;
+            for (int c = cur + 1; c < N && !moved; ++c) {
+                if (par[c] != cur) continue;
+                const int x = tok[c];
+                const double u = (double)u_accept[(size_t)b * N + c];
+                const double px = pt[x];
+                if (rb) rb[c] = px;
+                if (mb) {
+                    const double hi = u > px ? u : px;
+                    mb[c] = hi > 0 ? fabs(u - px) / hi : 0.0;
+                }
+                if (u < px) {
+                    ++len;
+                    pb[len] = c;
+                    ob[len - 1] = x;
+                    cur = c;
+                    softmax64(target + ((size_t)b * N + cur) * V, V, pt);
+                    moved = 1;
+                } else {
+                    /* p~ <- normalize(max(0, p~ - one-hot(x))) */
+                    double S = 0.0;
+                    for (int v = 0; v < V; ++v) {
+                        const double r = pt[v] - (v == x ? 1.0 : 0.0);
+                        pt[v] = r > 0.0 ? r : 0.0;
+                        S += pt[v];
+                    }
+                    if (S > 0.0)
+                        for (int v = 0; v < V; ++v) pt[v] /= S;
+                }
+            }
+            if (!moved) break;
+        }
+        double tot = 0.0;
+        for (int v = 0; v < V; ++v) tot += pt[v];
+        const double thr = (double)u_bonus[b] * tot;
+        double cum = 0.0, prev = 0.0;
+        int pick = -1;
+        for (int v = 0; v < V; ++v) {
+            prev = cum;
+            cum += pt[v];
+            if (cum > thr) {
+                pick = v;
+                break;
+            }
+        }
+        double margin = 0.0;
+        if (pick < 0) {
+            for (int v = V - 1; v >= 0; --v)
+                if (pt[v] > 0.0) {
+                    pick = v;
+                    break;
+                }
+        } else {
+            const double a = thr - prev, c2 = cum - thr;
+            margin = (a < c2 ? a : c2) / tot;
+        }
+        ob[len] = pick;
+        accept_len[b] = len;
+        if (bonus_margin) bonus_margin[b] = margin;
+        free(pt);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* O8: EAGLE-2 dynamic tree construction, fp64.                              */
+/* A pool per sequence holds every node created so far, by creation id      */
+/* (cid): parent cid (-1 for the root), depth, token and value. The root is  */
+/* cid 0 with value 1. One expansion round takes the draft logits row of    */
+/* each frontier node (frontier[b][r], -1 entries only at the end), creates */
+/* for each its top-k draft tokens (by probability, ties to the lower id)   */
+/* as children with value = parent value * confidence, the confidence being */
+/* the draft softmax probability of the child's token, numbered in order of */
+/* frontier position then rank; the next frontier is the top-k of the new   */
+/* children by (value desc, cid asc), -1 padded. select_gap[b] reports the */
+/* relative gap between the last selected and the first unselected value   */
+/* (+inf when nothing was left out), so a caller can tell near ties.        */
+/* ------------------------------------------------------------------------ */
+int oracle_eagle2_expand(const float *rows, int B, int R, int V, int k, const int32_t *frontier,
+                         int C, int32_t *pool_parent, int32_t *pool_depth, int32_t *pool_token,
+                         double *pool_value, int32_t *pool_count, int32_t *next_frontier,
+                         double *select_gap) {
+    if (B < 0 || R < 1 || V < 1 || k < 1 || k > V || C < 1) return -1;
+    for (int b = 0; b < B; ++b) {
+        int32_t *pp = pool_parent + (size_t)b * C, *pd = pool_depth + (size_t)b * C;
+        int32_t *pt = pool_token + (size_t)b * C;
+        double *pv = pool_value + (size_t)b * C;
+        const int first = pool_count[b];
+        int cnt = first;
+        double *prob = (double *)malloc(sizeof(double) * V);
+        char *taken = (char *)malloc((size_t)V);
+        for (int r = 0; r < R; ++r) {
+            const int f = frontier[(size_t)b * R + r];
+            if (f < 0) break;
+            softmax64(rows + ((size_t)b * R + r) * V, V, prob);
+            memset(taken, 0, (size_t)V);
+            for (int i = 0; i < k; ++i) {
+                int best = -1;
+                for (int v = 0; v < V; ++v)
+                    if (!taken[v] && (best < 0 || prob[v] > prob[best])) best = v;
+                taken[best] = 1;
+                if (cnt < C) {
+                    pp[cnt] = f;
+                    pd[cnt] = pd[f] + 1;
+                    pt[cnt] = best;
+                    pv[cnt] = pv[f] * prob[best];
+                }
+                ++cnt;
+            }
+        }
+        if (cnt > C) cnt = C;
+        pool_count[b] = cnt;
+        /* next frontier: top-k of the new children by (value desc, cid asc) */
+        char *sel = (char *)calloc((size_t)(cnt - first) + 1, 1);
+        double last = INFINITY;
+        for (int i = 0; i < k; ++i) {
+            int best = -1;
+            for (int c = first; c < cnt; ++c)
+                if (!sel[c - first] && (best < 0 || pv[c] > pv[best])) best = c;
+            next_frontier[(size_t)b * k + i] = best;
+            if (best >= 0) {
+                sel[best - first] = 1;
+                last = pv[best];
+            }
+        }
+        double gap = INFINITY;
+        for (int c = first; c < cnt; ++c)
+            if (!sel[c - first] && last > 0.0) {
+                const double g = (last - pv[c]) / last;
+                if (g < gap) gap = g;
+            }
+        if (select_gap) select_gap[b] = gap;
+        free(sel);
+        free(prob);
+        free(taken);
+    }
+    return 0;
+}
+
+/* Rerank and flatten: keep the root and the n_nodes - 1 best other nodes by */
+/* (value desc, depth asc, cid asc); number them in BFS order, level by     */
+/* level, a level ordered by (parent's new index, value desc, cid asc).     */
+/* Outputs [B, n_nodes]: parent (new indices, -1 for the root), token,      */
+/* value, cid; -1 / 0 padded when the pool holds fewer nodes. n_out[b] is  */
+/* the number of nodes kept, cut_gap[b] the relative gap between the last   */
+/* kept and the first dropped value (+inf when nothing was dropped), and   */
+/* connected[b] 1 if every kept node's parent was kept.                     */
+int oracle_eagle2_finalize(int B, int C, const int32_t *pool_parent, const int32_t *pool_depth,
+                           const int32_t *pool_token, const double *pool_value,
+                           const int32_t *pool_count, int n_nodes, int32_t *parent,
+                           int32_t *token, double *value, int32_t *cid, int32_t *n_out,
+                           double *cut_gap, int32_t *connected) {
+    if (B < 0 || C < 1 || n_nodes < 1) return -1;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *pp = pool_parent + (size_t)b * C, *pd = pool_depth + (size_t)b * C;
+        const int32_t *pt = pool_token + (size_t)b * C;
+        const double *pv = pool_value + (size_t)b * C;
+        const int cnt = pool_count[b];
+        int32_t *ob_p = parent + (size_t)b * n_nodes, *ob_t = token + (size_t)b * n_nodes;
+        int32_t *ob_c = cid + (size_t)b * n_nodes;
+        double *ob_v = value + (size_t)b * n_nodes;
+        for (int i = 0; i < n_nodes; ++i) {
+            ob_p[i] = -1;
+            ob_t[i] = -1;
+            ob_c[i] = -1;
+            ob_v[i] = 0.0;
+        }
+        char *kept = (char *)calloc((size_t)cnt, 1);
+        kept[0] = 1;
+        int nk = 1;
+        double last = INFINITY;
+        while (nk < n_nodes) {
+            int best = -1;
+            for (int c = 1; c < cnt; ++c) {
+                if (kept[c]) continue;
+                if (best < 0 || pv[c] > pv[best] || (pv[c] == pv[best] && pd[c] < pd[best]))
+                    best = c;
+            }
+            if (best < 0) break;
+            kept[best] = 1;
+            last = pv[best];
+            ++nk;
+        }
+        double gap = INFINITY;
+        for (int c = 1; c < cnt; ++c)
+            if (!kept[c] && last > 0.0 && last < INFINITY) {
+                const double g = (last - pv[c]) / last;
+                if (g < gap) gap = g;
+            }
+        int conn = 1;
+        for (int c = 1; c < cnt; ++c)
+            if (kept[c] && !kept[pp[c]]) conn = 0;
+        /* BFS numbering */
+        int *newidx = (int *)malloc(sizeof(int) * (size_t)cnt);
+        char *placed = (char *)calloc((size_t)cnt, 1);
+        for (int c = 0; c < cnt; ++c) newidx[c] = -1;
+        newidx[0] = 0;
+        placed[0] = 1;
+        ob_p[0] = -1;
+        ob_t[0] = pt[0];
+        ob_v[0] = pv[0];
+        ob_c[0] = 0;
+        int at = 1;
+        for (int d = 1; at < nk; ++d) {
+            for (;;) {
+                int best = -1;
+                for (int c = 1; c < cnt; ++c) {
+                    if (!kept[c] || placed[c] || pd[c] != d || newidx[pp[c]] < 0) continue;
+                    if (best < 0) {
+                        best = c;
+                        continue;
+                    }
+                    const int a1 = newidx[pp[c]], a0 = newidx[pp[best]];
+                    if (a1 < a0 || (a1 == a0 && (pv[c] > pv[best] ||
+                                                 (pv[c] == pv[best] && c < best))))
+                        best = c;
+                }
+                if (best < 0) break;
+                placed[best] = 1;
+                newidx[best] = at;
+                ob_p[at] = newidx[pp[best]];
+                ob_t[at] = pt[best];
+                ob_v[at] = pv[best];
+                ob_c[at] = best;
+                ++at;
+            }
+            if (d > C) break;
+        }
+        n_out[b] = at;
+        if (cut_gap) cut_gap[b] = gap;
+        if (connected) connected[b] = conn;
+        free(kept);
+        free(newidx);
+        free(placed);
     }
     return 0;
 }

@@ -38,6 +38,11 @@ EXPORTED = [
     "svf_spec_accept",
     "svf_spec_accept_noalloc",
     "svf_kv_commit",
+    "svf_spec_accept_greedy",
+    "svf_spec_accept_onehot",
+    "svf_eagle2_init",
+    "svf_eagle2_expand",
+    "svf_eagle2_finalize",
     "svf_status_string",
     "svf_version",
 ]
@@ -72,6 +77,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_spec_accept.restype = I
     lib.svf_spec_accept_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P]
     lib.svf_spec_accept_noalloc.restype = I
+    lib.svf_spec_accept_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, P]
+    lib.svf_spec_accept_greedy.restype = I
+    lib.svf_spec_accept_onehot.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.svf_spec_accept_onehot.restype = I
+    lib.svf_eagle2_init.argtypes = [P, I, I, P, P, P, P, P, P]
+    lib.svf_eagle2_init.restype = I
+    lib.svf_eagle2_expand.argtypes = [P, I, I, I, I, P, I, P, P, P, P, P, P, P]
+    lib.svf_eagle2_expand.restype = I
+    lib.svf_eagle2_finalize.argtypes = [I, I, P, P, P, P, P, I, P, P, P, P, P, P]
+    lib.svf_eagle2_finalize.restype = I
     lib.svf_kv_commit.argtypes = [P, P, I, ctypes.c_longlong, I, I, P, I, P, P, P, I, I, I, I,
                                   I, P, P, I, P, P, P]
     lib.svf_kv_commit.restype = I
@@ -255,6 +270,128 @@ def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor, tokens:
         _ptr(o.get("ratio")), _ptr(workspace), ws_bytes, _ptr(o["status"]), _stream(stream))
     _check(rc, "svf_spec_accept")
     return o
+
+
+def _variant_outputs(o, B, N, dev, want_ratio):
+    if "accept_len" not in o:
+        o["accept_len"] = torch.empty((B,), dtype=torch.int32, device=dev)
+        o["path"] = torch.empty((B, N), dtype=torch.int32, device=dev)
+        o["out_tokens"] = torch.empty((B, N), dtype=torch.int32, device=dev)
+        o["ratio"] = torch.empty((B, N), dtype=torch.float32, device=dev) if want_ratio else None
+        o["status"] = torch.empty((B,), dtype=torch.int32, device=dev)
+    return o
+
+
+def spec_accept_greedy(target_logits: torch.Tensor, tokens: torch.Tensor, parent: torch.Tensor,
+                       outputs: Optional[dict] = None, stream=None) -> dict:
+    """Temperature-0 acceptance (argmax matching). Returns a dict of device
+    tensors: accept_len [B], path [B, N], out_tokens [B, N], status [B]."""
+    lib = load_library()
+    _dev(target_logits, "target_logits", torch.float32)
+    B, N, V = target_logits.shape
+    _dev(tokens, "tokens", torch.int32, (B, N))
+    _dev(parent, "parent", torch.int32, (B, N))
+    o = _variant_outputs(outputs if outputs is not None else {}, B, N, target_logits.device,
+                         False)
+    rc = lib.svf_spec_accept_greedy(_ptr(target_logits), _ptr(tokens), _ptr(parent), B, N, V,
+                                    _ptr(o["accept_len"]), _ptr(o["path"]),
+                                    _ptr(o["out_tokens"]), _ptr(o["status"]), _stream(stream))
+    _check(rc, "svf_spec_accept_greedy")
+    return o
+
+
+def spec_accept_onehot(target_logits: torch.Tensor, tokens: torch.Tensor, parent: torch.Tensor,
+                       u_accept: torch.Tensor, u_bonus: torch.Tensor, want_ratio: bool = True,
+                       outputs: Optional[dict] = None, stream=None) -> dict:
+    """The sampling rule with q = one-hot(candidate) for every child. Returns
+    accept_len, path, out_tokens, ratio (or None) and status."""
+    lib = load_library()
+    _dev(target_logits, "target_logits", torch.float32)
+    B, N, V = target_logits.shape
+    _dev(tokens, "tokens", torch.int32, (B, N))
+    _dev(parent, "parent", torch.int32, (B, N))
+    _dev(u_accept, "u_accept", torch.float32, (B, N))
+    _dev(u_bonus, "u_bonus", torch.float32, (B,))
+    o = _variant_outputs(outputs if outputs is not None else {}, B, N, target_logits.device,
+                         want_ratio)
+    rc = lib.svf_spec_accept_onehot(_ptr(target_logits), _ptr(tokens), _ptr(parent),
+                                    _ptr(u_accept), _ptr(u_bonus), B, N, V,
+                                    _ptr(o["accept_len"]), _ptr(o["path"]),
+                                    _ptr(o["out_tokens"]), _ptr(o.get("ratio")),
+                                    _ptr(o["status"]), _stream(stream))
+    _check(rc, "svf_spec_accept_onehot")
+    return o
+
+
+# ---------------------------------------------------------------------------
+# EAGLE-2 tree construction
+# ---------------------------------------------------------------------------
+
+def eagle2_init(pool: dict, root_tokens: torch.Tensor, stream=None) -> dict:
+    """Reset ``pool`` to the roots alone (a new build in the same arrays)."""
+    lib = load_library()
+    _dev(root_tokens, "root_tokens", torch.int32)
+    B, C = pool["parent"].shape
+    if root_tokens.shape != (B,):
+        raise SpecVerifyError("root_tokens must be [B]")
+    rc = lib.svf_eagle2_init(_ptr(root_tokens), B, C, _ptr(pool["parent"]),
+                             _ptr(pool["depth"]), _ptr(pool["token"]), _ptr(pool["value"]),
+                             _ptr(pool["count"]), _stream(stream))
+    _check(rc, "svf_eagle2_init")
+    return pool
+
+
+def eagle2_pool(root_tokens: torch.Tensor, capacity: int, stream=None) -> dict:
+    """A node pool per sequence holding only the root (device tensors)."""
+    _dev(root_tokens, "root_tokens", torch.int32)
+    B = root_tokens.shape[0]
+    dev = root_tokens.device
+    pool = {"parent": torch.empty((B, capacity), dtype=torch.int32, device=dev),
+            "depth": torch.empty((B, capacity), dtype=torch.int32, device=dev),
+            "token": torch.empty((B, capacity), dtype=torch.int32, device=dev),
+            "value": torch.empty((B, capacity), dtype=torch.float64, device=dev),
+            "count": torch.empty((B,), dtype=torch.int32, device=dev)}
+    return eagle2_init(pool, root_tokens, stream)
+
+
+def eagle2_expand(pool: dict, draft_rows: torch.Tensor, frontier: torch.Tensor, k: int,
+                  next_frontier: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One expansion round in place; returns the next frontier [B, k]."""
+    lib = load_library()
+    _dev(draft_rows, "draft_rows", torch.float32)
+    B, R, V = draft_rows.shape
+    _dev(frontier, "frontier", torch.int32, (B, R))
+    C = pool["parent"].shape[1]
+    if next_frontier is None:
+        next_frontier = torch.empty((B, k), dtype=torch.int32, device=draft_rows.device)
+    rc = lib.svf_eagle2_expand(_ptr(draft_rows), B, R, V, k, _ptr(frontier), C,
+                               _ptr(pool["parent"]), _ptr(pool["depth"]), _ptr(pool["token"]),
+                               _ptr(pool["value"]), _ptr(pool["count"]), _ptr(next_frontier),
+                               _stream(stream))
+    _check(rc, "svf_eagle2_expand")
+    return next_frontier
+
+
+def eagle2_finalize(pool: dict, n_nodes: int, outputs: Optional[dict] = None,
+                    stream=None) -> dict:
+    """Rerank and flatten: parent [B, n], tokens, values, cids, n_out."""
+    lib = load_library()
+    B, C = pool["parent"].shape
+    dev = pool["parent"].device
+    out = outputs if outputs is not None else {}
+    if "parent" not in out:
+        out.update({"parent": torch.empty((B, n_nodes), dtype=torch.int32, device=dev),
+                    "tokens": torch.empty((B, n_nodes), dtype=torch.int32, device=dev),
+                    "values": torch.empty((B, n_nodes), dtype=torch.float64, device=dev),
+                    "cids": torch.empty((B, n_nodes), dtype=torch.int32, device=dev),
+                    "n_out": torch.empty((B,), dtype=torch.int32, device=dev)})
+    rc = lib.svf_eagle2_finalize(B, C, _ptr(pool["parent"]), _ptr(pool["depth"]),
+                                 _ptr(pool["token"]), _ptr(pool["value"]), _ptr(pool["count"]),
+                                 n_nodes, _ptr(out["parent"]), _ptr(out["tokens"]),
+                                 _ptr(out["values"]), _ptr(out["cids"]), _ptr(out["n_out"]),
+                                 _stream(stream))
+    _check(rc, "svf_eagle2_finalize")
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -138,6 +138,96 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 
+static int accept_variant_args(const float *target, const int32_t *tokens, const int32_t *parent,
+                               int B, int N, int V, const int32_t *accept_len,
+                               const int32_t *path, const int32_t *out_tokens,
+                               const int32_t *status) {
+    if (B < 0 || N < 0 || V < 0) return SVF_ERR_ARG;
+    if (B == 0) return 1;
+    if (!target || !tokens || !parent || !accept_len || !path || !out_tokens || !status)
+        return SVF_ERR_ARG;
+    if (N < 1 || N > 1024 || V < 1 || !accept_target_supported(V)) return SVF_ERR_UNSUPPORTED;
+    if ((V & 3) == 0 && !aligned16(target)) return SVF_ERR_ARG;
+    return SVF_OK;
+}
+
+int svf_spec_accept_greedy(const float *target_logits, const int32_t *tokens,
+                           const int32_t *parent, int B, int N, int V, int32_t *accept_len,
+                           int32_t *path, int32_t *out_tokens, int32_t *status,
+                           svf_stream_t stream) {
+    const int rc = accept_variant_args(target_logits, tokens, parent, B, N, V, accept_len, path,
+                                       out_tokens, status);
+    if (rc != SVF_OK) return rc > 0 ? SVF_OK : rc;
+    cudaError_t e = launch_accept_target(true, target_logits, tokens, parent, nullptr, nullptr, B,
+                                         N, V, accept_len, path, out_tokens, nullptr, status,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+int svf_spec_accept_onehot(const float *target_logits, const int32_t *tokens,
+                           const int32_t *parent, const float *u_accept, const float *u_bonus,
+                           int B, int N, int V, int32_t *accept_len, int32_t *path,
+                           int32_t *out_tokens, float *ratio, int32_t *status,
+                           svf_stream_t stream) {
+    const int rc = accept_variant_args(target_logits, tokens, parent, B, N, V, accept_len, path,
+                                       out_tokens, status);
+    if (rc != SVF_OK) return rc > 0 ? SVF_OK : rc;
+    if (!u_accept || !u_bonus) return SVF_ERR_ARG;
+    cudaError_t e = launch_accept_target(false, target_logits, tokens, parent, u_accept, u_bonus,
+                                         B, N, V, accept_len, path, out_tokens, ratio, status,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+int svf_eagle2_init(const int32_t *root_tokens, int B, int capacity, int32_t *pool_parent,
+                    int32_t *pool_depth, int32_t *pool_token, double *pool_value,
+                    int32_t *pool_count, svf_stream_t stream) {
+    if (B < 0 || capacity < 1) return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (!root_tokens || !pool_parent || !pool_depth || !pool_token || !pool_value || !pool_count)
+        return SVF_ERR_ARG;
+    if (capacity > kEagle2MaxPool) return SVF_ERR_UNSUPPORTED;
+    cudaError_t e = launch_eagle2_init(root_tokens, B, capacity, pool_parent, pool_depth,
+                                       pool_token, pool_value, pool_count,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+int svf_eagle2_expand(const float *draft_rows, int B, int R, int V, int k,
+                      const int32_t *frontier, int capacity, int32_t *pool_parent,
+                      int32_t *pool_depth, int32_t *pool_token, double *pool_value,
+                      int32_t *pool_count, int32_t *next_frontier, svf_stream_t stream) {
+    if (B < 0 || R < 0 || V < 0 || k < 0 || capacity < 1) return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (!draft_rows || !frontier || !pool_parent || !pool_depth || !pool_token || !pool_value ||
+        !pool_count || !next_frontier)
+        return SVF_ERR_ARG;
+    if (R < 1 || R > 65535 || k < 1 || k > kEagle2MaxK || k > V || capacity > kEagle2MaxPool)
+        return SVF_ERR_UNSUPPORTED;
+    cudaError_t e = launch_eagle2_expand(draft_rows, B, R, V, k, frontier, capacity, pool_parent,
+                                         pool_depth, pool_token, pool_value, pool_count,
+                                         next_frontier, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+int svf_eagle2_finalize(int B, int capacity, const int32_t *pool_parent,
+                        const int32_t *pool_depth, const int32_t *pool_token,
+                        const double *pool_value, const int32_t *pool_count, int n_nodes,
+                        int32_t *parent, int32_t *tokens, double *values, int32_t *cids,
+                        int32_t *n_out, svf_stream_t stream) {
+    if (B < 0 || capacity < 1 || n_nodes < 0) return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (!pool_parent || !pool_depth || !pool_token || !pool_value || !pool_count || !parent ||
+        !tokens || !values || !cids || !n_out)
+        return SVF_ERR_ARG;
+    if (n_nodes < 1 || n_nodes > 1024 || capacity > kEagle2MaxPool) return SVF_ERR_UNSUPPORTED;
+    cudaError_t e = launch_eagle2_finalize(B, capacity, pool_parent, pool_depth, pool_token,
+                                           pool_value, pool_count, n_nodes, parent, tokens,
+                                           values, cids, n_out,
+                                           reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
 int svf_kv_commit(void *k_cache, void *v_cache, int num_layers, long long layer_stride,
                   int num_pages, int page_size, const int32_t *page_table, int max_pages,
                   const int32_t *seq_lens, const int32_t *path, const int32_t *accept_len, int B,

@@ -13,6 +13,31 @@ namespace svf {
 cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint64_t *anc, int32_t *depth,
                              int32_t *status, cudaStream_t stream);
 
+// EAGLE-2 tree construction (eagle2.cu).
+constexpr int kEagle2MaxK = 16;
+constexpr int kEagle2MaxPool = 2048;
+size_t eagle2_finalize_smem(int C);
+cudaError_t launch_eagle2_init(const int32_t *root_tokens, int B, int C, int32_t *parent,
+                               int32_t *depth, int32_t *token, double *value, int32_t *count,
+                               cudaStream_t stream);
+cudaError_t launch_eagle2_expand(const float *rows, int B, int R, int V, int k,
+                                 const int32_t *frontier, int C, int32_t *parent, int32_t *depth,
+                                 int32_t *token, double *value, int32_t *count, int32_t *next,
+                                 cudaStream_t stream);
+cudaError_t launch_eagle2_finalize(int B, int C, const int32_t *parent, const int32_t *depth,
+                                   const int32_t *token, const double *value,
+                                   const int32_t *count, int n_nodes, int32_t *out_parent,
+                                   int32_t *out_token, double *out_value, int32_t *out_cid,
+                                   int32_t *n_out, cudaStream_t stream);
+
+// Target-only acceptance variants (accept_target.cu): greedy or one-hot q.
+bool accept_target_supported(int V);
+cudaError_t launch_accept_target(bool greedy, const float *target, const int32_t *tokens,
+                                 const int32_t *parent, const float *u_accept,
+                                 const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                                 int32_t *path, int32_t *out_tokens, float *ratio,
+                                 int32_t *status, cudaStream_t stream);
+
 // Arguments of one KV commit call (kv_commit.cu).
 struct KvCommitArgs {
     void *k_cache;

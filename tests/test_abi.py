@@ -117,6 +117,22 @@ def test_kv_commit_argument_checks(lib):
     assert call(k=ctypes.c_void_p(264)) == -1           # not 16-byte aligned
 
 
+def test_accept_variant_argument_checks(lib):
+    def greedy(B=2, N=3, V=100, t=P):
+        return lib.svf_spec_accept_greedy(t, P, P, B, N, V, P, P, P, P, None)
+
+    def onehot(B=2, N=3, V=100, t=P, u=P):
+        return lib.svf_spec_accept_onehot(t, P, P, u, P, B, N, V, P, P, P, None, P, None)
+    for call in (greedy, onehot):
+        assert call(B=-1) == -1
+        assert call(B=0, t=None) == 0
+        assert call(t=None) == -1
+        assert call(N=0) == -2 and call(N=1025) == -2
+        assert call(V=262145) == -2
+        assert call(V=128, t=ctypes.c_void_p(260)) == -1   # float4 loads need 16-byte rows
+    assert onehot(u=None) == -1
+
+
 def test_workspace_sizes_without_gpu(lib):
     # bf16 attention with many KV tiles per (sequence, head) splits the KV range
     n = lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 1, 1, 2176)

@@ -1,0 +1,186 @@
+"""GPU parity of the target-only acceptance variants (greedy, one-hot
+candidates) against the oracle."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+from scipy.stats import chisquare
+
+import oracle
+from gpu_common import ACCEPT_REL_TIE, BONUS_DELTA_PURE, BONUS_DELTA_RESIDUAL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from speculative_decoding_tree_03_gb300 import build as _b
+    _b.build()
+    import speculative_decoding_tree_03_gb300 as m
+    return m
+
+
+def _np(t):
+    return None if t is None else t.detach().cpu().numpy()
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _random_tree(rng, N):
+    return np.array([-1] + [int(rng.integers(0, i)) for i in range(1, N)], np.int32)
+
+
+def _case(seed, B, N, V, topk_children=True, sigma=3.0, noise=1.0, binary=False):
+    """Target rows ~ N(0, sigma^2); children carry the top tokens of a draft row
+    (target + noise) at their parent, in sibling order, so greedy and one-hot
+    walks go deep."""
+    rng = np.random.default_rng(seed)
+    tgt = (sigma * rng.standard_normal((B, N, V))).astype(np.float32)
+    if binary:
+        parent = np.broadcast_to(np.array([-1] + [(i - 1) // 2 for i in range(1, N)], np.int32),
+                                 (B, N)).copy()
+    else:
+        parent = np.stack([_random_tree(rng, N) for _ in range(B)])
+    tokens = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for j in range(N):
+            kids = np.nonzero(parent[b] == j)[0]
+            if len(kids) == 0:
+                continue
+            d = tgt[b, j] + noise * rng.standard_normal(V).astype(np.float32)
+            if topk_children:
+                order = np.argsort(-d, kind="stable")[: len(kids)]
+            else:
+                order = rng.integers(0, V, size=len(kids))
+            tokens[b, kids] = order
+    return dict(target=tgt, tokens=tokens, parent=parent,
+                u_accept=rng.random((B, N), dtype=np.float32),
+                u_bonus=rng.random(B, dtype=np.float32))
+
+
+def _greedy(sv, a):
+    r = sv.spec_accept_greedy(_dev(a["target"]), _dev(a["tokens"]), _dev(a["parent"]))
+    torch.cuda.synchronize()
+    return {k: _np(v) for k, v in r.items()}
+
+
+def _onehot(sv, a):
+    r = sv.spec_accept_onehot(_dev(a["target"]), _dev(a["tokens"]), _dev(a["parent"]),
+                              _dev(a["u_accept"]), _dev(a["u_bonus"]))
+    torch.cuda.synchronize()
+    return {k: _np(v) for k, v in r.items()}
+
+
+def _compare_onehot(gpu, orc, max_flag_frac=0.05):
+    """Bit-exact except decisions the oracle flags as near ties."""
+    B = gpu["path"].shape[0]
+    assert (gpu["status"] == orc["status"]).all()
+    flagged = 0
+    for b in range(B):
+        same_walk = (gpu["accept_len"][b] == orc["accept_len"][b]
+                     and (gpu["path"][b] == orc["path"][b]).all())
+        if same_walk and (gpu["out_tokens"][b] == orc["out_tokens"][b]).all():
+            continue
+        flagged += 1
+        if same_walk:
+            assert orc["bonus_margin"][b] < BONUS_DELTA_RESIDUAL, (
+                f"sequence {b}: bonus {gpu['out_tokens'][b]} vs {orc['out_tokens'][b]}, "
+                f"margin {orc['bonus_margin'][b]:.3g}")
+        else:
+            am = orc["accept_margin"][b]
+            assert (am[~np.isnan(am)] < ACCEPT_REL_TIE).any(), (
+                f"sequence {b}: path {gpu['path'][b]} vs {orc['path'][b]}")
+    assert flagged <= max(2, math.ceil(max_flag_frac * B)), flagged
+    both = ~np.isnan(orc["ratio"]) & ~np.isnan(gpu["ratio"])
+    if both.any():
+        err = np.abs(gpu["ratio"][both] - orc["ratio"][both]) / np.maximum(1e-30,
+                                                                          orc["ratio"][both])
+        assert np.quantile(err, 0.99) < 1e-4, err.max()
+    return flagged
+
+
+VOCABS = [8, 37, 1000, 4096, 5003, 32000, 128256, 151936]
+
+
+@pytest.mark.parametrize("V", VOCABS)
+def test_greedy_matches_oracle(sv, V):
+    B = 24 if V > 100000 else 64
+    a = _case(V, B, 15, V, noise=0.5)
+    gpu = _greedy(sv, a)
+    orc = oracle.spec_accept_greedy(a["target"], a["tokens"], a["parent"])
+    for k in ("accept_len", "path", "out_tokens", "status"):
+        np.testing.assert_array_equal(gpu[k], orc[k], err_msg=k)
+    assert orc["accept_len"].max() >= 2
+
+
+@pytest.mark.parametrize("V", VOCABS)
+def test_onehot_matches_oracle(sv, V):
+    B = 24 if V > 100000 else 64
+    # a flat softmax over a large vocabulary accepts nothing: peak it there
+    a = _case(V + 7, B, 15, V, sigma=2.0 if V <= 5003 else 8.0, noise=0.7)
+    gpu = _onehot(sv, a)
+    orc = oracle.spec_accept_onehot(a["target"], a["tokens"], a["parent"], a["u_accept"],
+                                    a["u_bonus"])
+    _compare_onehot(gpu, orc)
+    assert orc["accept_len"].max() >= 1
+
+
+def test_variants_many_sequences(sv):
+    """More sequences than SMs at the 70B-serving vocabulary: binary trees."""
+    a = _case(99, 64, 31, 128256, noise=1.5, binary=True)
+    g = _greedy(sv, a)
+    o = oracle.spec_accept_greedy(a["target"], a["tokens"], a["parent"])
+    for k in ("accept_len", "path", "out_tokens"):
+        np.testing.assert_array_equal(g[k], o[k], err_msg=k)
+    h = _onehot(sv, a)
+    _compare_onehot(h, oracle.spec_accept_onehot(a["target"], a["tokens"], a["parent"],
+                                                 a["u_accept"], a["u_bonus"]))
+
+
+def test_variants_status_and_edges(sv):
+    a = _case(5, 4, 7, 100)
+    a["parent"][1, 3] = 5          # not BFS
+    a["tokens"][2, 4] = 100        # outside the vocabulary
+    a["parent"][3] = [-1, 0, 1, 2, 3, 4, 5]   # a chain
+    a["tokens"][3, 1:] = 7         # duplicate tokens along it
+    for run, ref in ((_greedy, lambda: oracle.spec_accept_greedy(a["target"], a["tokens"],
+                                                                  a["parent"])),
+                     (_onehot, lambda: oracle.spec_accept_onehot(**a))):
+        gpu = run(sv, a)
+        orc = ref()
+        assert gpu["status"].tolist() == orc["status"].tolist() == [0, 1, 2, 0]
+        for b in (1, 2):
+            assert (gpu["path"][b] == -1).all() and (gpu["out_tokens"][b] == -1).all()
+            assert gpu["accept_len"][b] == 0
+        for b in (0, 3):
+            assert gpu["path"][b].tolist() == orc["path"][b].tolist()
+    # a single-node tree: only the bonus token
+    one = _case(6, 3, 1, 50)
+    g = _greedy(sv, one)
+    assert g["out_tokens"][:, 0].tolist() == np.argmax(one["target"][:, 0], -1).tolist()
+    h = _onehot(sv, one)
+    o = oracle.spec_accept_onehot(**one)
+    _compare_onehot(h, o)
+
+
+def test_onehot_lossless_on_gpu(sv):
+    """Depth-1 tree with three fixed candidates (the draft's top-3): over 10^6
+    sequences the emitted token follows the target softmax."""
+    rng = np.random.default_rng(8)
+    V, T = 8, 1_000_000
+    p = rng.dirichlet(np.ones(V))
+    q = rng.dirichlet(np.ones(V))
+    top3 = np.argsort(-q)[:3]
+    tgt = np.broadcast_to(np.log(p).astype(np.float32), (T, 4, V))
+    a = dict(target=tgt, tokens=np.broadcast_to(np.concatenate([[0], top3]).astype(np.int32), (T, 4)),
+             parent=np.broadcast_to(np.array([-1, 0, 0, 0], np.int32), (T, 4)),
+             u_accept=rng.random((T, 4), dtype=np.float32), u_bonus=rng.random(T, dtype=np.float32))
+    gpu = _onehot(sv, a)
+    counts = np.bincount(gpu["out_tokens"][:, 0], minlength=V)
+    _, pval = chisquare(counts, p * T)
+    assert pval > 1e-4, pval

@@ -323,6 +323,16 @@ def test_accept_vocab_sizes(sv, V):
     print(V, stats)
 
 
+@pytest.mark.parametrize("V", [32000, 100003])
+def test_accept_many_sequences(sv, V):
+    """More sequences than clusters that fit at once (vector and scalar loads)."""
+    B = 100 if V == 32000 else 40
+    arrs = _synthetic_accept(V + 1, B, 15, V, [-1] + [(i - 1) // 2 for i in range(1, 15)],
+                             sigma=3.0, noise=1.5)
+    gpu = _accept_gpu(sv, arrs)
+    compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
+
+
 def test_accept_streaming_vocabulary(sv):
     """A vocabulary above what one cluster holds on chip (262144) takes the
     streaming kernels with their statistics pre-pass."""
