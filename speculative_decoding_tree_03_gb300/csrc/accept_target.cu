@@ -327,8 +327,8 @@ __global__ void __launch_bounds__(NT, 1) accept_target_kernel(
         float M = -INFINITY, Z = 0.0f;
         for (int r = 0; r < ncta; ++r) ms_merge(M, Z, ws.recv[s][r].x, ws.recv[s][r].y);
         // ---- the children in order: scalar tests against p~ = p / (1 - p(R)),
-        // decided by one thread in fp64 (this part's fp64 rate is low: the
-        // other threads wait for the answer)
+        // decided by one thread (fp32 exponentials, fp64 mass and division;
+        // this part's fp64 pipe is slow, so no fp64 exp)
         if (threadIdx.x == 0) {
             double rej_mass = 0.0;
             int pick = -1;
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(NT, 1) accept_target_kernel(
                 const int x = stok[c];
                 bool dup = false;  // an earlier (rejected) sibling with the same token
                 for (int c2 = sfirst[cur]; c2 != c; c2 = snext[c2]) dup |= stok[c2] == x;
-                const double px = exp((double)slx[c] - (double)M) / (double)Z;
+                const double px = (double)ex2_approx((slx[c] - M) * kLog2e) / (double)Z;
                 const double pt = dup ? 0.0 : px / (1.0 - rej_mass);
                 if (lead && ratio) ratio[base + c] = (float)pt;
                 if ((double)su[c] < pt) {

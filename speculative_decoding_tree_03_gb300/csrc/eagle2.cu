@@ -117,24 +117,29 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     float M = m;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    double zz = (m == -INFINITY) ? 0.0 : (double)z * (double)ex2_approx((m - M) * 1.4426950408889634f);
+    float zw = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - M) * 1.4426950408889634f);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+    for (int o = 16; o > 0; o >>= 1) zw += __shfl_xor_sync(0xffffffffu, zw, o);
     if (lane == 0) {
         s_m[warp] = M;
-        s_z[warp] = zz;
+        s_z[warp] = (double)zw;
     }
     __syncthreads();
     float Mc = -INFINITY;
     for (int w = 0; w < NW; ++w) Mc = fmaxf(Mc, s_m[w]);
-    // the fp64 merge of the warps' sums by one thread (fp64 is slow here)
+    // warp 0 merges the warps' sums, one lane per warp (NW == 32); the
+    // exponentials are fp32, the sum fp64 (this part's fp64 pipe is slow, so
+    // no fp64 exp)
     __shared__ double s_Z;
-    if (threadIdx.x == 0) {
-        double Zt = 0.0;
-        for (int w = 0; w < NW; ++w)
-            if (s_m[w] != -INFINITY) Zt += s_z[w] * exp((double)s_m[w] - (double)Mc);
-        s_Z = Zt;
+    if (warp == 0) {
+        double t = s_m[lane] == -INFINITY
+                       ? 0.0
+                       : s_z[lane] * (double)ex2_approx((s_m[lane] - Mc) * 1.4426950408889634f);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) s_Z = t;
     }
+    static_assert(NW == 32, "one lane of warp 0 per warp");
 
     // the CTA's top-k: k rounds of (logit, id) maximum over the threads'
     // current heads; the winning thread drops its head
@@ -188,7 +193,8 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
         const long long slot = (long long)count[b] + (long long)r * k + i;
         if (slot < C && s_win[i] != INT_MAX) {
             const size_t o = (size_t)b * C;
-            const double conf = exp((double)s_winv[i] - (double)Mc) / Z;
+            const double conf =
+                (double)ex2_approx((s_winv[i] - Mc) * 1.4426950408889634f) / Z;
             parent[o + slot] = f;
             depth[o + slot] = depth[o + f] + 1;
             token[o + slot] = s_win[i];
