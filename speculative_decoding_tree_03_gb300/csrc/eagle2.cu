@@ -58,7 +58,7 @@ __global__ void eagle2_init_kernel(const int32_t *__restrict__ root_tokens, int 
 
 // One CTA per (frontier row r, sequence b). Child i of frontier node f gets
 // pool slot count[b] + r k + i.
-template <int KMAX>  // per-thread candidate list, KMAX >= k
+template <int KMAX>  // merge list length, KMAX >= k
 __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     const float *__restrict__ rows, int R, int V, int k, const int32_t *__restrict__ frontier,
     int C, int32_t *__restrict__ parent, int32_t *__restrict__ depth, int32_t *__restrict__ token,
@@ -69,8 +69,6 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __shared__ float s_m[NW];
     __shared__ double s_z[NW];
-    __shared__ float s_bv[NW];
-    __shared__ int s_bi[NW];
     __shared__ int s_win[KMAX];
     __shared__ float s_winv[KMAX];
     pdl_wait();
@@ -79,36 +77,56 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     if (f < 0 || f >= min(count[b], C)) return;  // an unused frontier slot
     const float *row = rows + ((size_t)b * R + r) * (size_t)V;
 
-    // one pass: running maximum, sum of e^(l - max) and this thread's top-k
+    // one pass: each thread's running (max, sum e^(l - max)); each warp's
+    // top-k, kept sorted (best first) in lanes 0 .. k-1 of (wv, wi). A chunk
+    // of 32 elements (one per lane) is compared with the warp's k-th entry and
+    // only the lanes that beat it (a ballot) are inserted, one at a time.
     float m = -INFINITY;
     float z = 0.0f;
-    float tv[KMAX];
-    int ti[KMAX];
+    float wv = -INFINITY;
+    int wi = INT_MAX;
+    constexpr int kBatch = KMAX >= 16 ? 8 : 16;
+    // the loop bound is the warp's first element, so every lane of a warp runs
+    // the same iterations (the ballots and shuffles need the whole warp)
+    for (int v0 = threadIdx.x; v0 - lane < V; v0 += kBatch * kRowThreads) {
+        float lb[kBatch];
 #pragma unroll
-    for (int i = 0; i < KMAX; ++i) {
-        tv[i] = -INFINITY;
-        ti[i] = INT_MAX;
-    }
-    for (int v = threadIdx.x; v < V; v += kRowThreads) {
-        const float l = __ldg(row + v);
-        if (l > m) {
-            z = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - l) * 1.4426950408889634f);
-            m = l;
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = v0 + u * kRowThreads;
+            lb[u] = v < V ? __ldg(row + v) : -INFINITY;
         }
-        z += ex2_approx((l - m) * 1.4426950408889634f);
-        if (before(l, v, tv[KMAX - 1], ti[KMAX - 1])) {
-            // insert, keeping tv/ti sorted by (logit desc, id asc)
-            float cv = l;
-            int ci = v;
 #pragma unroll
-            for (int i = 0; i < KMAX; ++i) {
-                if (before(cv, ci, tv[i], ti[i])) {
-                    const float t0 = tv[i];
-                    const int t1 = ti[i];
-                    tv[i] = cv;
-                    ti[i] = ci;
-                    cv = t0;
-                    ci = t1;
+        for (int u = 0; u < kBatch; ++u) {
+            const int v = v0 + u * kRowThreads;
+            const float l = lb[u];
+            if (v < V) {
+                if (l > m) {
+                    z = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - l) * 1.4426950408889634f);
+                    m = l;
+                }
+                z += ex2_approx((l - m) * 1.4426950408889634f);
+            }
+            const float tv = __shfl_sync(0xffffffffu, wv, k - 1);
+            const int tix = __shfl_sync(0xffffffffu, wi, k - 1);
+            unsigned mask = __ballot_sync(0xffffffffu, v < V && before(l, v, tv, tix));
+            while (mask) {
+                const int src = __ffs(mask) - 1;
+                mask &= mask - 1;
+                const float cv = __shfl_sync(0xffffffffu, l, src);
+                const int ci = __shfl_sync(0xffffffffu, v, src);
+                // position = entries that stay ahead of the candidate
+                const int pos = __popc(__ballot_sync(0xffffffffu,
+                                                     lane < k && before(wv, wi, cv, ci)));
+                const float upv = __shfl_up_sync(0xffffffffu, wv, 1);
+                const int upi = __shfl_up_sync(0xffffffffu, wi, 1);
+                if (pos < k && lane < k) {
+                    if (lane == pos) {
+                        wv = cv;
+                        wi = ci;
+                    } else if (lane > pos) {
+                        wv = upv;
+                        wi = upi;
+                    }
                 }
             }
         }
@@ -120,72 +138,68 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     float zw = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - M) * 1.4426950408889634f);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) zw += __shfl_xor_sync(0xffffffffu, zw, o);
+    __shared__ float s_lv[NW][KMAX];
+    __shared__ int s_li[NW][KMAX];
     if (lane == 0) {
         s_m[warp] = M;
         s_z[warp] = (double)zw;
     }
+    if (lane < k) {
+        s_lv[warp][lane] = wv;
+        s_li[warp][lane] = wi;
+    }
     __syncthreads();
     float Mc = -INFINITY;
     for (int w = 0; w < NW; ++w) Mc = fmaxf(Mc, s_m[w]);
-    // warp 0 merges the warps' sums, one lane per warp (NW == 32); the
-    // exponentials are fp32, the sum fp64 (this part's fp64 pipe is slow, so
-    // no fp64 exp)
+    static_assert(NW == 32, "one lane of warp 0 per warp");
     __shared__ double s_Z;
     if (warp == 0) {
+        // the row's normaliser: one lane per warp, fp32 exponentials and an
+        // fp64 sum (this part's fp64 pipe is slow, so no fp64 exp)
         double t = s_m[lane] == -INFINITY
                        ? 0.0
                        : s_z[lane] * (double)ex2_approx((s_m[lane] - Mc) * 1.4426950408889634f);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
         if (lane == 0) s_Z = t;
+        // the row's top-k: a k-way merge of the warps' sorted lists, lane w
+        // holding warp w's list as a shift register (head = element 0)
+        float hv[KMAX];
+        int hx[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            hv[j] = j < k ? s_lv[lane][j] : -INFINITY;
+            hx[j] = j < k ? s_li[lane][j] : INT_MAX;
+        }
+        for (int i = 0; i < k; ++i) {
+            float bv = hv[0];
+            int bi = hx[0];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (before(ov, oi, bv, bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (lane == 0) {
+                s_win[i] = bi;
+                s_winv[i] = bv;
+            }
+            if (hx[0] == bi) {
+#pragma unroll
+                for (int j = 0; j < KMAX - 1; ++j) {
+                    hv[j] = hv[j + 1];
+                    hx[j] = hx[j + 1];
+                }
+                hv[KMAX - 1] = -INFINITY;
+                hx[KMAX - 1] = INT_MAX;
+            }
+        }
     }
-    static_assert(NW == 32, "one lane of warp 0 per warp");
+    __syncthreads();
 
-    // the CTA's top-k: k rounds of (logit, id) maximum over the threads'
-    // current heads; the winning thread drops its head
-    for (int i = 0; i < k; ++i) {
-        // tv/ti is a shift register: the head is always element 0
-        const float hv = tv[0];
-        const int hi = ti[0];
-        float bv = hv;
-        int bi = hi;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (before(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (lane == 0) {
-            s_bv[warp] = bv;
-            s_bi[warp] = bi;
-        }
-        __syncthreads();
-        float wv = s_bv[0];
-        int wi = s_bi[0];
-        for (int w = 1; w < NW; ++w)
-            if (before(s_bv[w], s_bi[w], wv, wi)) {
-                wv = s_bv[w];
-                wi = s_bi[w];
-            }
-        if (threadIdx.x == 0) {
-            s_win[i] = wi;
-            s_winv[i] = wv;
-        }
-        if (hi == wi) {
-            // pop the head
-#pragma unroll
-            for (int j = 0; j < KMAX - 1; ++j) {
-                tv[j] = tv[j + 1];
-                ti[j] = ti[j + 1];
-            }
-            tv[KMAX - 1] = -INFINITY;
-            ti[KMAX - 1] = INT_MAX;
-        }
-        __syncthreads();
-    }
     // children: value = parent value * confidence
     const double Z = s_Z;
     if (threadIdx.x < k) {
@@ -249,10 +263,15 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
     extern __shared__ __align__(8) unsigned char dyn[];
     // [C] values as ordered integer keys (values are >= 0; 0 for non-nodes)
     unsigned long long *sv = reinterpret_cast<unsigned long long *>(dyn);
-    int *sd = reinterpret_cast<int *>(sv + C);        // [C] depth
+    // the 8-byte arrays first, so every array stays aligned for any C
+    unsigned long long *kv = sv + C;                   // [C] key of kept node j
+    int *sd = reinterpret_cast<int *>(kv + C);         // [C] depth
     int *sp = sd + C;                                  // [C] parent id
     int *sidx = sp + C;                                // [C] new index, -1 if not kept
     int *snew = sidx + C;                              // [C] new index being computed
+    int *skept = snew + C;                             // [C] kept nodes by rerank rank
+    int *kd = skept + C;                               // [C] depth of kept node j
+    int *kpn = kd + C;                                 // [C] its parent's new index
     __shared__ int s_kept, s_maxd, s_at, s_lvl;
     const int b = blockIdx.x;
     pdl_wait();
@@ -292,6 +311,7 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
         }
         if (rank < n_nodes - 1) {
             sidx[c] = -2;  // kept, not yet numbered
+            skept[rank] = c;
             atomicAdd(&s_kept, 1);
             atomicMax(&s_maxd, dc);
         }
@@ -304,24 +324,38 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
     __syncthreads();
     // BFS numbering, a level at a time: (parent's new index, value desc, id
     // asc); the ranks of a level are all computed before any is published
+    // Only the kept nodes are scanned, from flat per-node copies (independent
+    // loads in the inner loop): skept[j] lists them by rerank rank, kd/kv hold
+    // their depth and key, kpn the parent's new index for the current level.
+    const int nk = s_kept;
+    for (int j = threadIdx.x; j < nk; j += blockDim.x) {
+        const int c = skept[j];
+        kd[j] = sd[c];
+        kv[j] = sv[c];
+    }
+    __syncthreads();
     for (int d = 1; d <= s_maxd; ++d) {
         const int base = s_at;
-        for (int c = 1 + (int)threadIdx.x; c < cnt; c += blockDim.x) {
-            if (sidx[c] != -2 || sd[c] != d) continue;
-            const int pc = sidx[sp[c]];
-            const unsigned long long vc = sv[c];
+        for (int j = threadIdx.x; j < nk; j += blockDim.x)
+            kpn[j] = kd[j] == d ? sidx[sp[skept[j]]] : -1;
+        __syncthreads();
+        for (int j = threadIdx.x; j < nk; j += blockDim.x) {
+            if (kd[j] != d) continue;
+            const int pc = kpn[j], c = skept[j];
+            const unsigned long long vc = kv[j];
             int rank = 0;
-            for (int e = 1; e < cnt; ++e) {
-                if (sidx[e] != -2 || sd[e] != d) continue;
-                const int pe = sidx[sp[e]];
-                rank += (pe < pc || (pe == pc && (sv[e] > vc || (sv[e] == vc && e < c)))) ? 1 : 0;
+            for (int q = 0; q < nk; ++q) {
+                if (kd[q] != d) continue;
+                const int pe = kpn[q];
+                const unsigned long long ve = kv[q];
+                rank += (pe < pc || (pe == pc && (ve > vc || (ve == vc && skept[q] < c)))) ? 1 : 0;
             }
-            snew[c] = base + rank;
+            snew[j] = base + rank;
         }
         __syncthreads();
-        for (int c = 1 + (int)threadIdx.x; c < cnt; c += blockDim.x) {
-            if (sidx[c] == -2 && sd[c] == d) {
-                sidx[c] = snew[c];
+        for (int j = threadIdx.x; j < nk; j += blockDim.x) {
+            if (kd[j] == d) {
+                sidx[skept[j]] = snew[j];
                 atomicAdd(&s_lvl, 1);
             }
         }
@@ -347,7 +381,9 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
 
 // ---------------------------------------------------------------- host side
 
-size_t eagle2_finalize_smem(int C) { return (size_t)C * (sizeof(unsigned long long) + 4 * sizeof(int)); }
+size_t eagle2_finalize_smem(int C) {
+    return (size_t)C * (2 * sizeof(unsigned long long) + 7 * sizeof(int));
+}
 
 cudaError_t launch_eagle2_init(const int32_t *root_tokens, int B, int C, int32_t *parent,
                                int32_t *depth, int32_t *token, double *value, int32_t *count,
