@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     float z = 0.0f;
     float wv = -INFINITY;
     int wi = INT_MAX;
+    float tv = -INFINITY;  // the warp's k-th entry, identical in every lane
+    int tix = INT_MAX;
     constexpr int kBatch = KMAX >= 16 ? 8 : 16;
     // the loop bound is the warp's first element, so every lane of a warp runs
     // the same iterations (the ballots and shuffles need the whole warp)
@@ -95,20 +97,28 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
             const int v = v0 + u * kRowThreads;
             lb[u] = v < V ? __ldg(row + v) : -INFINITY;
         }
+        // running (max, sum e^(l - max)): one rescale per batch
+        float bm = lb[0];
+#pragma unroll
+        for (int u = 1; u + 1 < kBatch; u += 2) bm = fmax3(bm, lb[u], lb[u + 1]);
+        if (kBatch % 2 == 0) bm = fmaxf(bm, lb[kBatch - 1]);
+        if (bm > m) {
+            z = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - bm) * 1.4426950408889634f);
+            m = bm;
+        }
+        if (m != -INFINITY) {  // (a thread with no element yet keeps z = 0)
+            const float ml2 = m * 1.4426950408889634f;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                z += ex2_approx(fmaf(lb[u], 1.4426950408889634f, -ml2));
+        }
+        // candidates for the warp's top-k
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int v = v0 + u * kRowThreads;
             const float l = lb[u];
-            if (v < V) {
-                if (l > m) {
-                    z = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - l) * 1.4426950408889634f);
-                    m = l;
-                }
-                z += ex2_approx((l - m) * 1.4426950408889634f);
-            }
-            const float tv = __shfl_sync(0xffffffffu, wv, k - 1);
-            const int tix = __shfl_sync(0xffffffffu, wi, k - 1);
             unsigned mask = __ballot_sync(0xffffffffu, v < V && before(l, v, tv, tix));
+            if (!mask) continue;
             while (mask) {
                 const int src = __ffs(mask) - 1;
                 mask &= mask - 1;
@@ -129,6 +139,8 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
                     }
                 }
             }
+            tv = __shfl_sync(0xffffffffu, wv, k - 1);
+            tix = __shfl_sync(0xffffffffu, wi, k - 1);
         }
     }
     // softmax statistics of the row: (max, sum) over the warp and the CTA
