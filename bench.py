@@ -179,7 +179,13 @@ def _oracle_inputs(inp):
     return cvt(inp.q), K, V
 
 
-def time_oracle(inp, budget_s=15.0, max_steps=20):
+def time_oracle(inp, budget_s=15.0, max_steps=20, steps=None, warmup=0):
+    """Time the fp64 oracle for the whole verify step on the host cores.
+
+    Without ``steps``: as many steps as fit in ``budget_s`` (at most
+    ``max_steps``). With ``steps``: ``warmup`` untimed steps, then exactly
+    ``steps`` timed ones, the attention rows sampled so that all of them fit
+    in ``budget_s``. Returns (seconds per step, sample text, cores)."""
     import oracle
     w = inp.w
     cores = len(os.sched_getaffinity(0))
@@ -192,15 +198,27 @@ def time_oracle(inp, budget_s=15.0, max_steps=20):
     one = max(time.perf_counter() - t0, 1e-6)
     frac = 1.0
     rows = None
-    if one * rows_all / cores > budget_s / 2:
-        nsel = max(cores, int(budget_s / 2 * cores / one))
+    per_step_budget = budget_s / 2 if steps is None else budget_s / max(1, steps + warmup)
+    if one * rows_all / cores > per_step_budget:
+        nsel = max(cores, int(per_step_budget * cores / one))
         sel = np.linspace(0, rows_all - 1, nsel).astype(np.int64)
         rows = np.stack([sel // (w.N * w.Hq), (sel // w.Hq) % w.N, sel % w.Hq], 1)
         frac = nsel / rows_all
+    def one_step():
+        oracle.tree_attn(q, K, V, inp.seq_lens, inp.parent, rows=rows)
+        oracle.tree_mask(inp.parent)
+        oracle.spec_accept(inp.target, inp.draft, inp.tokens, inp.parent, inp.u_accept,
+                           inp.u_bonus)
+
+    for _ in range(warmup):
+        one_step()
+    fixed = steps
     steps = 0
     t_attn = t_acc = 0.0
     start = time.perf_counter()
-    while steps < max_steps and (steps == 0 or time.perf_counter() - start < budget_s):
+    while ((fixed is not None and steps < fixed) or
+           (fixed is None and steps < max_steps and
+            (steps == 0 or time.perf_counter() - start < budget_s))):
         t0 = time.perf_counter()
         oracle.tree_attn(q, K, V, inp.seq_lens, inp.parent, rows=rows)
         t1 = time.perf_counter()
@@ -212,7 +230,8 @@ def time_oracle(inp, budget_s=15.0, max_steps=20):
         t_acc += t2 - t1
         steps += 1
     per_step = (t_attn + t_acc) / steps
-    sample = (f"{steps} full verify step(s) of {w.name}; attention "
+    sample = ((f"{warmup} untimed + " if warmup else "")
+              + f"{steps} timed verify step(s) of {w.name}; attention "
               + ("all rows" if rows is None else f"{len(rows)} of {rows_all} rows, scaled")
               + "; fp64 oracle, OpenMP")
     return per_step, sample, cores
@@ -223,7 +242,8 @@ def run_reference(args, w, idx):
     if rank != 0:
         return
     inp = make_inputs(w, 1000 + idx)
-    per_step, sample, cores = time_oracle(inp, budget_s=max(5.0, 2.0 * args.steps))
+    per_step, sample, cores = time_oracle(inp, budget_s=90.0, steps=args.steps,
+                                          warmup=args.warmup)
     value = w.B * w.N / per_step
     line = {
         "impl": "reference", "metric": "verified tree-nodes/s per attn layer", "value": value,

@@ -2,10 +2,11 @@
 //
 // "EAGLE 演化史", § Tree Verification 详解, A-B: node i of sequence b attends
 // to the cached prefix t < L_b and to tree positions L_b + j for j an ancestor
-// of i or i itself. One warp owns one (sequence, node, query head): the lanes
-// split head_dim, a shuffle reduction gives each score, and an online softmax
-// (running max, running sum, rescaled accumulator) folds the visible tokens in
-// order. fp32 arithmetic throughout with the accurate expf.
+// of i or i itself. One warp owns one (sequence, node, query head): each lane
+// scores one token of a block of 32, and an online softmax (running max,
+// running sum, rescaled accumulator; the lanes split head_dim for the output)
+// folds the visible tokens in blocks of 32. fp32 arithmetic throughout with
+// the accurate expf.
 #include <math.h>
 
 #include "common.cuh"
@@ -74,43 +75,72 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale)
         return;
     }
 
-    float q[E];
-    const Elt *qp = reinterpret_cast<const Elt *>(a.q) + row * D + lane * E;
+    const Elt *qp = reinterpret_cast<const Elt *>(a.q) + row * D;
+    // this warp's q row in shared memory: every lane reads all of it per token
+    __shared__ float sq[4][32 * E];
+    const int wib = (threadIdx.x >> 5) & 3;
 #pragma unroll
-    for (int e = 0; e < E; ++e) q[e] = to_f(qp[e]);
+    for (int e = 0; e < E; ++e) sq[wib][lane * E + e] = to_f(qp[lane * E + e]);
+    __syncwarp();
     const uint64_t anc = a.anc[(size_t)b * a.N + i];
-
+    const Elt *kc = reinterpret_cast<const Elt *>(a.k_cache);
+    const Elt *vc = reinterpret_cast<const Elt *>(a.v_cache);
+    // Blocks of 32 tokens: lane j scores token t0 + j over the whole head
+    // (the whole q row is read by every lane; it stays in L1), the block's
+    // maximum rescales the running output once, and the output lanes (which
+    // split head_dim) then fold the block's V rows in, whose loads are
+    // independent of one another.
     float mx = -INFINITY, l = 0.0f, acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.0f;
-    const Elt *kc = reinterpret_cast<const Elt *>(a.k_cache);
-    const Elt *vc = reinterpret_cast<const Elt *>(a.v_cache);
-    for (long long t = 0; t < Tlen; ++t) {
-        if (t >= L) {
-            const int j = (int)(t - L);
-            if (!((anc >> j) & 1ull)) continue;
+    for (long long t0 = 0; t0 < Tlen; t0 += 32) {
+        const long long t = t0 + lane;
+        bool vis = t < Tlen;
+        if (vis && t >= L) vis = (anc >> (int)(t - L)) & 1ull;
+        size_t off_t = 0;
+        float s = -INFINITY;
+        if (vis) {
+            off_t = (((size_t)pt[t / ps] * ps + (size_t)(t % ps)) * a.Hkv + g) * D;
+            float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 8
+            for (int d = 0; d < D; d += 2) {
+                s0 = fmaf(sq[wib][d], to_f(kc[off_t + d]), s0);
+                s1 = fmaf(sq[wib][d + 1], to_f(kc[off_t + d + 1]), s1);
+            }
+            s = (s0 + s1) * scale;
         }
-        const int page = pt[t / ps];
-        const int slot = (int)(t % ps);
-        const size_t off = (((size_t)page * ps + slot) * a.Hkv + g) * D + lane * E;
-        float s = 0.0f;
+        const float bm = warp_max(s);
+        if (bm == -INFINITY) continue;  // nothing visible in this block
+        const float mn = fmaxf(mx, bm);
+        const float corr = expf(mx - mn);  // 0 on the first visible block
+        const float p = vis ? expf(s - mn) : 0.0f;
+        l = l * corr + warp_sum(p);
 #pragma unroll
-        for (int e = 0; e < E; ++e) s = fmaf(q[e], to_f(kc[off + e]), s);
-        s = warp_sum(s) * scale;
-        const float mn = fmaxf(mx, s);
-        const float corr = expf(mx - mn);
-        const float p = expf(s - mn);
-        l = l * corr + p;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(p, to_f(vc[off + e]), acc[e] * corr);
+        for (int e = 0; e < E; ++e) acc[e] *= corr;
         mx = mn;
+        // eight V rows per batch: the (predicated) loads go out together; a
+        // token with p = 0 is not read (its slot may hold anything)
+        for (int j0 = 0; j0 < 32; j0 += 8) {
+            float pj[8], vv[8][E];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                pj[u] = __shfl_sync(0xffffffffu, p, j0 + u);
+                const size_t oj = __shfl_sync(0xffffffffu, off_t, j0 + u);
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    vv[u][e] = pj[u] != 0.0f ? to_f(vc[oj + lane * E + e]) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(pj[u], vv[u][e], acc[e]);
+        }
     }
     const float inv = 1.0f / l;
 #pragma unroll
     for (int e = 0; e < E; ++e) outp[lane * E + e] = from_f<Elt>(acc[e] * inv);
     if (lane == 0 && a.lse) a.lse[row] = mx + logf(l);
 }
-
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t stream) {
     const long long warps = (long long)a.B * a.N * a.Hq;
     const int threads = 128;
