@@ -149,6 +149,9 @@ CASES = [
     ("g1_many_heads", 7, 1, "binary3", [900], 8, 8, 128, "bf16", 16),
     ("fp32_d64", 8, 2, "worked", [200, 3], 4, 4, 64, "f32", 0),
     ("fp32_d128_paged", 9, 2, "binary3", [150, 40], 8, 2, 128, "f32", 16),
+    # 80 (sequence, KV head) units, lengths from 7 to 2000 tokens
+    ("bf16_mixed_lengths", 13, 10, "chain16",
+     [40, 900, 120, 2000, 333, 64, 1500, 7, 250, 1100], 32, 8, 128, "bf16", 16),
 ]
 
 
@@ -215,6 +218,27 @@ def test_attention_bad_page_and_length_status(sv):
                                     c["parent"][:1])
         tol = BF16_OUT_TOL if dtype == "bf16" else F32_TOL
         assert np.abs(out[0] - o_ref.reshape(out[0].shape)).max() <= tol
+
+
+def test_attention_mixed_lengths_with_bad_sequences(sv):
+    """80 units of mixed lengths with a bad page and a bad length in the batch:
+    those sequences get their status bit and zeros, the rest match."""
+    parent = chain_parent(16)
+    B = 10
+    parent = np.broadcast_to(parent, (B, parent.size)).copy()
+    lens = [40, 900, 120, 2000, 333, 64, 1500, 7, 250, 1100]
+    c = _attn_case(14, B, parent.shape[1], parent, lens, 32, 8, 128, "bf16", 16)
+    c["table"][3, 5] = c["P"] + 9           # page id outside the cache
+    c["lens"][6] = c["table"].shape[1] * 16  # overflows its page table
+    out, lse, status = _run_attn(sv, c, "bf16")
+    want = [0] * B
+    want[3], want[6] = 4, 8
+    assert status.tolist() == want, status
+    assert (out[3] == 0).all() and (out[6] == 0).all()
+    good = [b for b in range(B) if want[b] == 0]
+    o_ref, _ = oracle.tree_attn(c["q"][good], c["K"][good], c["V"][good], c["lens"][good],
+                                c["parent"][good])
+    assert np.abs(out[good] - o_ref.reshape(out[good].shape)).max() <= BF16_OUT_TOL
 
 
 @pytest.mark.parametrize("idx", [0, 1, 2, 3])
