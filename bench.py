@@ -451,9 +451,18 @@ def run_ours(args, w, idx):
             f = sv.eagle2_expand(e2pool, e2rows[r], f, e2k, next_frontier=e2fr[r])
         return sv.eagle2_finalize(e2pool, N, outputs=e2out)
 
+    # the walk on bf16 copies of the logits (one input set: larger than L2)
+    bf_logits = {k: sets[0][k].to(torch.bfloat16) for k in ("target", "draft")}
+    var_out["bf16"] = {}
+
+    def bf16_call(s):
+        sv.spec_accept(bf_logits["target"], bf_logits["draft"], s["tokens"], s["parent"],
+                       s["u_accept"], s["u_bonus"], outputs=var_out["bf16"])
+
     e2out = {}
     var_ms = {}
-    for name, fn in (("greedy", greedy_call), ("onehot", onehot_call), ("eagle2", eagle2_call)):
+    for name, fn in (("greedy", greedy_call), ("onehot", onehot_call), ("eagle2", eagle2_call),
+                     ("bf16", bf16_call)):
         fn(sets[0])
         barrier()
         graphs = [capture(fn, s) for s in sets]
@@ -548,6 +557,13 @@ def run_ours(args, w, idx):
         "config": f"k={e2k}, {e2rounds} rounds, N={N}, B={B}, V={w.V}: init, {e2rounds} "
                   f"expansions, rerank",
         "bytes_note": "draft rows read by the expansions"}}
+    bp = var_out["bf16"]["path"].cpu().numpy()
+    bl = var_out["bf16"]["accept_len"].cpu().numpy()
+    bfb = walk_bytes(w, inp.parent, bp, bl) // 2
+    var_kernels["spec_accept_bf16"] = {
+        "ms": var_ms["bf16"], "bytes": bfb, "gbs": bfb / (var_ms["bf16"] / 1e3) / 1e9,
+        "frac_of_hbm": bfb / (var_ms["bf16"] / 1e3) / 1e9 / peak,
+        "bytes_note": "bf16 rows of the visited nodes (the logits rounded to bf16)"}
     for name in ("greedy", "onehot"):
         vp = var_out[name]["path"].cpu().numpy()
         vl = var_out[name]["accept_len"].cpu().numpy()

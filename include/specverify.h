@@ -219,6 +219,23 @@ int svf_spec_accept_noalloc(const float *target_logits, const float *draft_logit
                             svf_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * svf_spec_accept_bf16 -- svf_spec_accept on bf16 logits.
+ *
+ * The same walk, rule and outputs as svf_spec_accept ("Eagle vs DFlash" and
+ * "EAGLE 演化史", § C); the logits rows are bf16 (raw bits, [B, N, V]) and
+ * are widened exactly to fp32 as they are read, so the result is
+ * svf_spec_accept's on the widened values. Reads half the bytes per visited
+ * row. No workspace.
+ * Limits: 1 <= N <= 1024, 1 <= V <= 262144 (rows held on chip); both logits
+ * arrays 8-byte aligned when V % 4 == 0.
+ * ---------------------------------------------------------------------- */
+int svf_spec_accept_bf16(const void *target_logits, const void *draft_logits,
+                         const int32_t *tokens, const int32_t *parent, const float *u_accept,
+                         const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                         int32_t *path, int32_t *out_tokens, float *ratio, int32_t *status,
+                         svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * svf_spec_accept_greedy -- temperature-0 acceptance over the tree.
  *
  * "Eagle vs DFlash", § A fair evaluation protocol: greedy speculative

@@ -38,6 +38,7 @@ EXPORTED = [
     "svf_spec_accept",
     "svf_spec_accept_noalloc",
     "svf_kv_commit",
+    "svf_spec_accept_bf16",
     "svf_spec_accept_greedy",
     "svf_spec_accept_onehot",
     "svf_eagle2_init",
@@ -77,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_spec_accept.restype = I
     lib.svf_spec_accept_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P]
     lib.svf_spec_accept_noalloc.restype = I
+    lib.svf_spec_accept_bf16.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.svf_spec_accept_bf16.restype = I
     lib.svf_spec_accept_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, P]
     lib.svf_spec_accept_greedy.restype = I
     lib.svf_spec_accept_onehot.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P, P, P]
@@ -243,11 +246,14 @@ def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor, tokens:
                 want_ratio: bool = True, workspace: Optional[torch.Tensor] = None,
                 outputs: Optional[dict] = None, stream=None) -> dict:
     """Acceptance walk. Returns a dict of device tensors: accept_len [B], path [B, N],
-    out_tokens [B, N], ratio [B, N] (or None), status [B]."""
+    out_tokens [B, N], ratio [B, N] (or None), status [B]. Logits are float32 or
+    bfloat16 (both the same dtype)."""
     lib = load_library()
-    _dev(target_logits, "target_logits", torch.float32)
+    _dev(target_logits, "target_logits")
+    if target_logits.dtype not in (torch.float32, torch.bfloat16):
+        raise SpecVerifyError("logits must be float32 or bfloat16")
     B, N, V = target_logits.shape
-    _dev(draft_logits, "draft_logits", torch.float32, (B, N, V))
+    _dev(draft_logits, "draft_logits", target_logits.dtype, (B, N, V))
     _dev(tokens, "tokens", torch.int32, (B, N))
     _dev(parent, "parent", torch.int32, (B, N))
     _dev(u_accept, "u_accept", torch.float32, (B, N))
@@ -260,6 +266,13 @@ def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor, tokens:
         o["out_tokens"] = torch.empty((B, N), dtype=torch.int32, device=dev)
         o["ratio"] = torch.empty((B, N), dtype=torch.float32, device=dev) if want_ratio else None
         o["status"] = torch.empty((B,), dtype=torch.int32, device=dev)
+    if target_logits.dtype == torch.bfloat16:
+        rc = lib.svf_spec_accept_bf16(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parent), _ptr(u_accept),
+            _ptr(u_bonus), B, N, V, _ptr(o["accept_len"]), _ptr(o["path"]),
+            _ptr(o["out_tokens"]), _ptr(o.get("ratio")), _ptr(o["status"]), _stream(stream))
+        _check(rc, "svf_spec_accept_bf16")
+        return o
     need = int(lib.svf_spec_accept_workspace_size(B, N, V))
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)

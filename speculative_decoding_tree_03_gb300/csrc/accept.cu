@@ -95,6 +95,34 @@ __device__ __forceinline__ void load_slice(const float *__restrict__ row, int V,
     }
 }
 
+// The same slice of a bf16 row (VEC: four bf16, 8 bytes, per load), widened
+// exactly to fp32.
+template <int E4, bool VEC>
+__device__ __forceinline__ void load_slice(const __nv_bfloat16 *__restrict__ row, int V, int g0,
+                                           int lane, float4 (&x)[E4]) {
+#pragma unroll
+    for (int k = 0; k < E4; ++k) {
+        const int v0 = (g0 + k) * 128 + lane * 4;
+        if (VEC) {
+            if (v0 < V) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2 *>(row + v0));
+                x[k] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                                   __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+            } else {
+                x[k] = neg_inf4();
+            }
+        } else {
+            x[k].x = v0 + 0 < V ? __bfloat162float(row[v0 + 0]) : -INFINITY;
+            x[k].y = v0 + 1 < V ? __bfloat162float(row[v0 + 1]) : -INFINITY;
+            x[k].z = v0 + 2 < V ? __bfloat162float(row[v0 + 2]) : -INFINITY;
+            x[k].w = v0 + 3 < V ? __bfloat162float(row[v0 + 3]) : -INFINITY;
+        }
+    }
+}
+
+__device__ __forceinline__ float ldg_logit(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float ldg_logit(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
 // Replace the logits of a thread's slice by e^(l - m_t), m_t the thread's own
 // maximum; returns (m_t, sum). A thread with no element returns (-inf, 0).
 template <int E4>
@@ -193,9 +221,9 @@ struct WalkSmem {
     DF gbase;                          // mass before gsel (gmode 1)
 };
 
-template <int NT, int E4, bool VEC, bool CLUSTER>
+template <int NT, int E4, bool VEC, bool CLUSTER, typename T>
 __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
-    const float *__restrict__ target, const float *__restrict__ draft,
+    const T *__restrict__ target, const T *__restrict__ draft,
     const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
     const float *__restrict__ u_accept, const float *__restrict__ u_bonus, int N, int V, int CL,
     int32_t *__restrict__ accept_len, int32_t *__restrict__ path,
@@ -293,9 +321,9 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
                 }
             const size_t row = (base + pp) * (size_t)V + stok[i];
             if (i < NT) {
-                lx_mine = make_float2(__ldg(target + row), __ldg(draft + row));
+                lx_mine = make_float2(ldg_logit(target + row), ldg_logit(draft + row));
             } else {
-                slx[i] = make_float2(__ldg(target + row), __ldg(draft + row));
+                slx[i] = make_float2(ldg_logit(target + row), ldg_logit(draft + row));
             }
         }
         snext[i] = nx;
@@ -383,7 +411,10 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
             // ask L2 for this CTA's slice of the first child's rows
             const int s0 = rank * NG * 128;
             if (s0 < V) {
-                const uint32_t bytes = (uint32_t)min(NG * 128, V - s0) * 4u;
+                // (a bulk prefetch wants a multiple of 16 bytes; the tail of
+                // a bf16 row may be left out, it is only a hint)
+                const uint32_t bytes =
+                    ((uint32_t)min(NG * 128, V - s0) * (uint32_t)sizeof(T)) & ~15u;
                 prefetch_l2_bulk(target + (base + c1) * V + s0, bytes);
                 if (sfirst[c1] >= 0) prefetch_l2_bulk(draft + (base + c1) * V + s0, bytes);
             }
@@ -655,13 +686,13 @@ size_t walk_smem(int N, const WalkCfg &c) {
            (size_t)(c.nt / 32) * c.e4 * sizeof(float) + 16;
 }
 
-template <int NT, int E4, bool VEC, bool CLUSTER>
-cudaError_t launch_walk(const WalkCfg &c, const float *target, const float *draft,
+template <int NT, int E4, bool VEC, bool CLUSTER, typename T>
+cudaError_t launch_walk(const WalkCfg &c, const T *target, const T *draft,
                         const int32_t *tokens, const int32_t *parent, const float *u_accept,
                         const float *u_bonus, int B, int N, int V, int32_t *accept_len,
                         int32_t *path, int32_t *out_tokens, float *ratio, int32_t *status,
                         cudaStream_t stream) {
-    auto kern = accept_walk_kernel<NT, E4, VEC, CLUSTER>;
+    auto kern = accept_walk_kernel<NT, E4, VEC, CLUSTER, T>;
     const size_t smem = walk_smem(N, c);
     if (smem > 48 * 1024) {
         cudaError_t e =
@@ -678,14 +709,15 @@ cudaError_t launch_walk(const WalkCfg &c, const float *target, const float *draf
                       accept_len, path, out_tokens, ratio, status);
 }
 
-template <bool VEC>
-cudaError_t dispatch_walk(const WalkCfg &c, const float *target, const float *draft,
+template <bool VEC, typename T>
+cudaError_t dispatch_walk(const WalkCfg &c, const T *target, const T *draft,
                           const int32_t *tokens, const int32_t *parent, const float *u_accept,
                           const float *u_bonus, int B, int N, int V, int32_t *accept_len,
                           int32_t *path, int32_t *out_tokens, float *ratio, int32_t *status,
                           cudaStream_t stream) {
 #define SVF_WALK(NT_, E4_, CL_)                                                                  \
-    return launch_walk<NT_, E4_, VEC, CL_>(c, target, draft, tokens, parent, u_accept, u_bonus, \
+    return launch_walk<NT_, E4_, VEC, CL_, T>(c, target, draft, tokens, parent, u_accept,       \
+                                              u_bonus,                                         \
                                            B, N, V, accept_len, path, out_tokens, ratio, status, \
                                            stream)
     if (c.nt == 32) {
@@ -727,12 +759,30 @@ cudaError_t launch_accept(const float *target, const float *draft, const int32_t
         return launch_accept_stream(target, draft, tokens, parent, u_accept, u_bonus, B, N, V,
                                     accept_len, path, out_tokens, ratio, workspace, status,
                                     stream);
-    return (V & 3) == 0 ? dispatch_walk<true>(c, target, draft, tokens, parent, u_accept, u_bonus,
-                                              B, N, V, accept_len, path, out_tokens, ratio,
-                                              status, stream)
-                        : dispatch_walk<false>(c, target, draft, tokens, parent, u_accept,
-                                               u_bonus, B, N, V, accept_len, path, out_tokens,
-                                               ratio, status, stream);
+    return (V & 3) == 0 ? dispatch_walk<true, float>(c, target, draft, tokens, parent, u_accept,
+                                                     u_bonus, B, N, V, accept_len, path,
+                                                     out_tokens, ratio, status, stream)
+                        : dispatch_walk<false, float>(c, target, draft, tokens, parent, u_accept,
+                                                      u_bonus, B, N, V, accept_len, path,
+                                                      out_tokens, ratio, status, stream);
+}
+
+bool accept_bf16_supported(int V) { return V >= 1 && accept_on_chip(V); }
+
+cudaError_t launch_accept_bf16(const __nv_bfloat16 *target, const __nv_bfloat16 *draft,
+                               const int32_t *tokens, const int32_t *parent,
+                               const float *u_accept, const float *u_bonus, int B, int N, int V,
+                               int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                               float *ratio, int32_t *status, cudaStream_t stream) {
+    WalkCfg c;
+    if (!walk_config(B, V, &c)) return cudaErrorInvalidValue;
+    return (V & 3) == 0
+               ? dispatch_walk<true, __nv_bfloat16>(c, target, draft, tokens, parent, u_accept,
+                                                    u_bonus, B, N, V, accept_len, path,
+                                                    out_tokens, ratio, status, stream)
+               : dispatch_walk<false, __nv_bfloat16>(c, target, draft, tokens, parent, u_accept,
+                                                     u_bonus, B, N, V, accept_len, path,
+                                                     out_tokens, ratio, status, stream);
 }
 
 }  // namespace svf

@@ -138,6 +138,27 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 
+int svf_spec_accept_bf16(const void *target_logits, const void *draft_logits,
+                         const int32_t *tokens, const int32_t *parent, const float *u_accept,
+                         const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                         int32_t *path, int32_t *out_tokens, float *ratio, int32_t *status,
+                         svf_stream_t stream) {
+    if (B < 0 || N < 0 || V < 0) return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (!target_logits || !draft_logits || !tokens || !parent || !u_accept || !u_bonus ||
+        !accept_len || !path || !out_tokens || !status)
+        return SVF_ERR_ARG;
+    if (N < 1 || N > 1024 || V < 1 || !accept_bf16_supported(V)) return SVF_ERR_UNSUPPORTED;
+    if ((V & 3) == 0 && (((uintptr_t)target_logits | (uintptr_t)draft_logits) & 7u) != 0)
+        return SVF_ERR_ARG;
+    cudaError_t e = launch_accept_bf16(reinterpret_cast<const __nv_bfloat16 *>(target_logits),
+                                       reinterpret_cast<const __nv_bfloat16 *>(draft_logits),
+                                       tokens, parent, u_accept, u_bonus, B, N, V, accept_len,
+                                       path, out_tokens, ratio, status,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
 static int accept_variant_args(const float *target, const int32_t *tokens, const int32_t *parent,
                                int B, int N, int V, const int32_t *accept_len,
                                const int32_t *path, const int32_t *out_tokens,

@@ -30,6 +30,14 @@ cudaError_t launch_eagle2_finalize(int B, int C, const int32_t *parent, const in
                                    int32_t *out_token, double *out_value, int32_t *out_cid,
                                    int32_t *n_out, cudaStream_t stream);
 
+// The acceptance walk on bf16 logits (accept.cu; on-chip vocabularies only).
+bool accept_bf16_supported(int V);
+cudaError_t launch_accept_bf16(const __nv_bfloat16 *target, const __nv_bfloat16 *draft,
+                               const int32_t *tokens, const int32_t *parent,
+                               const float *u_accept, const float *u_bonus, int B, int N, int V,
+                               int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                               float *ratio, int32_t *status, cudaStream_t stream);
+
 // Target-only acceptance variants (accept_target.cu): greedy or one-hot q.
 bool accept_target_supported(int V);
 cudaError_t launch_accept_target(bool greedy, const float *target, const int32_t *tokens,

@@ -117,6 +117,17 @@ def test_kv_commit_argument_checks(lib):
     assert call(k=ctypes.c_void_p(264)) == -1           # not 16-byte aligned
 
 
+def test_accept_bf16_argument_checks(lib):
+    def call(B=2, N=3, V=100, t=P):
+        return lib.svf_spec_accept_bf16(t, P, P, P, P, P, B, N, V, P, P, P, None, P, None)
+    assert call(B=-1) == -1
+    assert call(B=0, t=None) == 0
+    assert call(t=None) == -1
+    assert call(N=0) == -2 and call(N=1025) == -2
+    assert call(V=262145) == -2                      # only on-chip vocabularies
+    assert call(t=ctypes.c_void_p(260)) == -1        # 8-byte loads of four bf16
+
+
 def test_accept_variant_argument_checks(lib):
     def greedy(B=2, N=3, V=100, t=P):
         return lib.svf_spec_accept_greedy(t, P, P, B, N, V, P, P, P, P, None)

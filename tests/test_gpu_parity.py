@@ -357,6 +357,40 @@ def test_accept_many_sequences(sv, V):
     compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
 
 
+def _accept_gpu_bf16(sv, arrs):
+    """The bf16 call on the logits rounded to bf16; returns the GPU results
+    and the widened (exact) fp32 arrays the oracle is run on."""
+    wide = dict(arrs)
+    t = {}
+    for k in ("target", "draft"):
+        bits = f32_to_bf16_bits(np.ascontiguousarray(arrs[k], np.float32))
+        wide[k] = bf16_bits_to_f32(bits)
+        t[k] = bf16_tensor(bits, "cuda")
+    for k in ("tokens", "parent", "u_accept", "u_bonus"):
+        t[k] = torch.from_numpy(np.ascontiguousarray(arrs[k])).cuda()
+    res = sv.spec_accept(t["target"], t["draft"], t["tokens"], t["parent"], t["u_accept"],
+                         t["u_bonus"])
+    torch.cuda.synchronize()
+    return {k: (_np(v) if v is not None else None) for k, v in res.items()}, wide
+
+
+@pytest.mark.parametrize("V", [8, 37, 1000, 5003, 32000, 128256])
+def test_accept_bf16_logits(sv, V):
+    """bf16 logits (vector and scalar loads, warp, block and cluster paths)
+    against the oracle on the widened values."""
+    arrs = _synthetic_accept(V + 3, 48, 7, V, [-1, 0, 0, 1, 1, 2, 2], sigma=2.0, noise=0.7)
+    gpu, wide = _accept_gpu_bf16(sv, arrs)
+    compare_accept(gpu, wide, oracle.spec_accept(**wide))
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_accept_bf16_workloads(sv, idx):
+    w = WORKLOADS[idx]
+    inp = make_inputs(w, 1000 + idx, with_kv=False)
+    gpu, wide = _accept_gpu_bf16(sv, _arrays(inp))
+    compare_accept(gpu, wide, oracle.spec_accept(**wide))
+
+
 def test_accept_streaming_vocabulary(sv):
     """A vocabulary above what one cluster holds on chip (262144) takes the
     streaming kernels with their statistics pre-pass."""
