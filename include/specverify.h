@@ -388,6 +388,23 @@ int svf_kv_commit(void *k_cache, void *v_cache, int num_layers, long long layer_
                   int N, int Hkv, int D, int dtype, int32_t *new_seq_lens, int32_t *freed_pages,
                   int max_free, int32_t *n_freed, int32_t *status, svf_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * svf_selftest_wait_timeout -- a diagnostic: make a bounded wait run out.
+ *
+ * Every wait of this library's kernels on an mbarrier (for a TMA copy, a
+ * tensor-core commit, another warp or another CTA of a cluster) gives up
+ * after a deadline (2 s in the product kernels); the waiting CTA then leaves
+ * its loops, releases what it holds and sets SVF_DEV_TIMEOUT in the
+ * caller's status word, and the CUDA context stays usable. This call runs
+ * the same wait helpers, with deadline_ns (1 us .. 1 s), on mbarriers that
+ * nothing ever completes: one inside a CTA and one that a peer CTA of a
+ * two-CTA cluster would complete. result [4] int32 (device): status of the
+ * CTA wait, its elapsed microseconds, status of the cluster wait, its
+ * elapsed microseconds; both statuses are SVF_DEV_TIMEOUT when the waits
+ * are bounded. Nothing faults or traps.
+ * ---------------------------------------------------------------------- */
+int svf_selftest_wait_timeout(int32_t *result, long long deadline_ns, svf_stream_t stream);
+
 /* Human-readable name of a host return code or of one device status bit. */
 const char *svf_status_string(int code);
 

@@ -38,6 +38,7 @@ EXPORTED = [
     "svf_spec_accept",
     "svf_spec_accept_noalloc",
     "svf_kv_commit",
+    "svf_selftest_wait_timeout",
     "svf_spec_accept_bf16",
     "svf_spec_accept_greedy",
     "svf_spec_accept_onehot",
@@ -90,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_eagle2_expand.restype = I
     lib.svf_eagle2_finalize.argtypes = [I, I, P, P, P, P, P, I, P, P, P, P, P, P]
     lib.svf_eagle2_finalize.restype = I
+    lib.svf_selftest_wait_timeout.argtypes = [P, ctypes.c_longlong, P]
+    lib.svf_selftest_wait_timeout.restype = I
     lib.svf_kv_commit.argtypes = [P, P, I, ctypes.c_longlong, I, I, P, I, P, P, P, I, I, I, I,
                                   I, P, P, I, P, P, P]
     lib.svf_kv_commit.restype = I
@@ -405,6 +408,18 @@ def eagle2_finalize(pool: dict, n_nodes: int, outputs: Optional[dict] = None,
                                  _stream(stream))
     _check(rc, "svf_eagle2_finalize")
     return out
+
+
+def selftest_wait_timeout(deadline_s: float = 0.02, device="cuda", stream=None) -> dict:
+    """Run the bounded-wait diagnostic; returns the statuses and elapsed
+    times (seconds) of a CTA wait and a cluster wait that nothing completes."""
+    lib = load_library()
+    res = torch.zeros((4,), dtype=torch.int32, device=device)
+    rc = lib.svf_selftest_wait_timeout(_ptr(res), int(deadline_s * 1e9), _stream(stream))
+    _check(rc, "svf_selftest_wait_timeout")
+    r = res.cpu().tolist()
+    return {"cta_status": r[0], "cta_elapsed_s": r[1] * 1e-6,
+            "cluster_status": r[2], "cluster_elapsed_s": r[3] * 1e-6}
 
 
 # ---------------------------------------------------------------------------

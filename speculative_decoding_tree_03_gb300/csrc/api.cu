@@ -249,6 +249,13 @@ int svf_eagle2_finalize(int B, int capacity, const int32_t *pool_parent,
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 
+int svf_selftest_wait_timeout(int32_t *result, long long deadline_ns, svf_stream_t stream) {
+    if (!result || deadline_ns < 1000 || deadline_ns > 1000000000ll) return SVF_ERR_ARG;
+    cudaError_t e = launch_selftest_wait(result, (unsigned long long)deadline_ns,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
 int svf_kv_commit(void *k_cache, void *v_cache, int num_layers, long long layer_stride,
                   int num_pages, int page_size, const int32_t *page_table, int max_pages,
                   const int32_t *seq_lens, const int32_t *path, const int32_t *accept_len, int B,

@@ -74,19 +74,23 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete. Gives up after the
 // deadline or as soon as another thread of the CTA raised *abort; returns
 // false then (and raises *abort itself on a timeout).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                              unsigned long long deadline_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitDeadlineNs) {
+            if (globaltimer_ns() - t0 > deadline_ns) {
                 *abort = 1;
                 return false;
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return mbar_wait_for(bar, parity, abort, kWaitDeadlineNs);
 }
 
 // ---------------------------------------------------------------- clusters
@@ -122,13 +126,17 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
 
 // Bounded wait for a phase completed by other CTAs of the cluster; false after
 // the deadline.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_cluster_for(uint64_t *bar, uint32_t parity,
+                                                      unsigned long long deadline_ns) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitDeadlineNs) return false;
+        if ((it & 63u) == 0 && globaltimer_ns() - t0 > deadline_ns) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_cluster_for(bar, parity, kWaitDeadlineNs);
 }
 
 __device__ __forceinline__ void cluster_arrive() {

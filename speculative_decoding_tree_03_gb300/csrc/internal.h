@@ -13,6 +13,10 @@ namespace svf {
 cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint64_t *anc, int32_t *depth,
                              int32_t *status, cudaStream_t stream);
 
+// A bounded wait that runs out on purpose (selftest.cu).
+cudaError_t launch_selftest_wait(int32_t *result, unsigned long long deadline_ns,
+                                 cudaStream_t stream);
+
 // EAGLE-2 tree construction (eagle2.cu).
 constexpr int kEagle2MaxK = 16;
 constexpr int kEagle2MaxPool = 2048;

@@ -144,6 +144,12 @@ def test_accept_variant_argument_checks(lib):
     assert onehot(u=None) == -1
 
 
+def test_selftest_argument_checks(lib):
+    assert lib.svf_selftest_wait_timeout(None, 10 ** 6, None) == -1
+    assert lib.svf_selftest_wait_timeout(P, 10, None) == -1          # below 1 us
+    assert lib.svf_selftest_wait_timeout(P, 2 * 10 ** 9, None) == -1  # above 1 s
+
+
 def test_workspace_sizes_without_gpu(lib):
     # bf16 attention with many KV tiles per (sequence, head) splits the KV range
     n = lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 1, 1, 2176)
