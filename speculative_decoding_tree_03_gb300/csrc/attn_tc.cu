@@ -63,6 +63,10 @@ __host__ __device__ constexpr int vstages_for(int NH) { return NH == 1 ? 6 : 5; 
 // 512 TMEM columns with two halves; one half has room for four.
 __host__ __device__ constexpr int sbuffers_for(int NH) { return NH == 1 ? 4 : 2; }
 constexpr int kFixedTiles = 3;              // prologue + epilogue cost, in tiles
+// The combine reads a row's partials eight chunks at a time; each group of
+// eight costs about this many tiles of the call's time (measured: 8 chunks
+// beat 17 on a 33-tile, 8-unit batch, 14.4 against 16.4 us).
+constexpr float kCombineGroupTiles = 3.5f;
 // Warps: a K and a V producer, a QK issuer and a PV issuer per half, four
 // softmax warps per half. One thread issuing tcgen05.mma (or TMA copies)
 // sustains about one instruction per 100 cycles; several issuing warps
@@ -724,8 +728,9 @@ static bool make_q_map(CUtensorMap *map, const void *q, int B, int N, int Hq, in
 static int row_halves(int M) { return M > 128 ? 2 : 1; }
 
 // Chunk count of the KV range per (sequence, KV head, row block): minimises
-// max(waves x (tiles per chunk + fixed cost), total bytes / bandwidth), where
-// the bytes count the partial outputs written and read back, with at most
+// max(waves x (tiles per chunk + fixed cost), total bytes / bandwidth) plus
+// the combine's latency (one term per group of eight chunks), where the
+// bytes count the partial outputs written and read back, with at most
 // CMAX_TILES tiles per chunk.
 int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) {
     const int G = Hq / Hkv;
@@ -747,7 +752,8 @@ int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) 
         const long long waves = (units * s + C - 1) / C;
         const double t_chain = (double)waves * (per_cta + tc::kFixedTiles);
         const double t_bytes = (double)units * (tiles + (s > 1 ? s * part_tiles : 0.0)) / C;
-        const double t = t_chain > t_bytes ? t_chain : t_bytes;
+        const double t = (t_chain > t_bytes ? t_chain : t_bytes) +
+                         (s > 1 ? tc::kCombineGroupTiles * ((s + 7) / 8) : 0.0);
         if (t < best - 1e-9) {
             best = t;
             best_s = s;
