@@ -179,7 +179,7 @@ def _oracle_inputs(inp):
     return cvt(inp.q), K, V
 
 
-def time_oracle(inp, budget_s=15.0, max_steps=20, steps=None, warmup=0):
+def time_oracle(inp, budget_s=15.0, max_steps=20, steps=None, warmup=0, threads=None):
     """Time the fp64 oracle for the whole verify step on the host cores.
 
     Without ``steps``: as many steps as fit in ``budget_s`` (at most
@@ -188,7 +188,7 @@ def time_oracle(inp, budget_s=15.0, max_steps=20, steps=None, warmup=0):
     in ``budget_s``. Returns (seconds per step, sample text, cores)."""
     import oracle
     w = inp.w
-    cores = len(os.sched_getaffinity(0))
+    cores = threads or len(os.sched_getaffinity(0))
     oracle.set_threads(cores)
     q, K, V = _oracle_inputs(inp)
     rows_all = w.B * w.N * w.Hq
@@ -632,6 +632,13 @@ def run_ours(args, w, idx):
         per_step, sample, cores = time_oracle(inp)
         line["cpu_baseline"] = {"value": B * N / per_step, "unit": "nodes/s", "cores": cores,
                                 "kind": "oracle", "sample": sample}
+        if idx <= 2:
+            # the small workloads are also timed on one core
+            import oracle
+            per1, sample1, _ = time_oracle(inp, budget_s=10.0, max_steps=5, threads=1)
+            oracle.set_threads(cores)
+            line["cpu_baseline"]["single_thread"] = {"value": B * N / per1, "unit": "nodes/s",
+                                                     "cores": 1, "sample": sample1}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

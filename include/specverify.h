@@ -312,7 +312,8 @@ int svf_spec_accept_onehot(const float *target_logits, const int32_t *tokens,
  * value(f) * softmax(row)[token]; pool_count advances by k per valid row
  * (capped at capacity; children past it are dropped). next_frontier [B, k]
  * int32 gets the ids of the k most valuable new children (value desc, id
- * asc), -1 padded: the nodes to draft from next.
+ * asc), -1 padded: the nodes to draft from next. V <= 1048576 (else
+ * SVF_ERR_UNSUPPORTED).
  *
  * svf_eagle2_finalize: keeps the root and the n_nodes - 1 most valuable other
  * nodes (value desc, depth asc, id asc) and numbers them level by level, a

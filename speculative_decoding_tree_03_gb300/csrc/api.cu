@@ -223,7 +223,8 @@ int svf_eagle2_expand(const float *draft_rows, int B, int R, int V, int k,
     if (!draft_rows || !frontier || !pool_parent || !pool_depth || !pool_token || !pool_value ||
         !pool_count || !next_frontier)
         return SVF_ERR_ARG;
-    if (R < 1 || R > 65535 || k < 1 || k > kEagle2MaxK || k > V || capacity > kEagle2MaxPool)
+    if (R < 1 || R > 65535 || k < 1 || k > kEagle2MaxK || k > V || V > kEagle2MaxV ||
+        capacity > kEagle2MaxPool)
         return SVF_ERR_UNSUPPORTED;
     cudaError_t e = launch_eagle2_expand(draft_rows, B, R, V, k, frontier, capacity, pool_parent,
                                          pool_depth, pool_token, pool_value, pool_count,

@@ -12,9 +12,10 @@
 // The drafter runs between rounds, so the construction is three calls on a
 // per-sequence node pool (creation id = pool index; the root is id 0):
 //   eagle2_init_kernel      the root;
-//   eagle2_rows_kernel      one CTA per frontier row: softmax statistics and
-//                           the row's top-k tokens in one pass over V, then
-//                           the k children written at fixed pool slots;
+//   eagle2_rows_kernel      a cluster of CTAs per frontier row: softmax
+//                           statistics and the row's top-k tokens in one
+//                           pass over V, then the k children written at
+//                           fixed pool slots;
 //   eagle2_select_kernel    the next frontier, the k best new children;
 //   eagle2_finalize_kernel  rerank and BFS numbering, one CTA per sequence.
 // The row pass is bound by HBM (R rows of V floats per sequence and round);
@@ -22,8 +23,12 @@
 #include <float.h>
 #include <limits.h>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace svf {
 
@@ -32,6 +37,7 @@ namespace e2 {
 constexpr int kRowThreads = 1024;
 constexpr int kSelThreads = 256;
 constexpr int kFinThreads = 512;
+constexpr int kMaxSlices = 8;          // CTAs per row (a portable cluster)
 
 // (logit, id) order of the top-k search: larger logit first, then lower id.
 __device__ __forceinline__ bool before(float a, int ia, float b, int ib) {
@@ -56,161 +62,269 @@ __global__ void eagle2_init_kernel(const int32_t *__restrict__ root_tokens, int 
     count[b] = 1;
 }
 
-// One CTA per (frontier row r, sequence b). Child i of frontier node f gets
-// pool slot count[b] + r k + i.
-template <int KMAX>  // merge list length, KMAX >= k
+// One cluster of P CTAs per (frontier row r, sequence b), each CTA over a
+// contiguous slice of the row. A CTA reads its slice once: every thread keeps
+// a running (max, sum e^(l - max)) and its own best (logit, id). The k-th best
+// of the CTA's thread bests, T, bounds the slice's top-k from below, and only
+// the (at most k) threads whose best reaches T can hold a top-k element: they
+// re-read their elements (from cache) and post those that reach T, at most
+// k * 128 of them, for an exact rank. Rank 0 of the cluster merges the slices'
+// statistics and top-k lists (sent into its shared memory) and writes the
+// children: child i of frontier node f gets pool slot count[b] + r k + i.
+namespace e2 {
+
+constexpr int kGroups = 4;                         // float4 groups per thread per batch
+constexpr int kPerBatch = 4 * kGroups;             // elements per thread per batch
+constexpr int kBatchElems = kRowThreads * kPerBatch;
+constexpr int kMaxBatches = 8;                     // batches per slice (the candidate bound)
+
+// element j of a thread's batch at `base`: group j / 4, lane j % 4
+__device__ __forceinline__ int elem_id(int base, int j) {
+    return base + ((j >> 2) * kRowThreads + (int)threadIdx.x) * 4 + (j & 3);
+}
+
+// A thread's 16 elements of the batch at `base`; -inf past `hi`. VEC: 16-byte
+// loads (the row start and `hi` are multiples of 4 elements).
+template <bool VEC>
+__device__ __forceinline__ void load_batch(const float *__restrict__ row, int base, int hi,
+                                           float (&x)[kPerBatch]) {
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+        const int i = elem_id(base, 4 * g);
+        if (VEC) {
+            float4 t = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (i < hi) t = __ldg(reinterpret_cast<const float4 *>(row + i));
+            x[4 * g] = t.x;
+            x[4 * g + 1] = t.y;
+            x[4 * g + 2] = t.z;
+            x[4 * g + 3] = t.w;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) x[4 * g + c] = i + c < hi ? __ldg(row + i + c) : -INFINITY;
+        }
+    }
+}
+
+// k-way merge of n sorted lists (best first, k entries each) by warp 0: lane
+// q follows list q. Writes the k best (id INT_MAX past the real entries).
+template <int KMAX>
+__device__ __forceinline__ void merge_lists(const float (*lv)[KMAX], const int (*li)[KMAX],
+                                            int n, int k, float *outv, int *outi) {
+    const int lane = threadIdx.x & 31;
+    int h = 0;
+    for (int i = 0; i < k; ++i) {
+        float bv = (lane < n && h < k) ? lv[lane][h] : -INFINITY;
+        int bi = (lane < n && h < k) ? li[lane][h] : INT_MAX;
+        const int mine = bi;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (before(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (lane == 0) {
+            outv[i] = bv;
+            outi[i] = bi;
+        }
+        if (mine == bi && bi != INT_MAX) ++h;
+    }
+}
+
+}  // namespace e2
+
+template <int KMAX, bool VEC>  // KMAX >= k
 __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
-    const float *__restrict__ rows, int R, int V, int k, const int32_t *__restrict__ frontier,
-    int C, int32_t *__restrict__ parent, int32_t *__restrict__ depth, int32_t *__restrict__ token,
-    double *__restrict__ value, const int32_t *__restrict__ count) {
+    const float *__restrict__ rows, int R, int V, int k, int P,
+    const int32_t *__restrict__ frontier, int C, int32_t *__restrict__ parent,
+    int32_t *__restrict__ depth, int32_t *__restrict__ token, double *__restrict__ value,
+    const int32_t *__restrict__ count) {
     using namespace e2;
     constexpr int NW = kRowThreads / 32;
-    const int r = blockIdx.x, b = blockIdx.y;
+    constexpr int kCand = KMAX * kMaxBatches * kPerBatch;  // k threads x their elements
+    static_assert(NW == 32, "one lane of warp 0 per warp");
+    const int r = blockIdx.x / P, rank = blockIdx.x % P, b = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // this CTA's slice of the row, a multiple of 32 elements wide
+    const int per = ((V + P - 1) / P + 31) & ~31;
+    const int lo = rank * per, hi = min(V, lo + per);
+    __shared__ float s_rm[kMaxSlices];            // rank 0: the slices' maxima
+    __shared__ double s_rz[kMaxSlices];           //   their sums
+    __shared__ float s_rv[kMaxSlices][KMAX];      //   their top-k lists
+    __shared__ int s_ri[kMaxSlices][KMAX];
     __shared__ float s_m[NW];
     __shared__ double s_z[NW];
-    __shared__ int s_win[KMAX];
+    __shared__ double s_Z;
+    __shared__ float s_lv[NW][KMAX];              // each warp's best thread bests
+    __shared__ int s_li[NW][KMAX];
     __shared__ float s_winv[KMAX];
+    __shared__ int s_win[KMAX];
+    __shared__ float s_cv[kCand];                 // candidates reaching T
+    __shared__ int s_ci[kCand];
+    __shared__ int s_nc;
     pdl_wait();
     pdl_launch_dependents();
+    if (P > 1) cluster_arrive();  // waited on before the first remote store
     const int f = frontier[(size_t)b * R + r];
     if (f < 0 || f >= min(count[b], C)) return;  // an unused frontier slot
     const float *row = rows + ((size_t)b * R + r) * (size_t)V;
+    constexpr float kLog2e = 1.4426950408889634f;
 
-    // one pass: each thread's running (max, sum e^(l - max)); each warp's
-    // top-k, kept sorted (best first) in lanes 0 .. k-1 of (wv, wi). A chunk
-    // of 32 elements (one per lane) is compared with the warp's k-th entry and
-    // only the lanes that beat it (a ballot) are inserted, one at a time.
-    float m = -INFINITY;
-    float z = 0.0f;
-    float wv = -INFINITY;
-    int wi = INT_MAX;
-    float tv = -INFINITY;  // the warp's k-th entry, identical in every lane
-    int tix = INT_MAX;
-    constexpr int kBatch = KMAX >= 16 ? 8 : 16;
-    // the loop bound is the warp's first element, so every lane of a warp runs
-    // the same iterations (the ballots and shuffles need the whole warp)
-    for (int v0 = threadIdx.x; v0 - lane < V; v0 += kBatch * kRowThreads) {
-        float lb[kBatch];
+    // the one pass over the slice
+    float m = -INFINITY, z = 0.0f;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int base = lo; base < hi; base += kBatchElems) {
+        float x[kPerBatch];
+        load_batch<VEC>(row, base, hi, x);
+        float bm = fmax3(x[0], x[1], x[2]);
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int v = v0 + u * kRowThreads;
-            lb[u] = v < V ? __ldg(row + v) : -INFINITY;
-        }
-        // running (max, sum e^(l - max)): one rescale per batch
-        float bm = lb[0];
-#pragma unroll
-        for (int u = 1; u + 1 < kBatch; u += 2) bm = fmax3(bm, lb[u], lb[u + 1]);
-        if (kBatch % 2 == 0) bm = fmaxf(bm, lb[kBatch - 1]);
-        if (bm > m) {
-            z = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - bm) * 1.4426950408889634f);
+        for (int j = 3; j + 1 < kPerBatch; j += 2) bm = fmax3(bm, x[j], x[j + 1]);
+        bm = fmaxf(bm, x[kPerBatch - 1]);
+        if (bm > m) {  // one rescale per batch
+            z = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - bm) * kLog2e);
             m = bm;
         }
-        if (m != -INFINITY) {  // (a thread with no element yet keeps z = 0)
-            const float ml2 = m * 1.4426950408889634f;
+        if (m != -INFINITY) {
+            const float ml2 = m * kLog2e;
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                z += ex2_approx(fmaf(lb[u], 1.4426950408889634f, -ml2));
+            for (int j = 0; j < kPerBatch; ++j) z += ex2_approx(fmaf(x[j], kLog2e, -ml2));
         }
-        // candidates for the warp's top-k
+        if (bm > bv || (bm == bv && bi == INT_MAX)) {
+            // a new best for this thread: the batch's first element equal to
+            // bm (ids grow with j and from batch to batch)
+            int bj = -1;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int v = v0 + u * kRowThreads;
-            const float l = lb[u];
-            unsigned mask = __ballot_sync(0xffffffffu, v < V && before(l, v, tv, tix));
-            if (!mask) continue;
-            while (mask) {
-                const int src = __ffs(mask) - 1;
-                mask &= mask - 1;
-                const float cv = __shfl_sync(0xffffffffu, l, src);
-                const int ci = __shfl_sync(0xffffffffu, v, src);
-                // position = entries that stay ahead of the candidate
-                const int pos = __popc(__ballot_sync(0xffffffffu,
-                                                     lane < k && before(wv, wi, cv, ci)));
-                const float upv = __shfl_up_sync(0xffffffffu, wv, 1);
-                const int upi = __shfl_up_sync(0xffffffffu, wi, 1);
-                if (pos < k && lane < k) {
-                    if (lane == pos) {
-                        wv = cv;
-                        wi = ci;
-                    } else if (lane > pos) {
-                        wv = upv;
-                        wi = upi;
-                    }
-                }
+            for (int j = kPerBatch - 1; j >= 0; --j)
+                if (x[j] == bm && elem_id(base, j) < hi) bj = j;
+            if (bj >= 0 && before(bm, elem_id(base, bj), bv, bi)) {
+                bv = bm;
+                bi = elem_id(base, bj);
             }
-            tv = __shfl_sync(0xffffffffu, wv, k - 1);
-            tix = __shfl_sync(0xffffffffu, wi, k - 1);
         }
     }
-    // softmax statistics of the row: (max, sum) over the warp and the CTA
+
+    // softmax statistics of the slice: (max, sum) over the warp and the CTA
     float M = m;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float zw = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - M) * 1.4426950408889634f);
+    float zw = (m == -INFINITY) ? 0.0f : z * ex2_approx((m - M) * kLog2e);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) zw += __shfl_xor_sync(0xffffffffu, zw, o);
-    __shared__ float s_lv[NW][KMAX];
-    __shared__ int s_li[NW][KMAX];
+    // the warp's thread bests sorted best first (a bitonic sort over lanes)
+    float sv = bv;
+    int si = bi;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, sv, stride);
+            const int oi = __shfl_xor_sync(0xffffffffu, si, stride);
+            const bool best_first = (lane & size) == 0 || size == 32;
+            const bool low = (lane & stride) == 0;
+            const bool take = (best_first == low) ? before(ov, oi, sv, si) : before(sv, si, ov, oi);
+            if (take) {
+                sv = ov;
+                si = oi;
+            }
+        }
+    }
     if (lane == 0) {
         s_m[warp] = M;
         s_z[warp] = (double)zw;
     }
     if (lane < k) {
-        s_lv[warp][lane] = wv;
-        s_li[warp][lane] = wi;
+        s_lv[warp][lane] = sv;
+        s_li[warp][lane] = si;
     }
     __syncthreads();
     float Mc = -INFINITY;
     for (int w = 0; w < NW; ++w) Mc = fmaxf(Mc, s_m[w]);
-    static_assert(NW == 32, "one lane of warp 0 per warp");
-    __shared__ double s_Z;
     if (warp == 0) {
-        // the row's normaliser: one lane per warp, fp32 exponentials and an
+        // the slice's normaliser: one lane per warp, fp32 exponentials and an
         // fp64 sum (this part's fp64 pipe is slow, so no fp64 exp)
         double t = s_m[lane] == -INFINITY
                        ? 0.0
-                       : s_z[lane] * (double)ex2_approx((s_m[lane] - Mc) * 1.4426950408889634f);
+                       : s_z[lane] * (double)ex2_approx((s_m[lane] - Mc) * kLog2e);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0) s_Z = t;
-        // the row's top-k: a k-way merge of the warps' sorted lists, lane w
-        // holding warp w's list as a shift register (head = element 0)
-        float hv[KMAX];
-        int hx[KMAX];
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            hv[j] = j < k ? s_lv[lane][j] : -INFINITY;
-            hx[j] = j < k ? s_li[lane][j] : INT_MAX;
+        if (lane == 0) {
+            s_Z = t;
+            s_nc = 0;
         }
-        for (int i = 0; i < k; ++i) {
-            float bv = hv[0];
-            int bi = hx[0];
+        merge_lists<KMAX>(s_lv, s_li, NW, k, s_winv, s_win);
+    }
+    __syncthreads();
+    // T = the k-th best thread best; only threads reaching it re-read
+    const float tv = s_winv[k - 1];
+    const int ti = s_win[k - 1];
+    if (!before(tv, ti, bv, bi)) {
+        for (int base = lo; base < hi; base += kBatchElems) {
+            float x[kPerBatch];
+            load_batch<VEC>(row, base, hi, x);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (before(ov, oi, bv, bi)) {
-                    bv = ov;
-                    bi = oi;
+            for (int j = 0; j < kPerBatch; ++j) {
+                const int id = elem_id(base, j);
+                if (id < hi && !before(tv, ti, x[j], id)) {
+                    const int slot = atomicAdd(&s_nc, 1);
+                    if (slot < kCand) {
+                        s_cv[slot] = x[j];
+                        s_ci[slot] = id;
+                    }
                 }
-            }
-            if (lane == 0) {
-                s_win[i] = bi;
-                s_winv[i] = bv;
-            }
-            if (hx[0] == bi) {
-#pragma unroll
-                for (int j = 0; j < KMAX - 1; ++j) {
-                    hv[j] = hv[j + 1];
-                    hx[j] = hx[j + 1];
-                }
-                hv[KMAX - 1] = -INFINITY;
-                hx[KMAX - 1] = INT_MAX;
             }
         }
     }
     __syncthreads();
+    // the slice's top-k: each candidate's rank among the candidates
+    const int nc = min(s_nc, kCand);
+    if ((int)threadIdx.x >= nc && (int)threadIdx.x < k) {
+        s_winv[threadIdx.x] = -INFINITY;
+        s_win[threadIdx.x] = INT_MAX;
+    }
+    for (int c = threadIdx.x; c < nc; c += kRowThreads) {
+        const float cv = s_cv[c];
+        const int ci = s_ci[c];
+        int pos = 0;
+        for (int d = 0; d < nc; ++d) pos += before(s_cv[d], s_ci[d], cv, ci) ? 1 : 0;
+        if (pos < k) {
+            s_winv[pos] = cv;
+            s_win[pos] = ci;
+        }
+    }
+    __syncthreads();
+
+    float Mg = Mc;
+    if (P > 1) {
+        // every slice's (max, sum, top-k) into rank 0's shared memory
+        cg::cluster_group cl = cg::this_cluster();
+        cluster_wait();  // every CTA of the cluster has started
+        if (threadIdx.x == 0) {
+            *cl.map_shared_rank(&s_rm[rank], 0) = Mc;
+            *cl.map_shared_rank(&s_rz[rank], 0) = s_Z;
+        }
+        if (threadIdx.x < k) {
+            *cl.map_shared_rank(&s_rv[rank][threadIdx.x], 0) = s_winv[threadIdx.x];
+            *cl.map_shared_rank(&s_ri[rank][threadIdx.x], 0) = s_win[threadIdx.x];
+        }
+        cluster_arrive();
+        cluster_wait();
+        if (rank != 0) return;  // nothing reads this CTA's memory any more
+        Mg = -INFINITY;
+        for (int q = 0; q < P; ++q) Mg = fmaxf(Mg, s_rm[q]);
+        if (warp == 0) {
+            double t = (lane < P && s_rm[lane] != -INFINITY)
+                           ? s_rz[lane] * (double)ex2_approx((s_rm[lane] - Mg) * kLog2e)
+                           : 0.0;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            merge_lists<KMAX>(s_rv, s_ri, P, k, s_winv, s_win);
+            if (lane == 0) s_Z = t;
+        }
+        __syncthreads();
+    }
 
     // children: value = parent value * confidence
     const double Z = s_Z;
@@ -219,8 +333,7 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
         const long long slot = (long long)count[b] + (long long)r * k + i;
         if (slot < C && s_win[i] != INT_MAX) {
             const size_t o = (size_t)b * C;
-            const double conf =
-                (double)ex2_approx((s_winv[i] - Mc) * 1.4426950408889634f) / Z;
+            const double conf = (double)ex2_approx((s_winv[i] - Mg) * kLog2e) / Z;
             parent[o + slot] = f;
             depth[o + slot] = depth[o + f] + 1;
             token[o + slot] = s_win[i];
@@ -410,10 +523,26 @@ cudaError_t launch_eagle2_expand(const float *rows, int B, int R, int V, int k,
                                  int32_t *token, double *value, int32_t *count, int32_t *next,
                                  cudaStream_t stream) {
     cudaError_t e;
+    // CTAs per row: enough to fill the SMs when the rows are few (at least
+    // 4096 elements each), and enough to keep every thread within
+    // kMaxBatches batches (the bound on the candidate list)
+    const long long nrows = (long long)R * B;
+    int P = nrows >= num_sms() ? 1 : (int)(num_sms() / nrows);
+    const int p_elems = (V + 4095) / 4096;
+    if (P > p_elems) P = p_elems;
+    if (P > e2::kMaxSlices) P = e2::kMaxSlices;
+    if (P < 1) P = 1;
+    auto slice = [V](int p) { return ((V + p - 1) / p + 31) & ~31; };
+    while (P < e2::kMaxSlices && slice(P) > e2::kMaxBatches * e2::kBatchElems) ++P;
+    if (slice(P) > e2::kMaxBatches * e2::kBatchElems) return cudaErrorInvalidValue;
+    const bool vec = V % 4 == 0 && ((uintptr_t)rows & 15) == 0;
 #define SVF_E2ROWS(K_)                                                                          \
-    e = launch_pdl(eagle2_rows_kernel<K_>, dim3((unsigned)R, (unsigned)B),                        \
-                   dim3(e2::kRowThreads), 0, stream, 0u, rows, R, V, k, frontier, C, parent,      \
-                   depth, token, value, (const int32_t *)count)
+    e = vec ? launch_pdl(eagle2_rows_kernel<K_, true>, dim3((unsigned)(R * P), (unsigned)B),      \
+                         dim3(e2::kRowThreads), 0, stream, P > 1 ? (unsigned)P : 0u, rows, R, V, \
+                         k, P, frontier, C, parent, depth, token, value, (const int32_t *)count) \
+            : launch_pdl(eagle2_rows_kernel<K_, false>, dim3((unsigned)(R * P), (unsigned)B),     \
+                         dim3(e2::kRowThreads), 0, stream, P > 1 ? (unsigned)P : 0u, rows, R, V, \
+                         k, P, frontier, C, parent, depth, token, value, (const int32_t *)count)
     if (k <= 1) SVF_E2ROWS(1);
     else if (k <= 2) SVF_E2ROWS(2);
     else if (k <= 4) SVF_E2ROWS(4);

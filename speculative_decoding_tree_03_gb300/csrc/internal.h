@@ -20,6 +20,7 @@ cudaError_t launch_selftest_wait(int32_t *result, unsigned long long deadline_ns
 // EAGLE-2 tree construction (eagle2.cu).
 constexpr int kEagle2MaxK = 16;
 constexpr int kEagle2MaxPool = 2048;
+constexpr int kEagle2MaxV = 1 << 20;  // draft vocabulary of svf_eagle2_expand
 size_t eagle2_finalize_smem(int C);
 cudaError_t launch_eagle2_init(const int32_t *root_tokens, int B, int C, int32_t *parent,
                                int32_t *depth, int32_t *token, double *value, int32_t *count,

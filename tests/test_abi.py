@@ -144,6 +144,19 @@ def test_accept_variant_argument_checks(lib):
     assert onehot(u=None) == -1
 
 
+def test_eagle2_argument_checks(lib):
+    def expand(B=2, R=8, V=1000, k=8, cap=329, rows=P):
+        return lib.svf_eagle2_expand(rows, B, R, V, k, P, cap, P, P, P, P, P, P, None)
+    assert expand(B=-1) == -1
+    assert expand(B=0, rows=None) == 0
+    assert expand(rows=None) == -1
+    assert expand(k=0) == -2 and expand(k=17) == -2
+    assert expand(V=4, k=8) == -2                    # k > V
+    assert expand(V=(1 << 20) + 1) == -2             # beyond the draft vocabulary bound
+    assert expand(cap=2049) == -2
+    assert expand(R=65536) == -2
+
+
 def test_selftest_argument_checks(lib):
     assert lib.svf_selftest_wait_timeout(None, 10 ** 6, None) == -1
     assert lib.svf_selftest_wait_timeout(P, 10, None) == -1          # below 1 us

@@ -125,3 +125,76 @@ def test_eagle2_worked_tree(sv):
     assert _np(out["tokens"])[0].tolist() == [7, 0, 3, 4, 5, 6, 4]
     np.testing.assert_allclose(_np(out["values"])[0], [1.0, 0.7, 0.2, 0.42, 0.21, 0.10, 0.08],
                                rtol=1e-6)
+
+
+def _pattern_rows(rng, pattern, B, R, V):
+    """Draft rows built to stress the top-k search: the candidate bound (every
+    top value in one thread's elements), ties, and -inf logits."""
+    rows = rng.standard_normal((B, R, V)).astype(np.float32)
+    for b in range(B):
+        for r in range(R):
+            x = rows[b, r]
+            if pattern == "constant":
+                x[:] = 0.0
+            elif pattern == "levels":       # a few values, many ties
+                x[:] = rng.integers(0, 3, size=V)
+            elif pattern == "descending":
+                x[:] = np.linspace(4.0, -4.0, V, dtype=np.float32)
+            elif pattern == "one_thread":
+                # ids i0 + c + 4096 g (c, g < 4) share a thread in every
+                # slicing of the row into multiples of 32 elements, and so do
+                # the ids 16384 apart; give them the largest values
+                i0 = 4 * int(rng.integers(0, 1000)) + 32064
+                ids = [i0 + c + 4096 * g + 16384 * h for h in range(4) for g in range(4)
+                       for c in range(4)]
+                ids = [i for i in ids if i < V]
+                x[ids] = 6.0 + rng.standard_normal(len(ids)).astype(np.float32)
+            elif pattern == "few_finite":   # fewer finite logits than k
+                keep = rng.choice(V, size=5, replace=False)
+                y = np.full(V, -np.inf, np.float32)
+                y[keep] = x[keep]
+                x[:] = y
+    return rows
+
+
+@pytest.mark.parametrize("B,R", [(1, 1), (4, 8), (20, 8)])
+@pytest.mark.parametrize("pattern", ["constant", "levels", "descending", "one_thread",
+                                     "few_finite"])
+def test_eagle2_expand_patterns(sv, B, R, pattern):
+    """One expansion of R frontier rows per sequence; the rows per launch
+    decide how many CTAs share a row (8, 4 and 1 for these shapes)."""
+    V, k = 128256, 16
+    rng = np.random.default_rng(sum(map(ord, pattern)) + B)
+    cap = 1 + R + R * k
+    roots = rng.integers(0, V, size=B).astype(np.int32)
+    gpool = sv.eagle2_pool(torch.from_numpy(roots).cuda(), cap)
+    opool = oracle.eagle2_pool(roots, cap)
+    first = (2.0 * rng.standard_normal((B, 1, V))).astype(np.float32)
+    frontier0 = np.zeros((B, 1), np.int32)
+    sv.eagle2_expand(gpool, torch.from_numpy(first).cuda(), torch.from_numpy(frontier0).cuda(), R)
+    front, _ = oracle.eagle2_expand(opool, first, frontier0, R)
+    torch.cuda.synchronize()
+    for f in ("parent", "depth", "token", "value", "count"):
+        gpool[f].copy_(torch.from_numpy(opool[f]).cuda())   # start from the same pool
+    rows = _pattern_rows(rng, pattern, B, R, V)
+    gnext = sv.eagle2_expand(gpool, torch.from_numpy(rows).cuda(),
+                             torch.from_numpy(front).cuda(), k)
+    onext, gap = oracle.eagle2_expand(opool, rows, front, k)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_np(gpool["count"]), opool["count"])
+    for f in ("parent", "depth", "token"):
+        np.testing.assert_array_equal(_np(gpool[f]), opool[f], err_msg=f)
+    np.testing.assert_allclose(_np(gpool["value"]), opool["value"], rtol=VALUE_RTOL, atol=0)
+    gn = _np(gnext)
+    for b in range(B):
+        if not (gn[b] == onext[b]).all():
+            assert gap[b] < NEAR_TIE, f"sequence {b}: frontier {gn[b]} vs {onext[b]}"
+
+
+@pytest.mark.parametrize("V,k", [(1 << 20, 16), (262147, 5)])
+def test_eagle2_expand_large_vocab(sv, V, k):
+    """The largest vocabulary (eight slices of eight batches per thread) and
+    an odd one (element loads)."""
+    rng = np.random.default_rng(V)
+    gout, oout, exact = _build_both(sv, rng, 1, V, k, 2, 1 + k)
+    _compare_final(gout, oout, exact)
