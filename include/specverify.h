@@ -313,7 +313,9 @@ int svf_spec_accept_onehot(const float *target_logits, const int32_t *tokens,
  * (capped at capacity; children past it are dropped). next_frontier [B, k]
  * int32 gets the ids of the k most valuable new children (value desc, id
  * asc), -1 padded: the nodes to draft from next. V <= 1048576 (else
- * SVF_ERR_UNSUPPORTED).
+ * SVF_ERR_UNSUPPORTED). status [B] int32 (device, may be NULL) is
+ * overwritten: 0, or SVF_DEV_TIMEOUT when a wait of the row kernel gave up
+ * (that sequence's new nodes are then undefined).
  *
  * svf_eagle2_finalize: keeps the root and the n_nodes - 1 most valuable other
  * nodes (value desc, depth asc, id asc) and numbers them level by level, a
@@ -333,7 +335,8 @@ int svf_eagle2_init(const int32_t *root_tokens, int B, int capacity, int32_t *po
 int svf_eagle2_expand(const float *draft_rows, int B, int R, int V, int k,
                       const int32_t *frontier, int capacity, int32_t *pool_parent,
                       int32_t *pool_depth, int32_t *pool_token, double *pool_value,
-                      int32_t *pool_count, int32_t *next_frontier, svf_stream_t stream);
+                      int32_t *pool_count, int32_t *next_frontier, int32_t *status,
+                      svf_stream_t stream);
 int svf_eagle2_finalize(int B, int capacity, const int32_t *pool_parent,
                         const int32_t *pool_depth, const int32_t *pool_token,
                         const double *pool_value, const int32_t *pool_count, int n_nodes,

@@ -87,7 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_spec_accept_onehot.restype = I
     lib.svf_eagle2_init.argtypes = [P, I, I, P, P, P, P, P, P]
     lib.svf_eagle2_init.restype = I
-    lib.svf_eagle2_expand.argtypes = [P, I, I, I, I, P, I, P, P, P, P, P, P, P]
+    lib.svf_eagle2_expand.argtypes = [P, I, I, I, I, P, I, P, P, P, P, P, P, P, P]
     lib.svf_eagle2_expand.restype = I
     lib.svf_eagle2_finalize.argtypes = [I, I, P, P, P, P, P, I, P, P, P, P, P, P]
     lib.svf_eagle2_finalize.restype = I
@@ -371,8 +371,10 @@ def eagle2_pool(root_tokens: torch.Tensor, capacity: int, stream=None) -> dict:
 
 
 def eagle2_expand(pool: dict, draft_rows: torch.Tensor, frontier: torch.Tensor, k: int,
-                  next_frontier: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """One expansion round in place; returns the next frontier [B, k]."""
+                  next_frontier: Optional[torch.Tensor] = None,
+                  status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One expansion round in place; returns the next frontier [B, k].
+    ``status`` [B] int32, when given, gets 0 or SVF_DEV_TIMEOUT per sequence."""
     lib = load_library()
     _dev(draft_rows, "draft_rows", torch.float32)
     B, R, V = draft_rows.shape
@@ -380,10 +382,12 @@ def eagle2_expand(pool: dict, draft_rows: torch.Tensor, frontier: torch.Tensor, 
     C = pool["parent"].shape[1]
     if next_frontier is None:
         next_frontier = torch.empty((B, k), dtype=torch.int32, device=draft_rows.device)
+    if status is not None:
+        _dev(status, "status", torch.int32, (B,))
     rc = lib.svf_eagle2_expand(_ptr(draft_rows), B, R, V, k, _ptr(frontier), C,
                                _ptr(pool["parent"]), _ptr(pool["depth"]), _ptr(pool["token"]),
                                _ptr(pool["value"]), _ptr(pool["count"]), _ptr(next_frontier),
-                               _stream(stream))
+                               None if status is None else _ptr(status), _stream(stream))
     _check(rc, "svf_eagle2_expand")
     return next_frontier
 

@@ -217,7 +217,8 @@ int svf_eagle2_init(const int32_t *root_tokens, int B, int capacity, int32_t *po
 int svf_eagle2_expand(const float *draft_rows, int B, int R, int V, int k,
                       const int32_t *frontier, int capacity, int32_t *pool_parent,
                       int32_t *pool_depth, int32_t *pool_token, double *pool_value,
-                      int32_t *pool_count, int32_t *next_frontier, svf_stream_t stream) {
+                      int32_t *pool_count, int32_t *next_frontier, int32_t *status,
+                      svf_stream_t stream) {
     if (B < 0 || R < 0 || V < 0 || k < 0 || capacity < 1) return SVF_ERR_ARG;
     if (B == 0) return SVF_OK;
     if (!draft_rows || !frontier || !pool_parent || !pool_depth || !pool_token || !pool_value ||
@@ -228,7 +229,8 @@ int svf_eagle2_expand(const float *draft_rows, int B, int R, int V, int k,
         return SVF_ERR_UNSUPPORTED;
     cudaError_t e = launch_eagle2_expand(draft_rows, B, R, V, k, frontier, capacity, pool_parent,
                                          pool_depth, pool_token, pool_value, pool_count,
-                                         next_frontier, reinterpret_cast<cudaStream_t>(stream));
+                                         next_frontier, status,
+                                         reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 

@@ -34,7 +34,7 @@ namespace svf {
 
 namespace e2 {
 
-constexpr int kRowThreads = 1024;
+constexpr int kRowThreads = 512;
 constexpr int kSelThreads = 256;
 constexpr int kFinThreads = 512;
 constexpr int kMaxSlices = 8;          // CTAs per row (a portable cluster)
@@ -63,28 +63,35 @@ __global__ void eagle2_init_kernel(const int32_t *__restrict__ root_tokens, int 
 }
 
 // One cluster of P CTAs per (frontier row r, sequence b), each CTA over a
-// contiguous slice of the row. A CTA reads its slice once: every thread keeps
-// a running (max, sum e^(l - max)) and its own best (logit, id). The k-th best
-// of the CTA's thread bests, T, bounds the slice's top-k from below, and only
-// the (at most k) threads whose best reaches T can hold a top-k element: they
-// re-read their elements (from cache) and post those that reach T, at most
-// k * 128 of them, for an exact rank. Rank 0 of the cluster merges the slices'
-// statistics and top-k lists (sent into its shared memory) and writes the
-// children: child i of frontier node f gets pool slot count[b] + r k + i.
+// contiguous slice of the row. A CTA streams its slice once through a ring of
+// shared-memory stages filled by bulk copies (element loads when the rows are
+// not 16-byte aligned): every thread keeps a running (max, sum e^(l - max))
+// and its own best (logit, id). The k-th best of the CTA's thread bests, T,
+// bounds the slice's top-k from below, and only the (at most k) threads whose
+// best reaches T can hold a top-k element: they re-read their elements (from
+// cache) and post those that reach T into the freed stage memory, for an
+// exact rank. Rank 0 of the cluster merges the slices' statistics and top-k
+// lists (sent into its shared memory) and writes the children: child i of
+// frontier node f gets pool slot count[b] + r k + i. A stage wait that gives
+// up marks the row's child slots with token kTimeoutToken.
 namespace e2 {
 
-constexpr int kGroups = 4;                         // float4 groups per thread per batch
-constexpr int kPerBatch = 4 * kGroups;             // elements per thread per batch
-constexpr int kBatchElems = kRowThreads * kPerBatch;
-constexpr int kMaxBatches = 8;                     // batches per slice (the candidate bound)
+constexpr int kGroups = 4;                          // float4 groups per thread per batch
+constexpr int kPerBatch = 4 * kGroups;              // elements per thread per batch
+constexpr int kBatchElems = kRowThreads * kPerBatch;  // one stage: 32 KB
+constexpr int kStages = 3;
+constexpr size_t kRowSmem = (size_t)kStages * kBatchElems * sizeof(float);
+constexpr int kCandCap = (int)(kRowSmem / 8);       // (logit, id) pairs in the stages
+constexpr int kMaxBatches = 48;                     // KMAX * 16 * kMaxBatches <= kCandCap
+constexpr int kTimeoutToken = -2;
 
 // element j of a thread's batch at `base`: group j / 4, lane j % 4
 __device__ __forceinline__ int elem_id(int base, int j) {
     return base + ((j >> 2) * kRowThreads + (int)threadIdx.x) * 4 + (j & 3);
 }
 
-// A thread's 16 elements of the batch at `base`; -inf past `hi`. VEC: 16-byte
-// loads (the row start and `hi` are multiples of 4 elements).
+// A thread's 16 elements of the batch at `base` from global memory; -inf past
+// `hi`. VEC: 16-byte loads (the row start and `hi` are multiples of 4).
 template <bool VEC>
 __device__ __forceinline__ void load_batch(const float *__restrict__ row, int base, int hi,
                                            float (&x)[kPerBatch]) {
@@ -105,19 +112,37 @@ __device__ __forceinline__ void load_batch(const float *__restrict__ row, int ba
     }
 }
 
-// k-way merge of n sorted lists (best first, k entries each) by warp 0: lane
-// q follows list q. Writes the k best (id INT_MAX past the real entries).
+// The same 16 elements from a stage holding the batch at `base`.
+__device__ __forceinline__ void load_stage(const float *st, int base, int hi,
+                                           float (&x)[kPerBatch]) {
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+        const int off = (g * kRowThreads + (int)threadIdx.x) * 4;
+        float4 t = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (base + off < hi) t = *reinterpret_cast<const float4 *>(st + off);
+        x[4 * g] = t.x;
+        x[4 * g + 1] = t.y;
+        x[4 * g + 2] = t.z;
+        x[4 * g + 3] = t.w;
+    }
+}
+
+// The k best of n <= 32 sorted lists (best first, k entries each, ids
+// distinct except INT_MAX fillers), by one warp: lane q holds the head of
+// list q, and each round the best head (a shuffle reduction) is taken and
+// its list advances. Lane 0 writes the k entries, best first.
 template <int KMAX>
-__device__ __forceinline__ void merge_lists(const float (*lv)[KMAX], const int (*li)[KMAX],
-                                            int n, int k, float *outv, int *outi) {
+__device__ __forceinline__ void merge_lists(const float (*lv)[KMAX], const int (*li)[KMAX], int n,
+                                            int k, float *outv, int *outi) {
     const int lane = threadIdx.x & 31;
     int h = 0;
+    float hv = lane < n ? lv[lane][0] : -INFINITY;
+    int hx = lane < n ? li[lane][0] : INT_MAX;
+    const int o0 = n > 16 ? 16 : n > 8 ? 8 : n > 4 ? 4 : n > 2 ? 2 : 1;
     for (int i = 0; i < k; ++i) {
-        float bv = (lane < n && h < k) ? lv[lane][h] : -INFINITY;
-        int bi = (lane < n && h < k) ? li[lane][h] : INT_MAX;
-        const int mine = bi;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
+        float bv = hv;
+        int bi = hx;
+        for (int o = o0; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
             const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
             if (before(ov, oi, bv, bi)) {
@@ -129,29 +154,35 @@ __device__ __forceinline__ void merge_lists(const float (*lv)[KMAX], const int (
             outv[i] = bv;
             outi[i] = bi;
         }
-        if (mine == bi && bi != INT_MAX) ++h;
+        if (hx == bi && bi != INT_MAX && lane < n) {
+            ++h;
+            hv = h < k ? lv[lane][h] : -INFINITY;
+            hx = h < k ? li[lane][h] : INT_MAX;
+        }
     }
 }
 
 }  // namespace e2
 
-template <int KMAX, bool VEC>  // KMAX >= k
-__global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
+template <int KMAX, bool VEC>  // KMAX >= k; VEC: bulk copies of 16-byte aligned rows
+__global__ void __launch_bounds__(e2::kRowThreads, 2) eagle2_rows_kernel(
     const float *__restrict__ rows, int R, int V, int k, int P,
     const int32_t *__restrict__ frontier, int C, int32_t *__restrict__ parent,
     int32_t *__restrict__ depth, int32_t *__restrict__ token, double *__restrict__ value,
     const int32_t *__restrict__ count) {
     using namespace e2;
     constexpr int NW = kRowThreads / 32;
-    constexpr int kCand = KMAX * kMaxBatches * kPerBatch;  // k threads x their elements
-    static_assert(NW == 32, "one lane of warp 0 per warp");
-    const int r = blockIdx.x / P, rank = blockIdx.x % P, b = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // this CTA's slice of the row, a multiple of 32 elements wide
-    const int per = ((V + P - 1) / P + 31) & ~31;
-    const int lo = rank * per, hi = min(V, lo + per);
+    static_assert(NW <= 32 && NW * KMAX <= kRowThreads, "one lane of warp 0 per warp");
+    static_assert(KMAX * kPerBatch * kMaxBatches <= kCandCap, "candidate bound");
+    extern __shared__ __align__(128) unsigned char e2_dyn[];
+    float *stage = reinterpret_cast<float *>(e2_dyn);              // [kStages][kBatchElems]
+    float *s_cv = reinterpret_cast<float *>(e2_dyn);               // candidates, afterwards
+    int *s_ci = reinterpret_cast<int *>(e2_dyn + (size_t)kCandCap * sizeof(float));
+    __shared__ __align__(8) uint64_t s_full[kStages];
+    __shared__ int s_abort;
     __shared__ float s_rm[kMaxSlices];            // rank 0: the slices' maxima
     __shared__ double s_rz[kMaxSlices];           //   their sums
+    __shared__ int s_rbad[kMaxSlices];            //   their wait failures
     __shared__ float s_rv[kMaxSlices][KMAX];      //   their top-k lists
     __shared__ int s_ri[kMaxSlices][KMAX];
     __shared__ float s_m[NW];
@@ -161,9 +192,15 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     __shared__ int s_li[NW][KMAX];
     __shared__ float s_winv[KMAX];
     __shared__ int s_win[KMAX];
-    __shared__ float s_cv[kCand];                 // candidates reaching T
-    __shared__ int s_ci[kCand];
     __shared__ int s_nc;
+    __shared__ int s_nsel;
+    __shared__ int s_sel[kRowThreads];            // threads holding candidates
+    const int r = blockIdx.x / P, rank = blockIdx.x % P, b = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // this CTA's slice of the row, a multiple of 32 elements wide
+    const int per = ((V + P - 1) / P + 31) & ~31;
+    const int lo = rank * per, hi = min(V, lo + per);
+    const int nb = hi > lo ? (hi - lo + kBatchElems - 1) / kBatchElems : 0;
     pdl_wait();
     pdl_launch_dependents();
     if (P > 1) cluster_arrive();  // waited on before the first remote store
@@ -171,14 +208,49 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     if (f < 0 || f >= min(count[b], C)) return;  // an unused frontier slot
     const float *row = rows + ((size_t)b * R + r) * (size_t)V;
     constexpr float kLog2e = 1.4426950408889634f;
+    // the parent's value and depth, read early (its slot is older than count)
+    const size_t po = (size_t)b * C;
+    const double vf = (rank == 0 && threadIdx.x < k) ? value[po + f] : 0.0;
+    const int df = (rank == 0 && threadIdx.x < k) ? depth[po + f] : 0;
+
+    auto issue = [&](int c) {  // batch c of the slice into stage c % kStages
+        const int start = lo + c * kBatchElems;
+        const uint32_t bytes = (uint32_t)min(kBatchElems, hi - start) * 4u;
+        uint64_t *bar = &s_full[c % kStages];
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load_smem(stage + (size_t)(c % kStages) * kBatchElems, row + start, bytes, bar);
+    };
+    if (VEC && threadIdx.x == 0) {
+        s_abort = 0;
+        for (int s = 0; s < kStages; ++s) mbar_init(&s_full[s], 1);
+        mbar_fence_init();
+        for (int c = 0; c < min(kStages, nb); ++c) issue(c);
+    }
+    __syncthreads();
 
     // the one pass over the slice
     float m = -INFINITY, z = 0.0f;
     float bv = -INFINITY;
     int bi = INT_MAX;
-    for (int base = lo; base < hi; base += kBatchElems) {
+    bool bad = false;  // a stage wait gave up (the same in every thread)
+    int c = 0;
+    for (; c < nb; ++c) {
+        const int base = lo + c * kBatchElems;
         float x[kPerBatch];
-        load_batch<VEC>(row, base, hi, x);
+        if (VEC) {
+            if (mbar_wait(&s_full[c % kStages], (uint32_t)(c / kStages) & 1u, &s_abort))
+                load_stage(stage + (size_t)(c % kStages) * kBatchElems, base, hi, x);
+            else
+                bad = true;
+            // every thread is done with this stage: refill it
+            if (__syncthreads_or(bad)) {
+                bad = true;
+                break;
+            }
+            if (threadIdx.x == 0 && c + kStages < nb) issue(c + kStages);
+        } else {
+            load_batch<false>(row, base, hi, x);
+        }
         float bm = fmax3(x[0], x[1], x[2]);
 #pragma unroll
         for (int j = 3; j + 1 < kPerBatch; j += 2) bm = fmax3(bm, x[j], x[j + 1]);
@@ -205,6 +277,13 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
             }
         }
     }
+    if (VEC && bad && threadIdx.x == 0) {
+        // let the copies still in flight land before the memory is reused
+        s_abort = 0;
+        for (int d = c; d < min(c + kStages, nb); ++d)
+            mbar_wait_for(&s_full[d % kStages], (uint32_t)(d / kStages) & 1u, &s_abort,
+                          kWaitDeadlineNs);
+    }
 
     // softmax statistics of the slice: (max, sum) over the warp and the CTA
     float M = m;
@@ -222,7 +301,7 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, sv, stride);
             const int oi = __shfl_xor_sync(0xffffffffu, si, stride);
-            const bool best_first = (lane & size) == 0 || size == 32;
+            const bool best_first = (lane & size) == 0;
             const bool low = (lane & stride) == 0;
             const bool take = (best_first == low) ? before(ov, oi, sv, si) : before(sv, si, ov, oi);
             if (take) {
@@ -239,39 +318,58 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
         s_lv[warp][lane] = sv;
         s_li[warp][lane] = si;
     }
+    if (threadIdx.x < k) {
+        s_winv[threadIdx.x] = -INFINITY;
+        s_win[threadIdx.x] = INT_MAX;
+    }
+    if (threadIdx.x == 0) s_nc = 0;
     __syncthreads();
     float Mc = -INFINITY;
     for (int w = 0; w < NW; ++w) Mc = fmaxf(Mc, s_m[w]);
     if (warp == 0) {
+        // T: the k-th best of the thread bests
+        merge_lists<KMAX>(s_lv, s_li, NW, k, s_winv, s_win);
+        if (lane == 0) s_nsel = 0;
+    } else if (warp == 1) {
         // the slice's normaliser: one lane per warp, fp32 exponentials and an
         // fp64 sum (this part's fp64 pipe is slow, so no fp64 exp)
-        double t = s_m[lane] == -INFINITY
-                       ? 0.0
-                       : s_z[lane] * (double)ex2_approx((s_m[lane] - Mc) * kLog2e);
+        double t = (lane < NW && s_m[lane] != -INFINITY)
+                       ? s_z[lane] * (double)ex2_approx((s_m[lane] - Mc) * kLog2e)
+                       : 0.0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0) {
-            s_Z = t;
-            s_nc = 0;
-        }
-        merge_lists<KMAX>(s_lv, s_li, NW, k, s_winv, s_win);
+        if (lane == 0) s_Z = t;
     }
     __syncthreads();
-    // T = the k-th best thread best; only threads reaching it re-read
     const float tv = s_winv[k - 1];
     const int ti = s_win[k - 1];
-    if (!before(tv, ti, bv, bi)) {
-        for (int base = lo; base < hi; base += kBatchElems) {
-            float x[kPerBatch];
-            load_batch<VEC>(row, base, hi, x);
+    // only the threads whose best reaches T hold candidates; a warp re-reads
+    // each such thread's elements (from cache), eight loads per lane at a time
+    if (!bad && !before(tv, ti, bv, bi)) s_sel[atomicAdd(&s_nsel, 1)] = (int)threadIdx.x;
+    __syncthreads();
+    const int nsel = s_nsel;
+    const int nel = nb * kPerBatch;  // elements per thread
+    for (int q = warp; q < nsel; q += NW) {
+        const int t = s_sel[q];
+        for (int j0 = 0; j0 < nel; j0 += 8 * 32) {
+            float xv[8];
+            int xi[8];
 #pragma unroll
-            for (int j = 0; j < kPerBatch; ++j) {
-                const int id = elem_id(base, j);
-                if (id < hi && !before(tv, ti, x[j], id)) {
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u * 32 + lane;  // element j: batch j / 16, slot j % 16
+                const int jj = j % kPerBatch;
+                xi[u] = lo + (j / kPerBatch) * kBatchElems +
+                        ((jj >> 2) * kRowThreads + t) * 4 + (jj & 3);
+                xv[u] = (j < nel && xi[u] < hi) ? __ldg(row + xi[u]) : -INFINITY;
+                if (j >= nel) xi[u] = INT_MAX;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (xi[u] < hi && !before(tv, ti, xv[u], xi[u])) {
                     const int slot = atomicAdd(&s_nc, 1);
-                    if (slot < kCand) {
-                        s_cv[slot] = x[j];
-                        s_ci[slot] = id;
+                    if (slot < kCandCap) {
+                        s_cv[slot] = xv[u];
+                        s_ci[slot] = xi[u];
                     }
                 }
             }
@@ -279,14 +377,14 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     }
     __syncthreads();
     // the slice's top-k: each candidate's rank among the candidates
-    const int nc = min(s_nc, kCand);
+    const int nc = min(s_nc, kCandCap);
     if ((int)threadIdx.x >= nc && (int)threadIdx.x < k) {
         s_winv[threadIdx.x] = -INFINITY;
         s_win[threadIdx.x] = INT_MAX;
     }
-    for (int c = threadIdx.x; c < nc; c += kRowThreads) {
-        const float cv = s_cv[c];
-        const int ci = s_ci[c];
+    for (int e = threadIdx.x; e < nc; e += kRowThreads) {
+        const float cv = s_cv[e];
+        const int ci = s_ci[e];
         int pos = 0;
         for (int d = 0; d < nc; ++d) pos += before(s_cv[d], s_ci[d], cv, ci) ? 1 : 0;
         if (pos < k) {
@@ -297,13 +395,15 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     __syncthreads();
 
     float Mg = Mc;
+    bool any_bad = bad;
     if (P > 1) {
-        // every slice's (max, sum, top-k) into rank 0's shared memory
+        // every slice's (max, sum, failure, top-k) into rank 0's shared memory
         cg::cluster_group cl = cg::this_cluster();
         cluster_wait();  // every CTA of the cluster has started
         if (threadIdx.x == 0) {
             *cl.map_shared_rank(&s_rm[rank], 0) = Mc;
             *cl.map_shared_rank(&s_rz[rank], 0) = s_Z;
+            *cl.map_shared_rank(&s_rbad[rank], 0) = bad ? 1 : 0;
         }
         if (threadIdx.x < k) {
             *cl.map_shared_rank(&s_rv[rank][threadIdx.x], 0) = s_winv[threadIdx.x];
@@ -313,14 +413,18 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
         cluster_wait();
         if (rank != 0) return;  // nothing reads this CTA's memory any more
         Mg = -INFINITY;
-        for (int q = 0; q < P; ++q) Mg = fmaxf(Mg, s_rm[q]);
+        for (int q = 0; q < P; ++q) {
+            Mg = fmaxf(Mg, s_rm[q]);
+            any_bad = any_bad || s_rbad[q] != 0;
+        }
         if (warp == 0) {
+            merge_lists<KMAX>(s_rv, s_ri, P, k, s_winv, s_win);
+        } else if (warp == 1) {
             double t = (lane < P && s_rm[lane] != -INFINITY)
                            ? s_rz[lane] * (double)ex2_approx((s_rm[lane] - Mg) * kLog2e)
                            : 0.0;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-            merge_lists<KMAX>(s_rv, s_ri, P, k, s_winv, s_win);
             if (lane == 0) s_Z = t;
         }
         __syncthreads();
@@ -331,22 +435,25 @@ __global__ void __launch_bounds__(e2::kRowThreads) eagle2_rows_kernel(
     if (threadIdx.x < k) {
         const int i = threadIdx.x;
         const long long slot = (long long)count[b] + (long long)r * k + i;
-        if (slot < C && s_win[i] != INT_MAX) {
-            const size_t o = (size_t)b * C;
+        if (slot < C && any_bad) {
+            token[po + slot] = kTimeoutToken;
+        } else if (slot < C && s_win[i] != INT_MAX) {
             const double conf = (double)ex2_approx((s_winv[i] - Mg) * kLog2e) / Z;
-            parent[o + slot] = f;
-            depth[o + slot] = depth[o + f] + 1;
-            token[o + slot] = s_win[i];
-            value[o + slot] = value[o + f] * conf;
+            parent[po + slot] = f;
+            depth[po + slot] = df + 1;
+            token[po + slot] = s_win[i];
+            value[po + slot] = vf * conf;
         }
     }
 }
 
 // The next frontier: the k best of this round's new nodes by (value desc,
-// id asc), -1 padded; then the pool count moves past them.
+// id asc), -1 padded; then the pool count moves past them. status[b] (when
+// given) reports a row of this round whose stage wait gave up.
 __global__ void __launch_bounds__(e2::kSelThreads) eagle2_select_kernel(
     int R, int k, const int32_t *__restrict__ frontier, int C, const double *__restrict__ value,
-    int32_t *__restrict__ count, int32_t *__restrict__ next) {
+    const int32_t *__restrict__ token, int32_t *__restrict__ count, int32_t *__restrict__ next,
+    int32_t *__restrict__ status) {
     const int b = blockIdx.x;
     __shared__ int s_valid;
     pdl_wait();
@@ -374,8 +481,14 @@ __global__ void __launch_bounds__(e2::kSelThreads) eagle2_select_kernel(
         }
         if (rank < k) next[(size_t)b * k + rank] = c;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) count[b] = last;
+    int timed_out = 0;
+    for (int c = first + (int)threadIdx.x; c < last; c += blockDim.x)
+        timed_out |= token[(size_t)b * C + c] == e2::kTimeoutToken ? 1 : 0;
+    timed_out = __syncthreads_or(timed_out);
+    if (threadIdx.x == 0) {
+        count[b] = last;
+        if (status) status[b] = timed_out ? SVF_DEV_TIMEOUT : 0;
+    }
 }
 
 // Rerank and BFS numbering of one sequence's pool.
@@ -521,14 +634,15 @@ cudaError_t launch_eagle2_init(const int32_t *root_tokens, int B, int C, int32_t
 cudaError_t launch_eagle2_expand(const float *rows, int B, int R, int V, int k,
                                  const int32_t *frontier, int C, int32_t *parent, int32_t *depth,
                                  int32_t *token, double *value, int32_t *count, int32_t *next,
-                                 cudaStream_t stream) {
+                                 int32_t *status, cudaStream_t stream) {
     cudaError_t e;
-    // CTAs per row: enough to fill the SMs when the rows are few (at least
-    // 4096 elements each), and enough to keep every thread within
+    // CTAs per row: enough to fill the SMs (two CTAs each) when the rows are
+    // few, at least one batch each, and enough to keep every thread within
     // kMaxBatches batches (the bound on the candidate list)
     const long long nrows = (long long)R * B;
-    int P = nrows >= num_sms() ? 1 : (int)(num_sms() / nrows);
-    const int p_elems = (V + 4095) / 4096;
+    const long long slots = 2ll * num_sms();
+    int P = nrows >= slots ? 1 : (int)(slots / nrows);
+    const int p_elems = (V + e2::kBatchElems - 1) / e2::kBatchElems;
     if (P > p_elems) P = p_elems;
     if (P > e2::kMaxSlices) P = e2::kMaxSlices;
     if (P < 1) P = 1;
@@ -537,12 +651,15 @@ cudaError_t launch_eagle2_expand(const float *rows, int B, int R, int V, int k,
     if (slice(P) > e2::kMaxBatches * e2::kBatchElems) return cudaErrorInvalidValue;
     const bool vec = V % 4 == 0 && ((uintptr_t)rows & 15) == 0;
 #define SVF_E2ROWS(K_)                                                                          \
-    e = vec ? launch_pdl(eagle2_rows_kernel<K_, true>, dim3((unsigned)(R * P), (unsigned)B),      \
-                         dim3(e2::kRowThreads), 0, stream, P > 1 ? (unsigned)P : 0u, rows, R, V, \
-                         k, P, frontier, C, parent, depth, token, value, (const int32_t *)count) \
-            : launch_pdl(eagle2_rows_kernel<K_, false>, dim3((unsigned)(R * P), (unsigned)B),     \
-                         dim3(e2::kRowThreads), 0, stream, P > 1 ? (unsigned)P : 0u, rows, R, V, \
-                         k, P, frontier, C, parent, depth, token, value, (const int32_t *)count)
+    do {                                                                                        \
+        auto kern = vec ? eagle2_rows_kernel<K_, true> : eagle2_rows_kernel<K_, false>;         \
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,             \
+                                 (int)e2::kRowSmem);                                            \
+        if (e != cudaSuccess) return e;                                                         \
+        e = launch_pdl(kern, dim3((unsigned)(R * P), (unsigned)B), dim3(e2::kRowThreads),       \
+                       e2::kRowSmem, stream, P > 1 ? (unsigned)P : 0u, rows, R, V, k, P,       \
+                       frontier, C, parent, depth, token, value, (const int32_t *)count);       \
+    } while (0)
     if (k <= 1) SVF_E2ROWS(1);
     else if (k <= 2) SVF_E2ROWS(2);
     else if (k <= 4) SVF_E2ROWS(4);
@@ -551,7 +668,8 @@ cudaError_t launch_eagle2_expand(const float *rows, int B, int R, int V, int k,
 #undef SVF_E2ROWS
     if (e != cudaSuccess) return e;
     return launch_pdl(eagle2_select_kernel, dim3((unsigned)B), dim3(e2::kSelThreads), 0, stream,
-                      0u, R, k, frontier, C, (const double *)value, count, next);
+                      0u, R, k, frontier, C, (const double *)value, (const int32_t *)token, count,
+                      next, status);
 }
 
 cudaError_t launch_eagle2_finalize(int B, int C, const int32_t *parent, const int32_t *depth,

@@ -28,7 +28,7 @@ cudaError_t launch_eagle2_init(const int32_t *root_tokens, int B, int C, int32_t
 cudaError_t launch_eagle2_expand(const float *rows, int B, int R, int V, int k,
                                  const int32_t *frontier, int C, int32_t *parent, int32_t *depth,
                                  int32_t *token, double *value, int32_t *count, int32_t *next,
-                                 cudaStream_t stream);
+                                 int32_t *status, cudaStream_t stream);
 cudaError_t launch_eagle2_finalize(int B, int C, const int32_t *parent, const int32_t *depth,
                                    const int32_t *token, const double *value,
                                    const int32_t *count, int n_nodes, int32_t *out_parent,

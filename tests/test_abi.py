@@ -146,7 +146,7 @@ def test_accept_variant_argument_checks(lib):
 
 def test_eagle2_argument_checks(lib):
     def expand(B=2, R=8, V=1000, k=8, cap=329, rows=P):
-        return lib.svf_eagle2_expand(rows, B, R, V, k, P, cap, P, P, P, P, P, P, None)
+        return lib.svf_eagle2_expand(rows, B, R, V, k, P, cap, P, P, P, P, P, P, None, None)
     assert expand(B=-1) == -1
     assert expand(B=0, rows=None) == 0
     assert expand(rows=None) == -1

@@ -39,10 +39,12 @@ def _build_both(sv, rng, B, V, k, rounds, N, capacity=None, sigma=2.0):
     for _ in range(rounds):
         R = frontier.shape[1]
         rows = (sigma * rng.standard_normal((B, R, V))).astype(np.float32)
+        status = torch.full((B,), -1, dtype=torch.int32).cuda()
         gnext = sv.eagle2_expand(gpool, torch.from_numpy(rows).cuda(),
-                                 torch.from_numpy(frontier).cuda(), k)
+                                 torch.from_numpy(frontier).cuda(), k, status=status)
         onext, gap = oracle.eagle2_expand(opool, rows, frontier, k)
         torch.cuda.synchronize()
+        assert (_np(status) == 0).all()
         gn = _np(gnext)
         np.testing.assert_array_equal(_np(gpool["count"]), opool["count"])
         for b in range(B):
