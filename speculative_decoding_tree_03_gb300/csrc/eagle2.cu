@@ -506,11 +506,11 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
     int *sd = reinterpret_cast<int *>(kv + C);         // [C] depth
     int *sp = sd + C;                                  // [C] parent id
     int *sidx = sp + C;                                // [C] new index, -1 if not kept
-    int *snew = sidx + C;                              // [C] new index being computed
-    int *skept = snew + C;                             // [C] kept nodes by rerank rank
+    int *lcnt = sidx + C;                              // [C] kept nodes per depth
+    int *skept = lcnt + C;                             // [C] kept nodes by rerank rank
     int *kd = skept + C;                               // [C] depth of kept node j
     int *kpn = kd + C;                                 // [C] its parent's new index
-    __shared__ int s_kept, s_maxd, s_at, s_lvl;
+    __shared__ int s_kept, s_maxd;
     const int b = blockIdx.x;
     pdl_wait();
     pdl_launch_dependents();
@@ -519,15 +519,19 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
     if (threadIdx.x == 0) {
         s_kept = 0;
         s_maxd = 0;
-        s_lvl = 0;
     }
+    // a slot that is not a node gets key 0 and depth INT_MAX: it never ranks
+    // ahead of a node, so the rank loops need no branch
     for (int c = threadIdx.x; c < cnt; c += blockDim.x) {
         const int pc = pparent[o + c];
-        const bool ok = c == 0 || (pc >= 0 && pc < c);  // parents precede children
+        const int dc = pdepth[o + c];
+        // parents precede children, so a depth is at most the node's id
+        const bool ok = c == 0 || (pc >= 0 && pc < c && dc >= 1 && dc <= c);
         sv[c] = ok ? (unsigned long long)__double_as_longlong(pvalue[o + c]) : 0ull;
-        sd[c] = ok ? pdepth[o + c] : -1;
+        sd[c] = ok ? dc : INT_MAX;
         sp[c] = ok ? pc : 0;
         sidx[c] = -1;
+        lcnt[c] = 0;
     }
     for (int i = threadIdx.x; i < n_nodes; i += blockDim.x) {
         out_parent[(size_t)b * n_nodes + i] = -1;
@@ -540,31 +544,31 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
     for (int c = 1 + (int)threadIdx.x; c < cnt; c += blockDim.x) {
         const unsigned long long vc = sv[c];
         const int dc = sd[c];
-        if (dc < 1) continue;  // not a node of the tree
+        if (dc < 1 || dc == INT_MAX) continue;  // not a node of the tree
         int rank = 0;
+#pragma unroll 8
         for (int d = 1; d < cnt; ++d) {
             const unsigned long long vd = sv[d];
-            if (sd[d] < 1) continue;
-            rank += (vd > vc || (vd == vc && (sd[d] < dc || (sd[d] == dc && d < c)))) ? 1 : 0;
+            const int dd = sd[d];
+            rank += (int)((vd > vc) | ((vd == vc) & ((dd < dc) | ((dd == dc) & (d < c)))));
         }
         if (rank < n_nodes - 1) {
             sidx[c] = -2;  // kept, not yet numbered
             skept[rank] = c;
             atomicAdd(&s_kept, 1);
+            atomicAdd(&lcnt[dc], 1);
             atomicMax(&s_maxd, dc);
         }
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        sidx[0] = 0;
-        s_at = 1;
-    }
+    if (threadIdx.x == 0) sidx[0] = 0;
     __syncthreads();
     // BFS numbering, a level at a time: (parent's new index, value desc, id
-    // asc); the ranks of a level are all computed before any is published
-    // Only the kept nodes are scanned, from flat per-node copies (independent
-    // loads in the inner loop): skept[j] lists them by rerank rank, kd/kv hold
-    // their depth and key, kpn the parent's new index for the current level.
+    // asc). Only the kept nodes are scanned, from flat copies: skept[j] lists
+    // them by rerank rank, kd/kv hold their depth and key, kpn the parent's
+    // new index for the current level (INT_MAX off the level, so that those
+    // never rank ahead). A level's new indices start after all shallower
+    // kept nodes (lcnt), and the level is numbered in one pass that reads no
+    // index it writes.
     const int nk = s_kept;
     for (int j = threadIdx.x; j < nk; j += blockDim.x) {
         const int c = skept[j];
@@ -572,36 +576,26 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
         kv[j] = sv[c];
     }
     __syncthreads();
+    int base = 1;
     for (int d = 1; d <= s_maxd; ++d) {
-        const int base = s_at;
         for (int j = threadIdx.x; j < nk; j += blockDim.x)
-            kpn[j] = kd[j] == d ? sidx[sp[skept[j]]] : -1;
+            kpn[j] = kd[j] == d ? sidx[sp[skept[j]]] : INT_MAX;
         __syncthreads();
         for (int j = threadIdx.x; j < nk; j += blockDim.x) {
-            if (kd[j] != d) continue;
-            const int pc = kpn[j], c = skept[j];
+            const int pc = kpn[j];
+            if (pc == INT_MAX) continue;
+            const int c = skept[j];
             const unsigned long long vc = kv[j];
             int rank = 0;
+#pragma unroll 4
             for (int q = 0; q < nk; ++q) {
-                if (kd[q] != d) continue;
                 const int pe = kpn[q];
                 const unsigned long long ve = kv[q];
-                rank += (pe < pc || (pe == pc && (ve > vc || (ve == vc && skept[q] < c)))) ? 1 : 0;
+                rank += (int)((pe < pc) | ((pe == pc) & ((ve > vc) | ((ve == vc) & (skept[q] < c)))));
             }
-            snew[j] = base + rank;
+            sidx[c] = base + rank;
         }
-        __syncthreads();
-        for (int j = threadIdx.x; j < nk; j += blockDim.x) {
-            if (kd[j] == d) {
-                sidx[skept[j]] = snew[j];
-                atomicAdd(&s_lvl, 1);
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            s_at += s_lvl;
-            s_lvl = 0;
-        }
+        base += lcnt[d];
         __syncthreads();
     }
     // outputs
@@ -614,7 +608,7 @@ __global__ void __launch_bounds__(e2::kFinThreads) eagle2_finalize_kernel(
         out_value[q] = pvalue[o + c];
         out_cid[q] = c;
     }
-    if (threadIdx.x == 0) n_out[b] = s_at;
+    if (threadIdx.x == 0) n_out[b] = 1 + nk;
 }
 
 // ---------------------------------------------------------------- host side
