@@ -460,10 +460,22 @@ def run_ours(args, w, idx):
         sv.spec_accept(bf_logits["target"], bf_logits["draft"], s["tokens"], s["parent"],
                        s["u_accept"], s["u_bonus"], outputs=var_out["bf16"])
 
+    var_out["greedy_bf16"] = {}
+    var_out["onehot_bf16"] = {}
+
+    def greedy_bf16_call(s):
+        sv.spec_accept_greedy(bf_logits["target"], s["tokens"], s["parent"],
+                              outputs=var_out["greedy_bf16"])
+
+    def onehot_bf16_call(s):
+        sv.spec_accept_onehot(bf_logits["target"], s["tokens"], s["parent"], s["u_accept"],
+                              s["u_bonus"], outputs=var_out["onehot_bf16"])
+
     e2out = {}
     var_ms = {}
     for name, fn in (("greedy", greedy_call), ("onehot", onehot_call), ("eagle2", eagle2_call),
-                     ("bf16", bf16_call)):
+                     ("bf16", bf16_call), ("greedy_bf16", greedy_bf16_call),
+                     ("onehot_bf16", onehot_bf16_call)):
         fn(sets[0])
         barrier()
         graphs = [capture(fn, s) for s in sets]
@@ -592,10 +604,10 @@ def run_ours(args, w, idx):
         "ms": var_ms["bf16"], "bytes": bfb, "gbs": bfb / (var_ms["bf16"] / 1e3) / 1e9,
         "frac_of_hbm": bfb / (var_ms["bf16"] / 1e3) / 1e9 / peak,
         "bytes_note": "bf16 rows of the visited nodes (the logits rounded to bf16)"}
-    for name in ("greedy", "onehot"):
+    for name in ("greedy", "onehot", "greedy_bf16", "onehot_bf16"):
         vp = var_out[name]["path"].cpu().numpy()
         vl = var_out[name]["accept_len"].cpu().numpy()
-        vb = sum(int(vl[b]) + 1 for b in range(B)) * w.V * 4
+        vb = sum(int(vl[b]) + 1 for b in range(B)) * w.V * (2 if name.endswith("bf16") else 4)
         var_kernels["spec_accept_" + name] = {
             "ms": var_ms[name], "bytes": vb, "gbs": vb / (var_ms[name] / 1e3) / 1e9,
             "frac_of_hbm": vb / (var_ms[name] / 1e3) / 1e9 / peak,

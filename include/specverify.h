@@ -284,6 +284,23 @@ int svf_spec_accept_onehot(const float *target_logits, const int32_t *tokens,
                            svf_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * svf_spec_accept_greedy_bf16, svf_spec_accept_onehot_bf16 -- the same two
+ * rules on bf16 target logits (target_logits [B, N, V] bf16, each value
+ * widened exactly to fp32 on load; the arithmetic and the outputs are those
+ * of the fp32 calls on the widened logits). Limits as for the fp32 calls,
+ * with target_logits 8-byte aligned when V % 4 == 0.
+ * ---------------------------------------------------------------------- */
+int svf_spec_accept_greedy_bf16(const void *target_logits, const int32_t *tokens,
+                                const int32_t *parent, int B, int N, int V, int32_t *accept_len,
+                                int32_t *path, int32_t *out_tokens, int32_t *status,
+                                svf_stream_t stream);
+int svf_spec_accept_onehot_bf16(const void *target_logits, const int32_t *tokens,
+                                const int32_t *parent, const float *u_accept,
+                                const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                                int32_t *path, int32_t *out_tokens, float *ratio,
+                                int32_t *status, svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * EAGLE-2 dynamic draft-tree construction.
  *
  * "EAGLE 演化史", § E.2-E.3, and "The EAGLE Family" (EAGLE-2): a node's value

@@ -42,6 +42,8 @@ EXPORTED = [
     "svf_spec_accept_bf16",
     "svf_spec_accept_greedy",
     "svf_spec_accept_onehot",
+    "svf_spec_accept_greedy_bf16",
+    "svf_spec_accept_onehot_bf16",
     "svf_eagle2_init",
     "svf_eagle2_expand",
     "svf_eagle2_finalize",
@@ -85,6 +87,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_spec_accept_greedy.restype = I
     lib.svf_spec_accept_onehot.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P, P, P]
     lib.svf_spec_accept_onehot.restype = I
+    lib.svf_spec_accept_greedy_bf16.argtypes = [P, P, P, I, I, I, P, P, P, P, P]
+    lib.svf_spec_accept_greedy_bf16.restype = I
+    lib.svf_spec_accept_onehot_bf16.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.svf_spec_accept_onehot_bf16.restype = I
     lib.svf_eagle2_init.argtypes = [P, I, I, P, P, P, P, P, P]
     lib.svf_eagle2_init.restype = I
     lib.svf_eagle2_expand.argtypes = [P, I, I, I, I, P, I, P, P, P, P, P, P, P, P]
@@ -300,29 +306,37 @@ def _variant_outputs(o, B, N, dev, want_ratio):
 
 def spec_accept_greedy(target_logits: torch.Tensor, tokens: torch.Tensor, parent: torch.Tensor,
                        outputs: Optional[dict] = None, stream=None) -> dict:
-    """Temperature-0 acceptance (argmax matching). Returns a dict of device
-    tensors: accept_len [B], path [B, N], out_tokens [B, N], status [B]."""
+    """Temperature-0 acceptance (argmax matching) on float32 or bfloat16
+    logits. Returns a dict of device tensors: accept_len [B], path [B, N],
+    out_tokens [B, N], status [B]."""
     lib = load_library()
-    _dev(target_logits, "target_logits", torch.float32)
+    if target_logits.dtype not in (torch.float32, torch.bfloat16):
+        raise SpecVerifyError("target_logits must be float32 or bfloat16")
+    _dev(target_logits, "target_logits")
+    bf = target_logits.dtype == torch.bfloat16
     B, N, V = target_logits.shape
     _dev(tokens, "tokens", torch.int32, (B, N))
     _dev(parent, "parent", torch.int32, (B, N))
     o = _variant_outputs(outputs if outputs is not None else {}, B, N, target_logits.device,
                          False)
-    rc = lib.svf_spec_accept_greedy(_ptr(target_logits), _ptr(tokens), _ptr(parent), B, N, V,
-                                    _ptr(o["accept_len"]), _ptr(o["path"]),
-                                    _ptr(o["out_tokens"]), _ptr(o["status"]), _stream(stream))
-    _check(rc, "svf_spec_accept_greedy")
+    fn = lib.svf_spec_accept_greedy_bf16 if bf else lib.svf_spec_accept_greedy
+    rc = fn(_ptr(target_logits), _ptr(tokens), _ptr(parent), B, N, V, _ptr(o["accept_len"]),
+            _ptr(o["path"]), _ptr(o["out_tokens"]), _ptr(o["status"]), _stream(stream))
+    _check(rc, "svf_spec_accept_greedy" + ("_bf16" if bf else ""))
     return o
 
 
 def spec_accept_onehot(target_logits: torch.Tensor, tokens: torch.Tensor, parent: torch.Tensor,
                        u_accept: torch.Tensor, u_bonus: torch.Tensor, want_ratio: bool = True,
                        outputs: Optional[dict] = None, stream=None) -> dict:
-    """The sampling rule with q = one-hot(candidate) for every child. Returns
-    accept_len, path, out_tokens, ratio (or None) and status."""
+    """The sampling rule with q = one-hot(candidate) for every child, on
+    float32 or bfloat16 logits. Returns accept_len, path, out_tokens, ratio
+    (or None) and status."""
     lib = load_library()
-    _dev(target_logits, "target_logits", torch.float32)
+    if target_logits.dtype not in (torch.float32, torch.bfloat16):
+        raise SpecVerifyError("target_logits must be float32 or bfloat16")
+    _dev(target_logits, "target_logits")
+    bf = target_logits.dtype == torch.bfloat16
     B, N, V = target_logits.shape
     _dev(tokens, "tokens", torch.int32, (B, N))
     _dev(parent, "parent", torch.int32, (B, N))
@@ -330,12 +344,11 @@ def spec_accept_onehot(target_logits: torch.Tensor, tokens: torch.Tensor, parent
     _dev(u_bonus, "u_bonus", torch.float32, (B,))
     o = _variant_outputs(outputs if outputs is not None else {}, B, N, target_logits.device,
                          want_ratio)
-    rc = lib.svf_spec_accept_onehot(_ptr(target_logits), _ptr(tokens), _ptr(parent),
-                                    _ptr(u_accept), _ptr(u_bonus), B, N, V,
-                                    _ptr(o["accept_len"]), _ptr(o["path"]),
-                                    _ptr(o["out_tokens"]), _ptr(o.get("ratio")),
-                                    _ptr(o["status"]), _stream(stream))
-    _check(rc, "svf_spec_accept_onehot")
+    fn = lib.svf_spec_accept_onehot_bf16 if bf else lib.svf_spec_accept_onehot
+    rc = fn(_ptr(target_logits), _ptr(tokens), _ptr(parent), _ptr(u_accept), _ptr(u_bonus), B,
+            N, V, _ptr(o["accept_len"]), _ptr(o["path"]), _ptr(o["out_tokens"]),
+            _ptr(o.get("ratio")), _ptr(o["status"]), _stream(stream))
+    _check(rc, "svf_spec_accept_onehot" + ("_bf16" if bf else ""))
     return o
 
 

@@ -17,6 +17,9 @@
 // every test is a scalar: p~(x) = p(x) / (1 - p(R)) for x not in R, 0 for x
 // in R. The bonus token is the inverse CDF of p~ at u_bonus.
 //
+// Logits are fp32 or bf16 (widened exactly to fp32 on load); the arithmetic
+// is the same for both.
+//
 // Layout as in accept.cu: one CTA cluster per sequence (one CTA for small
 // vocabularies), each CTA owning a fixed slice of the vocabulary and holding
 // its slice of the current node's target row in registers as 128-element
@@ -56,6 +59,31 @@ __device__ __forceinline__ void load_row(const float *__restrict__ row, int V, i
         }
     }
 }
+
+// The same groups of a bf16 row (VEC: four bf16, 8 bytes, per load), widened
+// exactly to fp32.
+template <int E4, bool VEC>
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *__restrict__ row, int V, int g0,
+                                         int lane, float4 (&x)[E4]) {
+#pragma unroll
+    for (int k = 0; k < E4; ++k) {
+        const long long e0 = 128ll * (g0 + k) + 4 * lane;
+        if (VEC && e0 + 3 < V) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(row + e0));
+            x[k] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                               __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+        } else {
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = (e0 + i < V) ? __bfloat162float(row[e0 + i]) : -INFINITY;
+            x[k] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    }
+}
+
+__device__ __forceinline__ float logit_at(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float logit_at(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
 __device__ __forceinline__ float comp(const float4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -128,9 +156,9 @@ __device__ __forceinline__ void set_comp(float4 &v, int i, float x) {
 
 }  // namespace tgt
 
-template <int NT, int E4, bool VEC, bool CLUSTER, bool GREEDY>
+template <int NT, int E4, bool VEC, bool CLUSTER, bool GREEDY, typename T>
 __global__ void __launch_bounds__(NT, 1) accept_target_kernel(
-    const float *__restrict__ target, const int32_t *__restrict__ tokens,
+    const T *__restrict__ target, const int32_t *__restrict__ tokens,
     const int32_t *__restrict__ parent, const float *__restrict__ u_accept,
     const float *__restrict__ u_bonus, int N, int V, int CL, int32_t *__restrict__ accept_len,
     int32_t *__restrict__ path, int32_t *__restrict__ out_tokens, float *__restrict__ ratio,
@@ -211,7 +239,7 @@ __global__ void __launch_bounds__(NT, 1) accept_target_kernel(
                     nx = c;
                     break;
                 }
-            if (!GREEDY) slx[i] = __ldg(target + (base + pp) * (size_t)V + stok[i]);
+            if (!GREEDY) slx[i] = logit_at(target + (base + pp) * (size_t)V + stok[i]);
         }
         snext[i] = nx;
     }
@@ -558,13 +586,13 @@ bool target_config(int B, int V, TargetCfg *c) {
     return true;
 }
 
-template <int NT, int E4, bool VEC, bool CLUSTER, bool GREEDY>
-cudaError_t launch_target(const TargetCfg &c, const float *target, const int32_t *tokens,
+template <int NT, int E4, bool VEC, bool CLUSTER, bool GREEDY, typename T>
+cudaError_t launch_target(const TargetCfg &c, const T *target, const int32_t *tokens,
                           const int32_t *parent, const float *u_accept, const float *u_bonus,
                           int B, int N, int V, int32_t *accept_len, int32_t *path,
                           int32_t *out_tokens, float *ratio, int32_t *status,
                           cudaStream_t stream) {
-    auto kern = accept_target_kernel<NT, E4, VEC, CLUSTER, GREEDY>;
+    auto kern = accept_target_kernel<NT, E4, VEC, CLUSTER, GREEDY, T>;
     const size_t smem = (size_t)N * 6 * sizeof(int32_t);
     if (CLUSTER && c.cl > 8) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -576,14 +604,14 @@ cudaError_t launch_target(const TargetCfg &c, const float *target, const int32_t
                       accept_len, path, out_tokens, ratio, status);
 }
 
-template <bool VEC, bool GREEDY>
-cudaError_t dispatch_target(const TargetCfg &c, const float *target, const int32_t *tokens,
+template <bool VEC, bool GREEDY, typename T>
+cudaError_t dispatch_target(const TargetCfg &c, const T *target, const int32_t *tokens,
                             const int32_t *parent, const float *u_accept, const float *u_bonus,
                             int B, int N, int V, int32_t *accept_len, int32_t *path,
                             int32_t *out_tokens, float *ratio, int32_t *status,
                             cudaStream_t stream) {
 #define SVF_TGT(NT_, E4_, CL_)                                                                   \
-    return launch_target<NT_, E4_, VEC, CL_, GREEDY>(c, target, tokens, parent, u_accept,       \
+    return launch_target<NT_, E4_, VEC, CL_, GREEDY, T>(c, target, tokens, parent, u_accept,    \
                                                      u_bonus, B, N, V, accept_len, path,        \
                                                      out_tokens, ratio, status, stream)
     if (c.nt == tgt::kSmallThreads) {
@@ -610,11 +638,12 @@ bool accept_target_supported(int V) {
     return V >= 1 && target_config(1, V, &c);
 }
 
-cudaError_t launch_accept_target(bool greedy, const float *target, const int32_t *tokens,
-                                 const int32_t *parent, const float *u_accept,
-                                 const float *u_bonus, int B, int N, int V, int32_t *accept_len,
-                                 int32_t *path, int32_t *out_tokens, float *ratio,
-                                 int32_t *status, cudaStream_t stream) {
+template <typename T>
+cudaError_t launch_target_walk(bool greedy, const T *target, const int32_t *tokens,
+                               const int32_t *parent, const float *u_accept,
+                               const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                               int32_t *path, int32_t *out_tokens, float *ratio,
+                               int32_t *status, cudaStream_t stream) {
     TargetCfg c;
     if (!target_config(B, V, &c)) return cudaErrorInvalidValue;
     const bool vec = (V & 3) == 0;
@@ -631,6 +660,25 @@ cudaError_t launch_accept_target(bool greedy, const float *target, const int32_t
                : dispatch_target<false, false>(c, target, tokens, parent, u_accept, u_bonus, B,
                                                N, V, accept_len, path, out_tokens, ratio, status,
                                                stream);
+}
+
+cudaError_t launch_accept_target(bool greedy, const float *target, const int32_t *tokens,
+                                 const int32_t *parent, const float *u_accept,
+                                 const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                                 int32_t *path, int32_t *out_tokens, float *ratio,
+                                 int32_t *status, cudaStream_t stream) {
+    return launch_target_walk(greedy, target, tokens, parent, u_accept, u_bonus, B, N, V,
+                              accept_len, path, out_tokens, ratio, status, stream);
+}
+
+cudaError_t launch_accept_target_bf16(bool greedy, const __nv_bfloat16 *target,
+                                      const int32_t *tokens, const int32_t *parent,
+                                      const float *u_accept, const float *u_bonus, int B, int N,
+                                      int V, int32_t *accept_len, int32_t *path,
+                                      int32_t *out_tokens, float *ratio, int32_t *status,
+                                      cudaStream_t stream) {
+    return launch_target_walk(greedy, target, tokens, parent, u_accept, u_bonus, B, N, V,
+                              accept_len, path, out_tokens, ratio, status, stream);
 }
 
 }  // namespace svf

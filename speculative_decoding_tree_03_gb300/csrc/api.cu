@@ -159,16 +159,19 @@ int svf_spec_accept_bf16(const void *target_logits, const void *draft_logits,
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 
-static int accept_variant_args(const float *target, const int32_t *tokens, const int32_t *parent,
-                               int B, int N, int V, const int32_t *accept_len,
-                               const int32_t *path, const int32_t *out_tokens,
-                               const int32_t *status) {
+// Shared checks of the target-only variants; 1 for an empty batch. Rows of
+// V % 4 == 0 logits are read four at a time: 16-byte (fp32) or 8-byte (bf16)
+// aligned.
+static int accept_variant_args(const void *target, size_t elem, const int32_t *tokens,
+                               const int32_t *parent, int B, int N, int V,
+                               const int32_t *accept_len, const int32_t *path,
+                               const int32_t *out_tokens, const int32_t *status) {
     if (B < 0 || N < 0 || V < 0) return SVF_ERR_ARG;
     if (B == 0) return 1;
     if (!target || !tokens || !parent || !accept_len || !path || !out_tokens || !status)
         return SVF_ERR_ARG;
     if (N < 1 || N > 1024 || V < 1 || !accept_target_supported(V)) return SVF_ERR_UNSUPPORTED;
-    if ((V & 3) == 0 && !aligned16(target)) return SVF_ERR_ARG;
+    if ((V & 3) == 0 && ((uintptr_t)target % (4 * elem)) != 0) return SVF_ERR_ARG;
     return SVF_OK;
 }
 
@@ -176,8 +179,8 @@ int svf_spec_accept_greedy(const float *target_logits, const int32_t *tokens,
                            const int32_t *parent, int B, int N, int V, int32_t *accept_len,
                            int32_t *path, int32_t *out_tokens, int32_t *status,
                            svf_stream_t stream) {
-    const int rc = accept_variant_args(target_logits, tokens, parent, B, N, V, accept_len, path,
-                                       out_tokens, status);
+    const int rc = accept_variant_args(target_logits, sizeof(float), tokens, parent, B, N, V,
+                                       accept_len, path, out_tokens, status);
     if (rc != SVF_OK) return rc > 0 ? SVF_OK : rc;
     cudaError_t e = launch_accept_target(true, target_logits, tokens, parent, nullptr, nullptr, B,
                                          N, V, accept_len, path, out_tokens, nullptr, status,
@@ -190,13 +193,43 @@ int svf_spec_accept_onehot(const float *target_logits, const int32_t *tokens,
                            int B, int N, int V, int32_t *accept_len, int32_t *path,
                            int32_t *out_tokens, float *ratio, int32_t *status,
                            svf_stream_t stream) {
-    const int rc = accept_variant_args(target_logits, tokens, parent, B, N, V, accept_len, path,
-                                       out_tokens, status);
+    const int rc = accept_variant_args(target_logits, sizeof(float), tokens, parent, B, N, V,
+                                       accept_len, path, out_tokens, status);
     if (rc != SVF_OK) return rc > 0 ? SVF_OK : rc;
     if (!u_accept || !u_bonus) return SVF_ERR_ARG;
     cudaError_t e = launch_accept_target(false, target_logits, tokens, parent, u_accept, u_bonus,
                                          B, N, V, accept_len, path, out_tokens, ratio, status,
                                          reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+int svf_spec_accept_greedy_bf16(const void *target_logits, const int32_t *tokens,
+                                const int32_t *parent, int B, int N, int V, int32_t *accept_len,
+                                int32_t *path, int32_t *out_tokens, int32_t *status,
+                                svf_stream_t stream) {
+    const int rc = accept_variant_args(target_logits, sizeof(__nv_bfloat16), tokens, parent, B,
+                                       N, V, accept_len, path, out_tokens, status);
+    if (rc != SVF_OK) return rc > 0 ? SVF_OK : rc;
+    cudaError_t e = launch_accept_target_bf16(
+        true, reinterpret_cast<const __nv_bfloat16 *>(target_logits), tokens, parent, nullptr,
+        nullptr, B, N, V, accept_len, path, out_tokens, nullptr, status,
+        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
+int svf_spec_accept_onehot_bf16(const void *target_logits, const int32_t *tokens,
+                                const int32_t *parent, const float *u_accept,
+                                const float *u_bonus, int B, int N, int V, int32_t *accept_len,
+                                int32_t *path, int32_t *out_tokens, float *ratio,
+                                int32_t *status, svf_stream_t stream) {
+    const int rc = accept_variant_args(target_logits, sizeof(__nv_bfloat16), tokens, parent, B,
+                                       N, V, accept_len, path, out_tokens, status);
+    if (rc != SVF_OK) return rc > 0 ? SVF_OK : rc;
+    if (!u_accept || !u_bonus) return SVF_ERR_ARG;
+    cudaError_t e = launch_accept_target_bf16(
+        false, reinterpret_cast<const __nv_bfloat16 *>(target_logits), tokens, parent, u_accept,
+        u_bonus, B, N, V, accept_len, path, out_tokens, ratio, status,
+        reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 

@@ -50,6 +50,12 @@ cudaError_t launch_accept_target(bool greedy, const float *target, const int32_t
                                  const float *u_bonus, int B, int N, int V, int32_t *accept_len,
                                  int32_t *path, int32_t *out_tokens, float *ratio,
                                  int32_t *status, cudaStream_t stream);
+cudaError_t launch_accept_target_bf16(bool greedy, const __nv_bfloat16 *target,
+                                      const int32_t *tokens, const int32_t *parent,
+                                      const float *u_accept, const float *u_bonus, int B, int N,
+                                      int V, int32_t *accept_len, int32_t *path,
+                                      int32_t *out_tokens, float *ratio, int32_t *status,
+                                      cudaStream_t stream);
 
 // Arguments of one KV commit call (kv_commit.cu).
 struct KvCommitArgs {

@@ -144,6 +144,22 @@ def test_accept_variant_argument_checks(lib):
     assert onehot(u=None) == -1
 
 
+def test_accept_variant_bf16_argument_checks(lib):
+    def greedy(B=2, N=3, V=100, t=P):
+        return lib.svf_spec_accept_greedy_bf16(t, P, P, B, N, V, P, P, P, P, None)
+
+    def onehot(B=2, N=3, V=100, t=P, u=P):
+        return lib.svf_spec_accept_onehot_bf16(t, P, P, u, P, B, N, V, P, P, P, None, P, None)
+    for call in (greedy, onehot):
+        assert call(B=-1) == -1
+        assert call(B=0, t=None) == 0
+        assert call(t=None) == -1
+        assert call(N=0) == -2 and call(N=1025) == -2
+        assert call(V=262145) == -2
+        assert call(V=128, t=ctypes.c_void_p(260)) == -1   # 8-byte loads of four bf16
+    assert onehot(u=None) == -1
+
+
 def test_eagle2_argument_checks(lib):
     def expand(B=2, R=8, V=1000, k=8, cap=329, rows=P):
         return lib.svf_eagle2_expand(rows, B, R, V, k, P, cap, P, P, P, P, P, P, None, None)

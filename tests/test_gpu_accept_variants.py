@@ -184,3 +184,56 @@ def test_onehot_lossless_on_gpu(sv):
     counts = np.bincount(gpu["out_tokens"][:, 0], minlength=V)
     _, pval = chisquare(counts, p * T)
     assert pval > 1e-4, pval
+
+
+def _bf16(x):
+    """Logits rounded to bf16 on the CPU: the bf16 device tensor and the same
+    values widened to float32 for the oracle."""
+    t = torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16)
+    return t.cuda(), t.float().numpy()
+
+
+BF16_VOCABS = [37, 4096, 5003, 32000, 128256]
+
+
+@pytest.mark.parametrize("V", BF16_VOCABS)
+def test_greedy_bf16_matches_oracle(sv, V):
+    """bf16 rows: many equal maxima after rounding, each resolved to the
+    lowest id on both sides."""
+    B = 24 if V > 100000 else 48
+    a = _case(V + 11, B, 15, V, noise=0.5)
+    tb, tf = _bf16(a["target"])
+    r = sv.spec_accept_greedy(tb, _dev(a["tokens"]), _dev(a["parent"]))
+    torch.cuda.synchronize()
+    gpu = {k: _np(v) for k, v in r.items()}
+    orc = oracle.spec_accept_greedy(tf, a["tokens"], a["parent"])
+    for k in ("accept_len", "path", "out_tokens", "status"):
+        np.testing.assert_array_equal(gpu[k], orc[k], err_msg=k)
+
+
+@pytest.mark.parametrize("V", BF16_VOCABS)
+def test_onehot_bf16_matches_oracle(sv, V):
+    B = 24 if V > 100000 else 48
+    a = _case(V + 13, B, 15, V, sigma=2.0 if V <= 5003 else 8.0, noise=0.7)
+    tb, tf = _bf16(a["target"])
+    r = sv.spec_accept_onehot(tb, _dev(a["tokens"]), _dev(a["parent"]), _dev(a["u_accept"]),
+                              _dev(a["u_bonus"]))
+    torch.cuda.synchronize()
+    gpu = {k: _np(v) for k, v in r.items()}
+    orc = oracle.spec_accept_onehot(tf, a["tokens"], a["parent"], a["u_accept"], a["u_bonus"])
+    _compare_onehot(gpu, orc)
+
+
+def test_variants_bf16_many_sequences(sv):
+    a = _case(101, 64, 31, 128256, noise=1.5, binary=True)
+    tb, tf = _bf16(a["target"])
+    g = sv.spec_accept_greedy(tb, _dev(a["tokens"]), _dev(a["parent"]))
+    h = sv.spec_accept_onehot(tb, _dev(a["tokens"]), _dev(a["parent"]), _dev(a["u_accept"]),
+                              _dev(a["u_bonus"]))
+    torch.cuda.synchronize()
+    o = oracle.spec_accept_greedy(tf, a["tokens"], a["parent"])
+    for k in ("accept_len", "path", "out_tokens"):
+        np.testing.assert_array_equal(_np(g[k]), o[k], err_msg=k)
+    _compare_onehot({k: _np(v) for k, v in h.items()},
+                    oracle.spec_accept_onehot(tf, a["tokens"], a["parent"], a["u_accept"],
+                                              a["u_bonus"]))
