@@ -35,7 +35,37 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
 }
 
-template <typename Elt, int E>
+// Eight consecutive elements of a K or V row, widened to fp32. VEC: the row
+// is 16-byte aligned (two float4 loads, or one load of eight bf16).
+template <bool VEC>
+__device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
+    if (VEC) {
+        const float4 u = __ldg(reinterpret_cast<const float4 *>(p));
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(p + 4));
+        x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+        x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = __ldg(p + i);
+    }
+}
+template <bool VEC>
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
+    if (VEC) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(p[i]);
+    }
+}
+
+template <typename Elt, int E, bool VEC>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale) {
     constexpr int D = 32 * E;
     const int lane = threadIdx.x & 31;
@@ -101,11 +131,21 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale)
         float s = -INFINITY;
         if (vis) {
             off_t = (((size_t)pt[t / ps] * ps + (size_t)(t % ps)) * a.Hkv + g) * D;
+            // the K row in pieces of 64 elements, each piece's loads issued
+            // together
             float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll 8
-            for (int d = 0; d < D; d += 2) {
-                s0 = fmaf(sq[wib][d], to_f(kc[off_t + d]), s0);
-                s1 = fmaf(sq[wib][d + 1], to_f(kc[off_t + d + 1]), s1);
+#pragma unroll
+            for (int d0 = 0; d0 < D; d0 += 64) {
+                float kx[8][8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) load8<VEC>(kc + off_t + d0 + 8 * c, kx[c]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        s0 = fmaf(sq[wib][d0 + 8 * c + i], kx[c][i], s0);
+                        s1 = fmaf(sq[wib][d0 + 8 * c + i + 1], kx[c][i + 1], s1);
+                    }
             }
             s = (s0 + s1) * scale;
         }
@@ -118,12 +158,13 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale)
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] *= corr;
         mx = mn;
-        // eight V rows per batch: the (predicated) loads go out together; a
+        // VB V rows per batch: the (predicated) loads go out together; a
         // token with p = 0 is not read (its slot may hold anything)
-        for (int j0 = 0; j0 < 32; j0 += 8) {
-            float pj[8], vv[8][E];
+        constexpr int VB = E <= 2 ? 16 : 8;
+        for (int j0 = 0; j0 < 32; j0 += VB) {
+            float pj[VB], vv[VB][E];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < VB; ++u) {
                 pj[u] = __shfl_sync(0xffffffffu, p, j0 + u);
                 const size_t oj = __shfl_sync(0xffffffffu, off_t, j0 + u);
 #pragma unroll
@@ -131,7 +172,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale)
                     vv[u][e] = pj[u] != 0.0f ? to_f(vc[oj + lane * E + e]) : 0.0f;
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < VB; ++u)
 #pragma unroll
                 for (int e = 0; e < E; ++e) acc[e] = fmaf(pj[u], vv[u][e], acc[e]);
         }
@@ -146,17 +187,25 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t stream) {
     const int threads = 128;
     const long long blocks = (warps * 32 + threads - 1) / threads;
     const float scale = a.sm_scale > 0.0f ? a.sm_scale : 1.0f / sqrtf((float)a.D);
+    // K rows start at multiples of D elements: vector loads when the caches
+    // are 16-byte aligned
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.k_cache) |
+                       reinterpret_cast<uintptr_t>(a.v_cache)) & 15u) == 0;
+#define SVF_SIMT(T_, E_)                                                                       \
+    do {                                                                                       \
+        if (vec)                                                                               \
+            attn_simt_kernel<T_, E_, true><<<(unsigned)blocks, threads, 0, stream>>>(a, scale); \
+        else                                                                                   \
+            attn_simt_kernel<T_, E_, false><<<(unsigned)blocks, threads, 0, stream>>>(a, scale);\
+    } while (0)
     if (a.dtype == SVF_F32) {
-        if (a.D == 64)
-            attn_simt_kernel<float, 2><<<(unsigned)blocks, threads, 0, stream>>>(a, scale);
-        else
-            attn_simt_kernel<float, 4><<<(unsigned)blocks, threads, 0, stream>>>(a, scale);
+        if (a.D == 64) SVF_SIMT(float, 2);
+        else SVF_SIMT(float, 4);
     } else {
-        if (a.D == 64)
-            attn_simt_kernel<__nv_bfloat16, 2><<<(unsigned)blocks, threads, 0, stream>>>(a, scale);
-        else
-            attn_simt_kernel<__nv_bfloat16, 4><<<(unsigned)blocks, threads, 0, stream>>>(a, scale);
+        if (a.D == 64) SVF_SIMT(__nv_bfloat16, 2);
+        else SVF_SIMT(__nv_bfloat16, 4);
     }
+#undef SVF_SIMT
     return cudaGetLastError();
 }
 
