@@ -2,11 +2,12 @@
 //
 // "EAGLE 演化史", § Tree Verification 详解, A-B: node i of sequence b attends
 // to the cached prefix t < L_b and to tree positions L_b + j for j an ancestor
-// of i or i itself. One warp owns one (sequence, node, query head): each lane
-// scores one token of a block of 32, and an online softmax (running max,
-// running sum, rescaled accumulator; the lanes split head_dim for the output)
-// folds the visible tokens in blocks of 32. fp32 arithmetic throughout with
-// the accurate expf.
+// of i or i itself. One 4-warp CTA owns one (sequence, node, query head);
+// each warp takes every fourth block of 32 tokens: each lane scores one token
+// of the block, and an online softmax (running max, running sum, rescaled
+// accumulator; the lanes split head_dim for the output) folds the visible
+// tokens in. The warps' states merge at the end. fp32 arithmetic throughout
+// with the accurate expf.
 #include <math.h>
 
 #include "common.cuh"
@@ -68,13 +69,12 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
 template <typename Elt, int E, bool VEC>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale) {
     constexpr int D = 32 * E;
-    const int lane = threadIdx.x & 31;
-    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const long long total = (long long)a.B * a.N * a.Hq;
-    if (warp >= total) return;
-    const int h = (int)(warp % a.Hq);
-    const int i = (int)((warp / a.Hq) % a.N);
-    const int b = (int)(warp / ((long long)a.N * a.Hq));
+    constexpr int NWARP = 4;  // warps per row, each over every fourth block
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const long long rowid = blockIdx.x;  // (b, i, h)
+    const int h = (int)(rowid % a.Hq);
+    const int i = (int)((rowid / a.Hq) % a.N);
+    const int b = (int)(rowid / ((long long)a.N * a.Hq));
     const int G = a.Hq / a.Hkv;
     const int g = h / G;
     const int L = a.seq_lens[b];
@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale)
     const int ps = a.page_size;
     const int32_t *pt = a.page_table + (size_t)b * a.max_pages;
 
+    // every warp checks the whole page range, so every warp takes the same
+    // branch below
     int err = 0;
     if (L < 0 || Tlen > (long long)a.max_pages * ps) {
         err = SVF_DEV_BAD_LENGTH;
@@ -96,34 +98,34 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale)
     const size_t row = ((size_t)b * a.N + i) * a.Hq + h;
     Elt *outp = reinterpret_cast<Elt *>(a.out) + row * D;
     if (err) {
+        if (w == 0) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) outp[lane * E + e] = from_f<Elt>(0.0f);
-        if (lane == 0) {
-            if (a.lse) a.lse[row] = 0.0f;
-            atomicOr(&a.status[b], err);
+            for (int e = 0; e < E; ++e) outp[lane * E + e] = from_f<Elt>(0.0f);
+            if (lane == 0) {
+                if (a.lse) a.lse[row] = 0.0f;
+                atomicOr(&a.status[b], err);
+            }
         }
         return;
     }
 
     const Elt *qp = reinterpret_cast<const Elt *>(a.q) + row * D;
-    // this warp's q row in shared memory: every lane reads all of it per token
-    __shared__ float sq[4][32 * E];
-    const int wib = (threadIdx.x >> 5) & 3;
-#pragma unroll
-    for (int e = 0; e < E; ++e) sq[wib][lane * E + e] = to_f(qp[lane * E + e]);
-    __syncwarp();
+    // the q row in shared memory: every lane reads all of it per token
+    __shared__ float sq[32 * E];
+    for (int d = threadIdx.x; d < D; d += blockDim.x) sq[d] = to_f(qp[d]);
+    __syncthreads();
     const uint64_t anc = a.anc[(size_t)b * a.N + i];
     const Elt *kc = reinterpret_cast<const Elt *>(a.k_cache);
     const Elt *vc = reinterpret_cast<const Elt *>(a.v_cache);
-    // Blocks of 32 tokens: lane j scores token t0 + j over the whole head
-    // (the whole q row is read by every lane; it stays in L1), the block's
-    // maximum rescales the running output once, and the output lanes (which
-    // split head_dim) then fold the block's V rows in, whose loads are
-    // independent of one another.
+    // Blocks of 32 tokens, block k to warp k % 4: lane j scores token t0 + j
+    // over the whole head (the whole q row is read by every lane), the block's
+    // maximum rescales the warp's running output once, and the output lanes
+    // (which split head_dim) then fold the block's V rows in, whose loads are
+    // independent of one another. The four warps' states merge at the end.
     float mx = -INFINITY, l = 0.0f, acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.0f;
-    for (long long t0 = 0; t0 < Tlen; t0 += 32) {
+    for (long long t0 = 32ll * w; t0 < Tlen; t0 += 32 * NWARP) {
         const long long t = t0 + lane;
         bool vis = t < Tlen;
         if (vis && t >= L) vis = (anc >> (int)(t - L)) & 1ull;
@@ -142,9 +144,9 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale)
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
 #pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        s0 = fmaf(sq[wib][d0 + 8 * c + i], kx[c][i], s0);
-                        s1 = fmaf(sq[wib][d0 + 8 * c + i + 1], kx[c][i + 1], s1);
+                    for (int q = 0; q < 8; q += 2) {
+                        s0 = fmaf(sq[d0 + 8 * c + q], kx[c][q], s0);
+                        s1 = fmaf(sq[d0 + 8 * c + q + 1], kx[c][q + 1], s1);
                     }
             }
             s = (s0 + s1) * scale;
@@ -177,15 +179,39 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a, float scale)
                 for (int e = 0; e < E; ++e) acc[e] = fmaf(pj[u], vv[u][e], acc[e]);
         }
     }
-    const float inv = 1.0f / l;
+    // merge the warps' (max, sum, output): each scaled by e^(max_w - M)
+    __shared__ float s_mx[NWARP], s_l[NWARP], s_acc[NWARP][32 * E];
+    if (lane == 0) {
+        s_mx[w] = mx;
+        s_l[w] = l;
+    }
 #pragma unroll
-    for (int e = 0; e < E; ++e) outp[lane * E + e] = from_f<Elt>(acc[e] * inv);
-    if (lane == 0 && a.lse) a.lse[row] = mx + logf(l);
+    for (int e = 0; e < E; ++e) s_acc[w][lane * E + e] = acc[e];
+    __syncthreads();
+    if (w != 0) return;
+    float M = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < NWARP; ++v) M = fmaxf(M, s_mx[v]);
+    float f[NWARP], lt = 0.0f;
+#pragma unroll
+    for (int v = 0; v < NWARP; ++v) {
+        f[v] = s_mx[v] == -INFINITY ? 0.0f : expf(s_mx[v] - M);
+        lt = fmaf(s_l[v], f[v], lt);
+    }
+    const float inv = 1.0f / lt;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        float o = 0.0f;
+#pragma unroll
+        for (int v = 0; v < NWARP; ++v) o = fmaf(s_acc[v][lane * E + e], f[v], o);
+        outp[lane * E + e] = from_f<Elt>(o * inv);
+    }
+    if (lane == 0 && a.lse) a.lse[row] = M + logf(lt);
 }
+
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t stream) {
-    const long long warps = (long long)a.B * a.N * a.Hq;
+    const long long blocks = (long long)a.B * a.N * a.Hq;  // one 4-warp CTA per row
     const int threads = 128;
-    const long long blocks = (warps * 32 + threads - 1) / threads;
     const float scale = a.sm_scale > 0.0f ? a.sm_scale : 1.0f / sqrtf((float)a.D);
     // K rows start at multiples of D elements: vector loads when the caches
     // are 16-byte aligned
