@@ -191,3 +191,25 @@ def test_package_refuses_cpu_tensors():
     import speculative_decoding_tree_03_gb300 as sv
     with pytest.raises(sv.SpecVerifyError):
         sv.tree_mask_build(torch.zeros((1, 3), dtype=torch.int32))
+
+
+def test_package_checks_before_any_launch():
+    """Every binding call validates its tensors on the host: CPU tensors, a
+    wrong logits dtype and a wrong status shape raise before the library is
+    asked to launch anything."""
+    import torch
+    import speculative_decoding_tree_03_gb300 as sv
+    t = torch.zeros((1, 3, 16), dtype=torch.float32)
+    i = torch.zeros((1, 3), dtype=torch.int32)
+    u = torch.zeros((1, 3), dtype=torch.float32)
+    ub = torch.zeros((1,), dtype=torch.float32)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.spec_accept_greedy(t, i, i)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.spec_accept_onehot(t, i, i, u, ub)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.spec_accept_greedy(t.to(torch.float16), i, i)          # neither fp32 nor bf16
+    with pytest.raises(sv.SpecVerifyError):
+        sv.spec_accept(t, t, i, i, u, ub)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.eagle2_pool(torch.zeros((2,), dtype=torch.int32), 16)
