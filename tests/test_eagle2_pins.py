@@ -122,6 +122,8 @@ def test_values_are_products_of_confidences_and_rerank_is_connected(seed):
             depth[i] = depth[par[i]] + 1
         assert (np.diff(depth) >= 0).all()
         for i in range(1, n - 1):
+            if depth[i] == depth[i + 1]:
+                assert par[i] <= par[i + 1]   # a level is grouped by parent, in order
             if par[i] == par[i + 1]:
                 assert val[i] >= val[i + 1]
         # value = product of draft softmax probabilities along the root path
