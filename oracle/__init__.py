@@ -14,6 +14,8 @@ Functions (the C file cites the passage each one follows):
   spec_accept_greedy(target, tokens, parent) -> dict
   eagle2_pool / eagle2_expand / eagle2_finalize: EAGLE-2 tree construction
   spec_accept_onehot(target, tokens, parent, u_accept, u_bonus) -> dict
+  lm_head_logits(hidden, W)              -> logits [..., V] f64
+  spec_accept_lmhead(hidden, W, draft, tokens, parent, u_accept, u_bonus) -> dict
 """
 
 from __future__ import annotations
@@ -71,6 +73,8 @@ def _load():
             lib.oracle_eagle2_expand.restype = I
             lib.oracle_eagle2_finalize.argtypes = [I, I, P, P, P, P, P, I, P, P, P, P, P, P, P]
             lib.oracle_eagle2_finalize.restype = I
+            lib.oracle_lm_head.argtypes = [P, P, I, I, I, P]
+            lib.oracle_lm_head.restype = I
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = I
             lib.oracle_set_threads.argtypes = [I]
@@ -289,4 +293,33 @@ def eagle2_finalize(pool, n_nodes):
         _p(out["cid"]), _p(out["n_out"]), _p(out["cut_gap"]), _p(out["connected"]))
     if rc != 0:
         raise ValueError("oracle_eagle2_finalize: bad arguments")
+    return out
+
+
+def lm_head_logits(hidden, W):
+    """Target logits from the LM head: hidden [..., H] (one state per tree
+    node) times W [V, H] transposed, in fp64. bf16 inputs must arrive widened
+    to float32 (exactly)."""
+    hidden = np.ascontiguousarray(hidden, dtype=np.float32)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    H = hidden.shape[-1]
+    V = W.shape[0]
+    if W.shape[1] != H:
+        raise ValueError("W must be [V, H] with H = hidden.shape[-1]")
+    R = hidden.size // H
+    out = np.zeros((R, V), np.float64)
+    rc = _load().oracle_lm_head(_p(hidden), _p(W), R, H, V, _p(out))
+    if rc != 0:
+        raise ValueError("oracle_lm_head: bad arguments")
+    return out.reshape(hidden.shape[:-1] + (V,))
+
+
+def spec_accept_lmhead(hidden, W, draft, tokens, parent, u_accept, u_bonus):
+    """The acceptance walk with the target rows produced by the LM head:
+    hidden [B, N, H], W [V, H]. The logits are the fp64 products rounded to
+    float32 (the walk's logits type); the walk is spec_accept's. Returns
+    spec_accept's dict plus "target" (the float32 logits it used)."""
+    target = lm_head_logits(hidden, W).astype(np.float32)
+    out = spec_accept(target, draft, tokens, parent, u_accept, u_bonus)
+    out["target"] = target
     return out

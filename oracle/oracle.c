@@ -783,3 +783,29 @@ int oracle_eagle2_finalize(int B, int C, const int32_t *pool_parent, const int32
     }
     return 0;
 }
+
+/*
+ * LM head. "The EAGLE Family: Speculating in Feature Space", § Why predict
+ * features instead of tokens?: the target's next-token distribution is
+ * softmax(W_LM h_t), the LM head being a fixed linear map of the last hidden
+ * state. "EAGLE 演化史", § D.2, puts the verify pass's bandwidth cost here:
+ * one vocabulary-sized product per tree node.
+ *
+ * Inputs:  h [R, H] (one hidden state per tree node, R = B * N), W [V, H]
+ *          (row v = the LM-head weights of token v); bf16 values arrive
+ *          widened exactly to float.
+ * Output:  logits [R, V] fp64: sum over k of h[r][k] * W[v][k], accumulated
+ *          in fp64 in increasing k.
+ */
+int oracle_lm_head(const float *h, const float *W, int R, int H, int V, double *logits) {
+    if (R < 0 || H < 1 || V < 1) return -1;
+#pragma omp parallel for schedule(static)
+    for (long long rv = 0; rv < (long long)R * V; ++rv) {
+        const long long r = rv / V, v = rv % V;
+        const float *hr = h + r * H, *wv = W + v * H;
+        double s = 0.0;
+        for (int k = 0; k < H; ++k) s += (double)hr[k] * (double)wv[k];
+        logits[rv] = s;
+    }
+    return 0;
+}
