@@ -2,15 +2,21 @@
 acceptance walk, on synthetic inputs shaped like the workloads.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-cpu-baseline]
+                    [--impl ours|reference] [--no-cpu-baseline] [--no-per-workload]
 
-Prints ONE JSON line on rank 0. ``value`` is verified tree nodes per second
-(per attention layer) over all ranks, with inputs resident in HBM; ``e2e``
-repeats the measurement through the public API from pinned host buffers with
-the copies inside the timed region (one packed host-to-device copy per step,
-issued on a side stream one step ahead, and the outputs read back). Between timed steps the inputs rotate over
-enough copies that the working set exceeds L2. ``--impl reference`` times the
-fp64 CPU oracle on the host cores instead (the reference arm).
+Prints ONE JSON line on rank 0. The headline workload is the 70B serving
+layer (batch 64, context 32768, 31-node trees, 64/8 heads, vocabulary
+128256), the largest configuration. ``value`` is verified tree nodes per
+second (per attention layer) over all ranks, with inputs resident in HBM;
+``e2e`` repeats the measurement through the public API from pinned host
+buffers with the copies inside the timed region (one packed host-to-device
+copy per step, issued on a side stream one step ahead, and the outputs read
+back). Between timed steps the inputs rotate over enough copies that the
+working set exceeds L2. Per-kernel times are taken inside the step: a second
+capture of the step graph carries timing events between its kernels.
+``per_workload`` repeats the step measurement on the four other workloads.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(the reference arm).
 
 Multi-GPU: the path does not shard; each rank runs an independent replica of
 the workload (weak scaling) and the step time is the maximum over ranks.
@@ -38,8 +44,9 @@ if ROOT not in sys.path:
 from synth import WORKLOADS, make_inputs  # noqa: E402
 from synth.gen import algorithmic_bytes  # noqa: E402
 
-DEFAULT_WORKLOAD = "binary_tree_8b"
+DEFAULT_WORKLOAD = "serving_70b"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def workload_by_name(name):
@@ -57,6 +64,17 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """(burst, sustained) bf16 TFLOP/s of the measured cuBLAS GEMM, and their kind."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
 def source_hash(rel):
@@ -92,6 +110,10 @@ def walk_bytes(w, parent: np.ndarray, path: np.ndarray, accept_len: np.ndarray) 
             total += w.V * 4 * (2 if int(j) in kids else 1)
     return total
 
+
+def visited_nodes(accept_len: np.ndarray) -> int:
+    """Nodes a finished walk visited: the root plus every accepted node."""
+    return int(np.asarray(accept_len, np.int64).sum()) + int(np.asarray(accept_len).shape[0])
 
 
 def aggregate(local_ms: float, local_units: float, world: int, reduce_max, reduce_sum):
@@ -163,56 +185,62 @@ class ClockSampler:
 # reference arm / CPU baseline: the oracle on the host cores
 # ---------------------------------------------------------------------------
 
-def _oracle_inputs(inp):
-    """Logical float32 K/V, q for the oracle (regenerated from the generator)."""
+def _oracle_inputs(inp, bs):
+    """q and logical float32 K/V of sequences ``bs`` for the oracle, regenerated
+    from the generator's streams (only those sequences)."""
     from synth.gen import logical_kv, bf16_bits_to_f32
     w = inp.w
-    T = inp.seq_lens.astype(np.int64) + w.N
+    T = inp.seq_lens[bs].astype(np.int64) + w.N
     Tcap = int(T.max())
-    K = np.zeros((w.B, Tcap, w.Hkv, w.D), np.float32)
+    K = np.zeros((len(bs), Tcap, w.Hkv, w.D), np.float32)
     V = np.zeros_like(K)
     cvt = (lambda x: bf16_bits_to_f32(x)) if w.dtype == "bf16" else (lambda x: x)
-    for b in range(w.B):
+    for n, b in enumerate(bs):
         for g in range(w.Hkv):
-            k, v = logical_kv(w, inp.seed, b, g, int(T[b]))
-            K[b, : T[b], g] = cvt(k)
-            V[b, : T[b], g] = cvt(v)
-    return cvt(inp.q), K, V
+            k, v = logical_kv(w, inp.seed, int(b), g, int(T[n]))
+            K[n, : T[n], g] = cvt(k)
+            V[n, : T[n], g] = cvt(v)
+    return cvt(inp.q[bs]), K, V
 
 
 def time_oracle(inp, budget_s=15.0, max_steps=20, steps=None, warmup=0, threads=None):
     """Time the fp64 oracle for the whole verify step on the host cores.
 
-    Without ``steps``: as many steps as fit in ``budget_s`` (at most
-    ``max_steps``). With ``steps``: ``warmup`` untimed steps, then exactly
-    ``steps`` timed ones, the attention rows sampled so that all of them fit
-    in ``budget_s``. Returns (seconds per step, sample text, cores)."""
+    Attention is timed on a bounded sample: at most two sequences (their K/V
+    regenerated alone), and within them as many (node, head) rows as fit the
+    budget, scaled to all B*N*Hq rows. Masks and the acceptance walk run on
+    the whole batch. Without ``steps``: as many steps as fit in ``budget_s``
+    (at most ``max_steps``). With ``steps``: ``warmup`` untimed steps, then
+    exactly ``steps`` timed ones. Returns (seconds per step, sample text, cores)."""
     import oracle
     w = inp.w
     cores = threads or len(os.sched_getaffinity(0))
     oracle.set_threads(cores)
-    q, K, V = _oracle_inputs(inp)
+    nseq = min(w.B, 2)
+    bs = np.linspace(0, w.B - 1, nseq).astype(np.int64)
+    q, K, V = _oracle_inputs(inp, bs)
+    sl, par = inp.seq_lens[bs], inp.parent[bs]
     rows_all = w.B * w.N * w.Hq
-    # time one row first to size the sample
+    rows_pool = nseq * w.N * w.Hq
     t0 = time.perf_counter()
-    oracle.tree_attn(q, K, V, inp.seq_lens, inp.parent, rows=np.array([[0, 0, 0]]))
+    oracle.tree_attn(q, K, V, sl, par, rows=np.array([[0, 0, 0]]))
     one = max(time.perf_counter() - t0, 1e-6)
-    frac = 1.0
-    rows = None
     per_step_budget = budget_s / 2 if steps is None else budget_s / max(1, steps + warmup)
-    if one * rows_all / cores > per_step_budget:
-        nsel = max(cores, int(per_step_budget * cores / one))
-        sel = np.linspace(0, rows_all - 1, nsel).astype(np.int64)
-        rows = np.stack([sel // (w.N * w.Hq), (sel // w.Hq) % w.N, sel % w.Hq], 1)
-        frac = nsel / rows_all
-    def one_step():
-        oracle.tree_attn(q, K, V, inp.seq_lens, inp.parent, rows=rows)
+    nsel = rows_pool
+    if one * rows_pool / cores > per_step_budget:
+        nsel = max(cores, min(rows_pool, int(per_step_budget * cores / one)))
+    sel = np.linspace(0, rows_pool - 1, nsel).astype(np.int64)
+    rows = np.stack([sel // (w.N * w.Hq), (sel // w.Hq) % w.N, sel % w.Hq], 1)
+    scale = rows_all / nsel
+
+    def accept_part():
         oracle.tree_mask(inp.parent)
         oracle.spec_accept(inp.target, inp.draft, inp.tokens, inp.parent, inp.u_accept,
                            inp.u_bonus)
 
     for _ in range(warmup):
-        one_step()
+        oracle.tree_attn(q, K, V, sl, par, rows=rows)
+        accept_part()
     fixed = steps
     steps = 0
     t_attn = t_acc = 0.0
@@ -221,20 +249,18 @@ def time_oracle(inp, budget_s=15.0, max_steps=20, steps=None, warmup=0, threads=
            (fixed is None and steps < max_steps and
             (steps == 0 or time.perf_counter() - start < budget_s))):
         t0 = time.perf_counter()
-        oracle.tree_attn(q, K, V, inp.seq_lens, inp.parent, rows=rows)
+        oracle.tree_attn(q, K, V, sl, par, rows=rows)
         t1 = time.perf_counter()
-        oracle.tree_mask(inp.parent)
-        oracle.spec_accept(inp.target, inp.draft, inp.tokens, inp.parent, inp.u_accept,
-                           inp.u_bonus)
+        accept_part()
         t2 = time.perf_counter()
-        t_attn += (t1 - t0) / frac
+        t_attn += (t1 - t0) * scale
         t_acc += t2 - t1
         steps += 1
     per_step = (t_attn + t_acc) / steps
     sample = ((f"{warmup} untimed + " if warmup else "")
-              + f"{steps} timed verify step(s) of {w.name}; attention "
-              + ("all rows" if rows is None else f"{len(rows)} of {rows_all} rows, scaled")
-              + "; fp64 oracle, OpenMP")
+              + f"{steps} timed verify step(s) of {w.name}; attention on {nsel} of "
+              + f"{rows_all} (node, head) rows from {nseq} of {w.B} sequences, scaled to all "
+              + f"rows; masks and acceptance on all {w.B} sequences; fp64 oracle, OpenMP")
     return per_step, sample, cores
 
 
@@ -242,7 +268,7 @@ def run_reference(args, w, idx):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    inp = make_inputs(w, 1000 + idx)
+    inp = make_inputs(w, 1000 + idx, with_kv=False)
     per_step, sample, cores = time_oracle(inp, budget_s=90.0, steps=args.steps,
                                           warmup=args.warmup)
     value = w.B * w.N / per_step
@@ -251,8 +277,7 @@ def run_reference(args, w, idx):
         "unit": "nodes/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "N": w.N, "context": w.L, "Hq": w.Hq,
-                   "Hkv": w.Hkv, "head_dim": w.D, "vocab": w.V},
+        "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0,
@@ -261,9 +286,223 @@ def run_reference(args, w, idx):
     print(json.dumps(line), flush=True)
 
 
+def workload_config(w, page_size=None):
+    c = {"workload": w.name, "B": w.B, "N": w.N,
+         "context": w.L if w.L_hi is None else f"U[{w.L},{w.L_hi}]", "Hq": w.Hq,
+         "Hkv": w.Hkv, "head_dim": w.D, "vocab": w.V, "tree": w.tree}
+    if page_size is not None:
+        c["page_size"] = page_size
+    return c
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+
+class StepRunner:
+    """Device inputs (rotated over enough copies to exceed L2), outputs and the
+    three calls of one verify step for one workload."""
+
+    def __init__(self, sv, torch, w, inp, dev):
+        self.sv, self.torch, self.w, self.inp, self.dev = sv, torch, w, inp, dev
+        bf = w.dtype == "bf16"
+
+        def to_dev(x, as_bf16=False):
+            t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if as_bf16 else x).to(dev)
+            return t.view(torch.bfloat16) if as_bf16 else t
+
+        self.base = {
+            "q": to_dev(inp.q, bf), "k": to_dev(inp.k_cache, bf), "v": to_dev(inp.v_cache, bf),
+            "page_table": to_dev(inp.page_table), "seq_lens": to_dev(inp.seq_lens),
+            "parent": to_dev(inp.parent), "tokens": to_dev(inp.tokens),
+            "target": to_dev(inp.target), "draft": to_dev(inp.draft),
+            "u_accept": to_dev(inp.u_accept), "u_bonus": to_dev(inp.u_bonus),
+        }
+        self.step_bytes = sum(t.numel() * t.element_size() for t in self.base.values())
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.nsets = max(1, math.ceil(3 * self.l2 / self.step_bytes))
+        self.sets = [self.base] + [{k: v.clone() for k, v in self.base.items()}
+                                   for _ in range(self.nsets - 1)]
+        B, N, Hq, D = w.B, w.N, w.Hq, w.D
+        self.anc = torch.empty((B, N, 1), dtype=torch.int64, device=dev)
+        self.depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+        self.mstat = torch.empty((B,), dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.base["q"])
+        self.lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+        self.astat = torch.empty((B,), dtype=torch.int32, device=dev)
+        self.attn_ws_need = sv.tree_verify_attn_workspace_size(
+            B, N, Hq, w.Hkv, D, self.base["q"].dtype, inp.page_table.shape[1], inp.page_size)
+        self.attn_ws = torch.empty((max(self.attn_ws_need, 1),), dtype=torch.uint8, device=dev)
+        self.acc_ws_need = sv.spec_accept_workspace_size(B, N, w.V)
+        self.acc_ws = torch.empty((self.acc_ws_need,), dtype=torch.uint8, device=dev)
+        self.acc_out = {}
+        self.cap = torch.cuda.Stream(dev)
+
+    def mask_call(self, s):
+        self.sv.tree_mask_build(s["parent"], self.anc, self.depth, self.mstat)
+
+    def attn_call(self, s):
+        self.sv.tree_verify_attn(s["q"], s["k"], s["v"], s["page_table"], s["seq_lens"],
+                                 self.anc, out=self.out, lse=self.lse, workspace=self.attn_ws,
+                                 status=self.astat)
+
+    def accept_call(self, s):
+        self.sv.spec_accept(s["target"], s["draft"], s["tokens"], s["parent"], s["u_accept"],
+                            s["u_bonus"], workspace=self.acc_ws, outputs=self.acc_out)
+
+    def step(self, s):
+        self.mask_call(s)
+        self.attn_call(s)
+        self.accept_call(s)
+
+    def launches_per_step(self):
+        return 1 + 1 + (1 if self.attn_ws_need > 0 else 0) + (2 if self.acc_ws_need > 0 else 1)
+
+    def capture(self, fn, s):
+        g = self.torch.cuda.CUDAGraph()
+        with self.torch.cuda.graph(g, stream=self.cap):
+            fn(s)
+        return g
+
+    def capture_instrumented(self, s):
+        """The step graph with a timing event before, between and after its three
+        calls (events of external kind, so that replays can be timed), or None
+        where this PyTorch cannot record such events in a graph."""
+        torch = self.torch
+        try:
+            evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+        except TypeError:
+            return None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.cap):
+            evs[0].record()
+            self.mask_call(s)
+            evs[1].record()
+            self.attn_call(s)
+            evs[2].record()
+            self.accept_call(s)
+            evs[3].record()
+        return g, evs
+
+    def check(self):
+        self.torch.cuda.synchronize(self.dev)
+        assert int(self.astat.abs().sum()) == 0 and int(self.acc_out["status"].abs().sum()) == 0
+        assert int(self.mstat.abs().sum()) == 0
+        assert bool(self.torch.isfinite(self.out.float()).all())
+
+    def free(self):
+        self.sets = self.base = None
+        self.torch.cuda.synchronize(self.dev)
+        self.torch.cuda.empty_cache()
+
+
+def time_step(r: StepRunner, steps, warmup, barrier, stream, clk=None):
+    """Step time from replays of one CUDA graph per input set, and per-kernel
+    times inside the step from the instrumented capture.
+
+    Returns a dict: ``ms`` per step (plain graphs), ``in_step`` ms of the mask,
+    attention (with its split merge) and acceptance calls and their total
+    inside one instrumented step (its events sit between the kernels, so the
+    dependent-launch overlap of the plain graph is lost there), and
+    ``single_call`` ms of each call captured and replayed alone."""
+    torch = r.torch
+    for i in range(warmup):
+        r.step(r.sets[i % r.nsets])
+    barrier()
+    g_step = [r.capture(r.step, s) for s in r.sets]
+    barrier()
+    for i in range(warmup):
+        g_step[i % r.nsets].replay()
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        # keep the GPU busy until the sampler reports (nvidia-smi starts in ~0.1-0.5 s)
+        t_soak = time.perf_counter()
+        i = 0
+        n0 = len(clk.lines)
+        while (len(clk.lines) < n0 + 3 and time.perf_counter() - t_soak < 5.0) or i < warmup:
+            g_step[i % r.nsets].replay()
+            i += 1
+            if i % 16 == 0:
+                torch.cuda.synchronize(r.dev)
+        barrier()
+    t_start.record(stream)
+    for i in range(steps):
+        g_step[i % r.nsets].replay()
+    t_end.record(stream)
+    barrier()
+    ms = t_start.elapsed_time(t_end) / steps
+    res = {"ms": ms}
+    # per-kernel times inside the step
+    inst = [r.capture_instrumented(s) for s in r.sets]
+    if inst[0] is not None:
+        acc = np.zeros(4)
+        for i in range(steps):
+            g, evs = inst[i % r.nsets]
+            g.replay()
+            torch.cuda.synchronize(r.dev)
+            acc += [evs[0].elapsed_time(evs[1]), evs[1].elapsed_time(evs[2]),
+                    evs[2].elapsed_time(evs[3]), evs[0].elapsed_time(evs[3])]
+        acc /= steps
+        res["in_step"] = {"mask_ms": acc[0], "attn_ms": acc[1], "accept_ms": acc[2],
+                          "total_ms": acc[3],
+                          "method": "timing events captured between the calls of the step "
+                                    "graph; replayed per input set"}
+    # each call captured alone, replayed back to back with events around it
+    single = {}
+    for name, fn in (("mask", r.mask_call), ("attn", r.attn_call), ("accept", r.accept_call)):
+        gs = [r.capture(fn, s) for s in r.sets]
+        barrier()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            evs[i][0].record(stream)
+            gs[i % r.nsets].replay()
+            evs[i][1].record(stream)
+        barrier()
+        single[name + "_ms"] = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    res["single_call"] = single
+    if "in_step" not in res:
+        res["in_step"] = {"mask_ms": single["mask_ms"], "attn_ms": single["attn_ms"],
+                          "accept_ms": single["accept_ms"],
+                          "total_ms": single["mask_ms"] + single["attn_ms"] + single["accept_ms"],
+                          "method": "single-call graphs (this PyTorch records no timing "
+                                    "events inside a graph)"}
+    g_step.clear()
+    return res
+
+
+def workload_summary(r: StepRunner, t: dict, peak, clocks):
+    """Attention and acceptance times of one workload with their roofline shares."""
+    w, inp = r.w, r.inp
+    nb = algorithmic_bytes(w, inp.seq_lens, inp.parent)
+    path = r.acc_out["path"].cpu().numpy()
+    alen = r.acc_out["accept_len"].cpu().numpy()
+    acc_bytes = walk_bytes(w, inp.parent, path, alen)
+    nodes = visited_nodes(alen)
+    ins = t["in_step"]
+    attn_gbs = nb["attn_bytes"] / (ins["attn_ms"] / 1e3) / 1e9
+    acc_gbs = acc_bytes / (ins["accept_ms"] / 1e3) / 1e9
+    return {
+        "config": workload_config(w, inp.page_size),
+        "step_us": t["ms"] * 1e3,
+        "nodes_per_s": w.B * w.N / (t["ms"] / 1e3),
+        "attn_us": ins["attn_ms"] * 1e3,
+        "attn_bytes": nb["attn_bytes"],
+        "attn_frac_of_hbm": attn_gbs / peak,
+        "accept_us": ins["accept_ms"] * 1e3,
+        "accept_bytes": acc_bytes,
+        "accept_frac_of_hbm": acc_gbs / peak,
+        "accept_bytes_all_rows": nb["accept_bytes"],
+        "accept_visited_nodes": nodes,
+        "accept_us_per_visited_node": ins["accept_ms"] * 1e3 / nodes,
+        "accept_us_per_visited_node_per_sequence": ins["accept_ms"] * 1e3 * w.B / nodes,
+        "mask_us": ins["mask_ms"] * 1e3,
+        "in_step_total_us": ins["total_ms"] * 1e3,
+        "single_call_us": {k.replace("_ms", ""): v * 1e3 for k, v in t["single_call"].items()},
+        "clocks": clocks,
+    }
+
 
 def run_ours(args, w, idx):
     import torch
@@ -279,168 +518,106 @@ def run_ours(args, w, idx):
     _build.build()
     import speculative_decoding_tree_03_gb300 as sv
 
-    seed = 1000 + idx
-    inp = make_inputs(w, seed)
-    nb = algorithmic_bytes(w, inp.seq_lens, inp.parent)
     dev = torch.device("cuda", local)
-
-    def to_dev(x, bf16=False):
-        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if bf16 else x).to(dev)
-        return t.view(torch.bfloat16) if bf16 else t
-
-    bf = w.dtype == "bf16"
-    base = {
-        "q": to_dev(inp.q, bf), "k": to_dev(inp.k_cache, bf), "v": to_dev(inp.v_cache, bf),
-        "page_table": to_dev(inp.page_table), "seq_lens": to_dev(inp.seq_lens),
-        "parent": to_dev(inp.parent), "tokens": to_dev(inp.tokens),
-        "target": to_dev(inp.target), "draft": to_dev(inp.draft),
-        "u_accept": to_dev(inp.u_accept), "u_bonus": to_dev(inp.u_bonus),
-    }
-    step_bytes = sum(t.numel() * t.element_size() for t in base.values())
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    nsets = max(1, math.ceil(3 * l2 / step_bytes))
-    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
-
-    B, N, Hq, D = w.B, w.N, w.Hq, w.D
     stream = torch.cuda.current_stream(dev)
-    anc = torch.empty((B, N, 1), dtype=torch.int64, device=dev)
-    depth = torch.empty((B, N), dtype=torch.int32, device=dev)
-    mstat = torch.empty((B,), dtype=torch.int32, device=dev)
-    out = torch.empty_like(base["q"])
-    lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
-    astat = torch.empty((B,), dtype=torch.int32, device=dev)
-    ws_need = sv.tree_verify_attn_workspace_size(B, N, Hq, w.Hkv, D, base["q"].dtype,
-                                                 inp.page_table.shape[1], inp.page_size)
-    attn_ws = torch.empty((max(ws_need, 1),), dtype=torch.uint8, device=dev)
-    acc_ws = torch.empty((sv.spec_accept_workspace_size(B, N, w.V),), dtype=torch.uint8,
-                         device=dev)
-    acc_out = {}
-
-    def mask_call(s):
-        sv.tree_mask_build(s["parent"], anc, depth, mstat)
-
-    def attn_call(s):
-        sv.tree_verify_attn(s["q"], s["k"], s["v"], s["page_table"], s["seq_lens"], anc,
-                            out=out, lse=lse, workspace=attn_ws, status=astat)
-
-    def accept_call(s):
-        sv.spec_accept(s["target"], s["draft"], s["tokens"], s["parent"], s["u_accept"],
-                       s["u_bonus"], workspace=acc_ws, outputs=acc_out)
-
-    def step(s):
-        mask_call(s)
-        attn_call(s)
-        accept_call(s)
+    peak, peak_kind = measured_peaks()
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for i in range(args.warmup):
-        step(sets[i % nsets])
-    barrier()
-    # Each step is issued as one CUDA graph (as a serving loop replays its
-    # decode step); per-kernel times come from graphs of the single calls.
-    cap = torch.cuda.Stream(dev)
+    # ---- the other workloads first (small, freed afterwards), rank 0 only
+    per_workload = {}
+    if not args.no_per_workload and rank == 0:
+        for j, w2 in enumerate(WORKLOADS):
+            if w2.name == w.name:
+                continue
+            inp2 = make_inputs(w2, 1000 + j)
+            r2 = StepRunner(sv, torch, w2, inp2, dev)
+            with ClockSampler(local) as clk2:
+                t2 = time_step(r2, args.steps, args.warmup, lambda: torch.cuda.synchronize(dev),
+                               stream, clk2)
+                # a few more samples under load
+                t_tail = time.perf_counter()
+                n0 = len(clk2.lines)
+                while len(clk2.lines) < n0 + 2 and time.perf_counter() - t_tail < 2.0:
+                    for _ in range(16):
+                        r2.step(r2.sets[0])
+                    torch.cuda.synchronize(dev)
+            r2.check()
+            per_workload[w2.name] = workload_summary(r2, t2, peak, clk2.summary())
+            r2.free()
+            del r2, inp2
 
-    def capture(fn, s):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            fn(s)
-        return g
+    seed = 1000 + idx
+    inp = make_inputs(w, seed)
+    nb = algorithmic_bytes(w, inp.seq_lens, inp.parent)
+    r = StepRunner(sv, torch, w, inp, dev)
+    B, N, Hq, D = w.B, w.N, w.Hq, w.D
+    bf = w.dtype == "bf16"
 
-    g_step = [capture(step, s) for s in sets]
-    g_mask = [capture(mask_call, s) for s in sets]
-    g_attn = [capture(attn_call, s) for s in sets]
-    g_acc = [capture(accept_call, s) for s in sets]
-    barrier()
-    for i in range(args.warmup):
-        g_step[i % nsets].replay()
-    barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        # keep the GPU busy until the sampler reports (nvidia-smi starts in ~0.1-0.5 s)
-        t_soak = time.perf_counter()
-        i = 0
-        while (len(clk.lines) < 3 and time.perf_counter() - t_soak < 5.0) or i < args.warmup:
-            g_step[i % nsets].replay()
-            i += 1
-            if i % 64 == 0:
-                torch.cuda.synchronize(dev)
-        barrier()
-        t_start.record(stream)
-        for i in range(args.steps):
-            g_step[i % nsets].replay()
-        t_end.record(stream)
-        barrier()
-        for i in range(args.steps):
-            k = i % nsets
-            g_mask[k].replay()
-            evs[i][0].record(stream)
-            g_attn[k].replay()
-            evs[i][1].record(stream)
-            g_acc[k].replay()
-            evs[i][2].record(stream)
-        barrier()
-        # a few more samples under load after the timed region
+        t = time_step(r, args.steps, args.warmup, barrier, stream, clk)
         t_tail = time.perf_counter()
         n0 = len(clk.lines)
-        i = 0
         while len(clk.lines) < n0 + 2 and time.perf_counter() - t_tail < 2.0:
-            g_step[i % nsets].replay()
-            i += 1
-            if i % 64 == 0:
-                torch.cuda.synchronize(dev)
-        torch.cuda.synchronize(dev)
-    ms_local = t_start.elapsed_time(t_end) / args.steps
+            r.step(r.sets[0])
+            torch.cuda.synchronize(dev)
+    r.check()
+    ms_local = t["ms"]
+    ins = t["in_step"]
 
     # launch-amortised: 100 consecutive steps (rotating input sets) captured
     # as one CUDA graph, replayed after one warm-up replay
     g100 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g100, stream=cap):
+    with torch.cuda.graph(g100, stream=r.cap):
         for i in range(100):
-            step(sets[i % nsets])
+            r.step(r.sets[i % r.nsets])
     g100.replay()
     barrier()
     h0 = torch.cuda.Event(enable_timing=True)
     h1 = torch.cuda.Event(enable_timing=True)
+    reps = 3 if ms_local < 1.0 else 1
     h0.record(stream)
-    for _ in range(3):
+    for _ in range(reps):
         g100.replay()
     h1.record(stream)
     barrier()
-    ms100_local = h0.elapsed_time(h1) / 300
-    attn_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    acc_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    ms100_local = h0.elapsed_time(h1) / (100 * reps)
+    del g100
+
+    def timed_calls(fn, name_out=None):
+        """ms per call of ``fn`` captured alone per input set, replayed K times."""
+        fn(r.sets[0])
+        barrier()
+        graphs = [r.capture(fn, s) for s in r.sets]
+        barrier()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            graphs[i % r.nsets].replay()
+            evs[i][1].record(stream)
+        barrier()
+        return sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
 
     # ---- KV commit of the accepted path (one layer), timed on its own after
     # the step: it rewrites tree rows of the cache in place, which later
     # replays of the step read as ordinary (finite) K/V
     commit_out = {}
+    acc_out = r.acc_out
 
     def commit_call(s):
         sv.kv_commit(s["k"], s["v"], s["page_table"], s["seq_lens"], acc_out["path"],
                      acc_out["accept_len"], outputs=commit_out)
 
-    commit_call(sets[0])
-    barrier()
-    g_commit = [capture(commit_call, s) for s in sets]
-    barrier()
-    cevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        cevs[i][0].record(stream)
-        g_commit[i % nsets].replay()
-        cevs[i][1].record(stream)
-    barrier()
-    commit_ms = sum(e[0].elapsed_time(e[1]) for e in cevs) / args.steps
+    commit_ms = timed_calls(commit_call)
     assert int(commit_out["status"].abs().sum()) == 0
 
     # ---- the target-only acceptance variants on the same inputs, each timed
     # on its own (greedy argmax matching; one-hot candidate sampling)
-    var_out = {"greedy": {}, "onehot": {}}
+    var_out = {"greedy": {}, "onehot": {}, "bf16": {}, "greedy_bf16": {}, "onehot_bf16": {}}
 
     def greedy_call(s):
         sv.spec_accept_greedy(s["target"], s["tokens"], s["parent"], outputs=var_out["greedy"])
@@ -454,31 +631,28 @@ def run_ours(args, w, idx):
     e2k, e2rounds = 8, 6
     e2gen = torch.Generator(device=dev)
     e2gen.manual_seed(1234)
-    e2rows = [torch.randn((B, 1 if r == 0 else e2k, w.V), generator=e2gen, device=dev) * 2.0
-              for r in range(e2rounds)]
+    e2rows = [torch.randn((B, 1 if rr == 0 else e2k, w.V), generator=e2gen, device=dev) * 2.0
+              for rr in range(e2rounds)]
     e2roots = torch.zeros((B,), dtype=torch.int32, device=dev)
     e2cap = 1 + e2k + (e2rounds - 1) * e2k * e2k
     e2pool = sv.eagle2_pool(e2roots, e2cap)
     e2f0 = torch.zeros((B, 1), dtype=torch.int32, device=dev)
     e2fr = [torch.empty((B, e2k), dtype=torch.int32, device=dev) for _ in range(e2rounds)]
+    e2out = {}
 
     def eagle2_call(s):
         sv.eagle2_init(e2pool, e2roots)
         f = e2f0
-        for r in range(e2rounds):
-            f = sv.eagle2_expand(e2pool, e2rows[r], f, e2k, next_frontier=e2fr[r])
+        for rr in range(e2rounds):
+            f = sv.eagle2_expand(e2pool, e2rows[rr], f, e2k, next_frontier=e2fr[rr])
         return sv.eagle2_finalize(e2pool, N, outputs=e2out)
 
     # the walk on bf16 copies of the logits (one input set: larger than L2)
-    bf_logits = {k: sets[0][k].to(torch.bfloat16) for k in ("target", "draft")}
-    var_out["bf16"] = {}
+    bf_logits = {k: r.sets[0][k].to(torch.bfloat16) for k in ("target", "draft")}
 
     def bf16_call(s):
         sv.spec_accept(bf_logits["target"], bf_logits["draft"], s["tokens"], s["parent"],
                        s["u_accept"], s["u_bonus"], outputs=var_out["bf16"])
-
-    var_out["greedy_bf16"] = {}
-    var_out["onehot_bf16"] = {}
 
     def greedy_bf16_call(s):
         sv.spec_accept_greedy(bf_logits["target"], s["tokens"], s["parent"],
@@ -488,40 +662,29 @@ def run_ours(args, w, idx):
         sv.spec_accept_onehot(bf_logits["target"], s["tokens"], s["parent"], s["u_accept"],
                               s["u_bonus"], outputs=var_out["onehot_bf16"])
 
-    e2out = {}
     var_ms = {}
     for name, fn in (("greedy", greedy_call), ("onehot", onehot_call), ("eagle2", eagle2_call),
                      ("bf16", bf16_call), ("greedy_bf16", greedy_bf16_call),
                      ("onehot_bf16", onehot_bf16_call)):
-        fn(sets[0])
-        barrier()
-        graphs = [capture(fn, s) for s in sets]
-        barrier()
-        vev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
-               for _ in range(args.steps)]
-        for i in range(args.steps):
-            vev[i][0].record(stream)
-            graphs[i % nsets].replay()
-            vev[i][1].record(stream)
-        barrier()
-        var_ms[name] = sum(e[0].elapsed_time(e[1]) for e in vev) / args.steps
+        var_ms[name] = timed_calls(fn)
         if name != "eagle2":
             assert int(var_out[name]["status"].abs().sum()) == 0
     assert int(e2out["n_out"].min()) == min(N, e2cap)
+    del e2rows, bf_logits
 
     def rmax(x):
         if world == 1:
             return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        tt = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
 
     def rsum(x):
         if world == 1:
             return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
+        tt = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.SUM)
+        return float(tt.item())
 
     ms, value = aggregate(ms_local, B * N, world, rmax, rsum)
     ms100 = rmax(ms100_local)
@@ -531,6 +694,7 @@ def run_ours(args, w, idx):
     # into one of two device buffers whose slices the step's tensors view; a
     # side stream copies step i + 1 while step i runs (double buffering), and
     # every step's outputs come back to pinned host memory.
+    base = r.base
     offs, total = {}, 0
     for k, v in base.items():
         nbytes = v.numel() * v.element_size()
@@ -539,15 +703,19 @@ def run_ours(args, w, idx):
     host_in = torch.empty((total,), dtype=torch.uint8).pin_memory()
     for k, (o, nbytes, _, _) in offs.items():
         host_in[o:o + nbytes].copy_(base[k].reshape(-1).view(torch.uint8).cpu())
+    # the resident input copies are no longer needed: make room for the two
+    # end-to-end device buffers
+    r.sets = [r.base]
+    torch.cuda.empty_cache()
     dbufs = [torch.empty((total,), dtype=torch.uint8, device=dev) for _ in range(2)]
     dsets = [{k: buf[o:o + nbytes].view(dt).view(shape)
               for k, (o, nbytes, shape, dt) in offs.items()} for buf in dbufs]
     h2d = sum(nbytes for _, nbytes, _, _ in offs.values())
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
     res_h = {k: torch.empty((B, N) if k in ("path", "out_tokens") else (B,),
                             dtype=torch.int32).pin_memory()
              for k in ("accept_len", "path", "out_tokens", "status")}
-    d2h = out_h.numel() * out_h.element_size() + sum(t.numel() * 4 for t in res_h.values())
+    d2h = out_h.numel() * out_h.element_size() + sum(tt.numel() * 4 for tt in res_h.values())
     copy_stream = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event() for _ in dbufs]
     used = [torch.cuda.Event() for _ in dbufs]
@@ -568,9 +736,9 @@ def run_ours(args, w, idx):
                 issue_copy(i + 1)
             j = i % len(dbufs)
             stream.wait_event(copied[j])
-            step(dsets[j])
+            r.step(dsets[j])
             used[j].record(stream)
-            out_h.copy_(out, non_blocking=True)
+            out_h.copy_(r.out, non_blocking=True)
             for k in res_h:
                 res_h[k].copy_(acc_out[k], non_blocking=True)
 
@@ -584,23 +752,18 @@ def run_ours(args, w, idx):
     barrier()
     e2e_ms = rmax(e0.elapsed_time(e1) / args.steps)
     e2e_value = rsum(B * N) / (e2e_ms / 1e3)
-
-    # ---- checks that the timed work produced valid results
-    torch.cuda.synchronize(dev)
-    assert int(astat.abs().sum()) == 0 and int(acc_out["status"].abs().sum()) == 0
-    assert bool(torch.isfinite(out.float()).all())
+    r.check()
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    peak, peak_kind = measured_peaks()
+    head = workload_summary(r, t, peak, clk.summary())
+    attn_ms = ins["attn_ms"]
+    acc_ms = ins["accept_ms"]
     attn_gbs = nb["attn_bytes"] / (attn_ms / 1e3) / 1e9
-    # the walk reads only the rows of the nodes it visits (every input set is a
-    # copy of the same data, so the last walk stands for all)
-    acc_bytes = walk_bytes(w, inp.parent, acc_out["path"].cpu().numpy(),
-                           acc_out["accept_len"].cpu().numpy())
+    acc_bytes = head["accept_bytes"]
     acc_gbs = acc_bytes / (acc_ms / 1e3) / 1e9
     path_h = acc_out["path"].cpu().numpy()
     alen_h = acc_out["accept_len"].cpu().numpy()
@@ -632,8 +795,6 @@ def run_ours(args, w, idx):
             "mean_accept_len": float(vl.mean()),
             "bytes_note": "target rows of the visited nodes"}
         assert (vp[:, 0] == 0).all()
-    acc_ws_need = sv.spec_accept_workspace_size(B, N, w.V)
-    launches_per_step = 1 + 1 + (1 if ws_need > 0 else 0) + (2 if acc_ws_need > 0 else 1)
     line = {
         "metric": "verified tree-nodes/s per attn layer",
         "value": value,
@@ -648,11 +809,9 @@ def run_ours(args, w, idx):
         "dtype": "bf16" if bf else "f32",
         "data": "synthetic",
         "config": {
-            "workload": w.name, "B": B, "N": N, "context": w.L if w.L_hi is None else
-            f"U[{w.L},{w.L_hi}]", "Hq": Hq, "Hkv": w.Hkv, "head_dim": D, "vocab": w.V,
-            "page_size": inp.page_size, "tree": w.tree,
-            "l2": f"inputs rotate over {nsets} copies ({nsets * step_bytes / 1e6:.0f} MB > "
-                  f"L2 {l2 / 1e6:.0f} MB)",
+            **workload_config(w, inp.page_size),
+            "l2": f"inputs rotate over {r.nsets} copies ({r.nsets * r.step_bytes / 1e6:.0f} MB "
+                  f"> L2 {r.l2 / 1e6:.0f} MB)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "launch": "one CUDA graph per step (masks, attention, acceptance)",
             "e2e_copies": "one packed pinned host-to-device copy per step, issued one step "
@@ -661,14 +820,28 @@ def run_ours(args, w, idx):
         "accept_steps_per_s": rsum(B) / (ms / 1e3),
         "graph_100_steps": {"ms_per_step": ms100, "value": rsum(B * N) / (ms100 / 1e3),
                             "note": "100 steps captured as one CUDA graph"},
+        "in_step": {"mask_us": ins["mask_ms"] * 1e3, "attn_us": attn_ms * 1e3,
+                    "accept_us": acc_ms * 1e3, "total_us": ins["total_ms"] * 1e3,
+                    "step_us": ms * 1e3, "method": ins["method"],
+                    "note": "the plain step graph launches its kernels with programmatic "
+                            "dependent launch; events between them serialise the calls, so "
+                            "total_us is at least step_us"},
         "kernels": {
             "tree_verify_attn": {"ms": attn_ms, "bytes": nb["attn_bytes"], "gbs": attn_gbs,
-                                 "frac_of_hbm": attn_gbs / peak},
+                                 "frac_of_hbm": attn_gbs / peak,
+                                 "single_call_ms": t["single_call"]["attn_ms"]},
             "spec_accept": {"ms": acc_ms, "bytes": acc_bytes, "gbs": acc_gbs,
                             "frac_of_hbm": acc_gbs / peak,
+                            "single_call_ms": t["single_call"]["accept_ms"],
+                            "visited_nodes": head["accept_visited_nodes"],
+                            "us_per_visited_node": head["accept_us_per_visited_node"],
+                            "us_per_visited_node_per_sequence":
+                                head["accept_us_per_visited_node_per_sequence"],
                             "bytes_all_rows": nb["accept_bytes"],
                             "bytes_note": "rows of the visited nodes; bytes_all_rows counts "
                                           "every row a walk could test"},
+            "tree_mask_build": {"ms": ins["mask_ms"],
+                                "single_call_ms": t["single_call"]["mask_ms"]},
             "kv_commit": {"ms": commit_ms, "bytes": commit_bytes, "gbs": commit_gbs,
                           "frac_of_hbm": commit_gbs / peak, "rows_moved": rows_moved,
                           "bytes_note": "K and V rows of accepted nodes not yet in place, "
@@ -684,23 +857,18 @@ def run_ours(args, w, idx):
             "unit": "GB/s",
             "frac": attn_gbs / peak,
             "traffic": committed_traffic(w.name, "speculative_decoding_tree_03_gb300/csrc/attn_tc.cu"),
+            "duration_from": "CUDA events around the attention call inside the step graph",
         },
+        "per_workload": per_workload,
         "e2e": {"value": e2e_value, "unit": "nodes/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": r.launches_per_step() * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
         per_step, sample, cores = time_oracle(inp)
         line["cpu_baseline"] = {"value": B * N / per_step, "unit": "nodes/s", "cores": cores,
                                 "kind": "oracle", "sample": sample}
-        if idx <= 2:
-            # the small workloads are also timed on one core
-            import oracle
-            per1, sample1, _ = time_oracle(inp, budget_s=10.0, max_steps=5, threads=1)
-            oracle.set_threads(cores)
-            line["cpu_baseline"]["single_thread"] = {"value": B * N / per1, "unit": "nodes/s",
-                                                     "cores": 1, "sample": sample1}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -714,6 +882,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -327,64 +327,44 @@ def page_layout(w: Workload, seed: int, seq_lens: np.ndarray):
     return ps, P, table
 
 
-def _fill_kv_chunk(args):
-    (shm_k, shm_v, shape, dt, w, seed, b, g, T, rows_pages, slots) = args
-    from multiprocessing import shared_memory
-    sk = shared_memory.SharedMemory(name=shm_k)
-    sv = shared_memory.SharedMemory(name=shm_v)
-    try:
-        kc = np.ndarray(shape, dtype=dt, buffer=sk.buf)
-        vc = np.ndarray(shape, dtype=dt, buffer=sv.buf)
-        k, v = logical_kv(w, seed, b, g, T)
-        kc[rows_pages, slots, g, :] = k
-        vc[rows_pages, slots, g, :] = v
-        del kc, vc
-    finally:
-        sk.close()
-        sv.close()
-    return b, g
+def _kv_chunk(args):
+    w, seed, b, g, T = args
+    return b, g, logical_kv(w, seed, b, g, T)
 
 
 def build_kv_cache(w: Workload, seed: int, seq_lens, page_size, num_pages, table, workers: int = 0):
-    """Paged K and V caches [num_pages, page_size, Hkv, D] (float32 or bf16 bits)."""
+    """Paged K and V caches [num_pages, page_size, Hkv, D] (float32 or bf16 bits).
+
+    Large caches draw their (sequence, KV head) chunks in a pool of spawned
+    processes; this process scatters each returned chunk into the pages."""
     dt = np.uint16 if w.dtype == "bf16" else np.float32
     shape = (num_pages, page_size, w.Hkv, w.D)
     T_all = seq_lens.astype(np.int64) + w.N
-    jobs = []
-    for b in range(w.B):
-        T = int(T_all[b])
-        t = np.arange(T)
-        pages = table[b, t // page_size]
-        slots = t % page_size
-        for g in range(w.Hkv):
-            jobs.append((b, g, T, pages, slots))
+    kc = np.zeros(shape, dtype=dt)
+    vc = np.zeros(shape, dtype=dt)
+    kflat = kc.reshape(num_pages * page_size, w.Hkv, w.D)
+    vflat = vc.reshape(num_pages * page_size, w.Hkv, w.D)
+    slot_of = {}
+
+    def slots(b):
+        if b not in slot_of:
+            t = np.arange(int(T_all[b]))
+            slot_of[b] = table[b, t // page_size].astype(np.int64) * page_size + t % page_size
+        return slot_of[b]
+
+    jobs = [(w, seed, b, g, int(T_all[b])) for b in range(w.B) for g in range(w.Hkv)]
     nbytes = int(np.prod(shape)) * np.dtype(dt).itemsize
     if workers <= 1 or nbytes < (256 << 20):
-        kc = np.zeros(shape, dtype=dt)
-        vc = np.zeros(shape, dtype=dt)
-        for (b, g, T, pages, slots) in jobs:
-            k, v = logical_kv(w, seed, b, g, T)
-            kc[pages, slots, g, :] = k
-            vc[pages, slots, g, :] = v
+        results = map(_kv_chunk, jobs)
+        for b, g, (k, v) in results:
+            kflat[slots(b), g, :] = k
+            vflat[slots(b), g, :] = v
         return kc, vc
     import multiprocessing as mp
-    from multiprocessing import shared_memory
-    sk = shared_memory.SharedMemory(create=True, size=nbytes)
-    sv = shared_memory.SharedMemory(create=True, size=nbytes)
-    try:
-        np.ndarray(shape, dtype=dt, buffer=sk.buf).fill(0)
-        np.ndarray(shape, dtype=dt, buffer=sv.buf).fill(0)
-        ctx = mp.get_context("spawn")
-        args = [(sk.name, sv.name, shape, dt, w, seed, b, g, T, pages, slots)
-                for (b, g, T, pages, slots) in jobs]
-        with ctx.Pool(workers) as pool:
-            for _ in pool.imap_unordered(_fill_kv_chunk, args, chunksize=4):
-                pass
-        kc = np.ndarray(shape, dtype=dt, buffer=sk.buf).copy()
-        vc = np.ndarray(shape, dtype=dt, buffer=sv.buf).copy()
-    finally:
-        sk.close(); sk.unlink()
-        sv.close(); sv.unlink()
+    with mp.get_context("spawn").Pool(workers) as pool:
+        for b, g, (k, v) in pool.imap_unordered(_kv_chunk, jobs, chunksize=2):
+            kflat[slots(b), g, :] = k
+            vflat[slots(b), g, :] = v
     return kc, vc
 
 
@@ -419,29 +399,46 @@ def _logits_rows(w, seed, b, keys):
     return t, d
 
 
+def _sequence_job(args):
+    """Tree and (optionally) logits rows of one sequence."""
+    w, seed, b, with_logits = args
+    parent, keys, tokens = make_tree(w, seed, b)
+    rows = _logits_rows(w, seed, b, keys) if with_logits else None
+    return parent, keys, tokens, rows
+
+
 def make_inputs(w: Workload, seed: int, with_kv: bool = True, with_logits: bool = True,
                 workers: Optional[int] = None) -> Inputs:
-    """All inputs of one workload, as host arrays."""
+    """All inputs of one workload, as host arrays. Large batches build their
+    sequences' trees and logits in a pool of spawned processes; every value
+    comes from its own keyed stream, so the result does not depend on it."""
     if workers is None:
         workers = min(16, os.cpu_count() or 1)
     seq_lens = prefix_lengths(w, seed)
     parent = np.empty((w.B, w.N), dtype=np.int32)
     tokens = np.empty((w.B, w.N), dtype=np.int32)
     keys = np.empty((w.B, w.N), dtype=np.int64)
-    for b in range(w.B):
-        parent[b], keys[b], tokens[b] = make_tree(w, seed, b)
+    tgt = dft = None
+    if with_logits:
+        tgt = np.empty((w.B, w.N, w.V), dtype=np.float32)
+        dft = np.empty((w.B, w.N, w.V), dtype=np.float32)
+    jobs = [(w, seed, b, with_logits) for b in range(w.B)]
+    if workers > 1 and w.B >= 8 and w.N * w.V >= (1 << 20):
+        import multiprocessing as mp
+        with mp.get_context("spawn").Pool(min(workers, w.B)) as pool:
+            results = pool.map(_sequence_job, jobs, chunksize=1)
+    else:
+        results = map(_sequence_job, jobs)
+    for b, (pa, ke, to, rows) in enumerate(results):
+        parent[b], keys[b], tokens[b] = pa, ke, to
+        if with_logits:
+            tgt[b], dft[b] = rows
     bf = w.dtype == "bf16"
     q = np.stack([normal_chunk(seed, (TAG_Q, b), (w.N, w.Hq, w.D), bf) for b in range(w.B)])
     ps, P, table = page_layout(w, seed, seq_lens)
     kc = vc = None
     if with_kv:
         kc, vc = build_kv_cache(w, seed, seq_lens, ps, P, table, workers=workers)
-    tgt = dft = None
-    if with_logits:
-        tgt = np.empty((w.B, w.N, w.V), dtype=np.float32)
-        dft = np.empty((w.B, w.N, w.V), dtype=np.float32)
-        for b in range(w.B):
-            tgt[b], dft[b] = _logits_rows(w, seed, b, keys[b])
     u_acc = np.stack([rng(seed, TAG_UACC, b).random(w.N, dtype=np.float32) for b in range(w.B)])
     u_bon = np.array([rng(seed, TAG_UBON, b).random(dtype=np.float32) for b in range(w.B)],
                      dtype=np.float32)

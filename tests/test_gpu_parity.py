@@ -1,7 +1,8 @@
 """GPU parity: every kernel through the C ABI against the fp64 oracle.
 
 Masks, accepted paths, accepted lengths and tokens must match bit for bit
-(near ties aside, see gpu_common); attention outputs within max-abs 2e-2
+(near ties aside, under the error model in gpu_common); acceptance ratios
+within 1e-5 relative at first tests; attention outputs within max-abs 2e-2
 (bf16 inputs and output) or 1e-5 (fp32), lse within 2e-3 (bf16) or 1e-5.
 """
 
@@ -13,8 +14,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_common import (bf16_tensor, compare_accept, compare_ratio, device_inputs,
-                        oracle_attention, as_f32)
+from gpu_common import (bf16_tensor, compare_accept, device_inputs, oracle_attention,
+                        as_f32)
 from synth import WORKLOADS, make_inputs, binary_tree_parent, chain_parent
 from synth.gen import Workload, f32_to_bf16_bits, bf16_bits_to_f32
 
@@ -263,8 +264,13 @@ def test_attention_workloads_full(sv, idx):
 
 def test_attention_serving_70b_sampled(sv):
     """Full-size 70B-shaped workload (8.6 GB paged cache) in the launch shape
-    the benchmark times; the oracle recomputes sampled rows one by one."""
+    the benchmark times. Every (sequence, KV head) is checked on six of its
+    N*G = 248 query rows: the first and last row of each 128-row half (rows
+    0, 127, 128, 247) and one more row drawn in each half. Every row merges
+    all KV chunks, so every chunk boundary of every sequence is crossed. The
+    oracle recomputes the rows one by one, eight sequences at a time."""
     w = WORKLOADS[4]
+    G = w.Hq // w.Hkv
     inp = make_inputs(w, 1004, with_kv=True, with_logits=False)
     d = device_inputs(inp)
     anc, _, _ = sv.tree_mask_build(d["parent"])
@@ -272,20 +278,31 @@ def test_attention_serving_70b_sampled(sv):
                                            d["seq_lens"], anc)
     torch.cuda.synchronize()
     assert (_np(status) == 0).all()
-    rng = np.random.default_rng(7)
-    bs = [0, 33, 63]
-    rows = []
-    for n in range(len(bs)):
-        for i in (0, 1, 14, 30):
-            for h in rng.choice(w.Hq, size=6, replace=False):
-                rows.append((n, i, int(h)))
-    o_ref, l_ref = oracle_attention(inp, bs=bs, rows=np.array(rows))
     out = _np(out.float())
     lse = _np(lse)
-    for r, (n, i, h) in enumerate(rows):
-        b = bs[n]
-        assert np.abs(out[b, i, h] - o_ref[r]).max() <= BF16_OUT_TOL
-        assert abs(lse[b, i, h] - l_ref[r]) <= BF16_LSE_TOL
+    del d
+    rng = np.random.default_rng(7)
+    M = w.N * G
+    worst_o = worst_l = 0.0
+    checked = 0
+    for b0 in range(0, w.B, 8):
+        bs = list(range(b0, min(w.B, b0 + 8)))
+        rows = []
+        for n in range(len(bs)):
+            for g in range(w.Hkv):
+                picks = [0, 127, 128, M - 1, int(rng.integers(1, 127)),
+                         int(rng.integers(129, M - 1))]
+                for R in picks:
+                    rows.append((n, R // G, g * G + R % G))
+        o_ref, l_ref = oracle_attention(inp, bs=bs, rows=np.array(rows))
+        for r, (n, i, h) in enumerate(rows):
+            b = bs[n]
+            worst_o = max(worst_o, float(np.abs(out[b, i, h] - o_ref[r]).max()))
+            worst_l = max(worst_l, abs(float(lse[b, i, h]) - float(l_ref[r])))
+        checked += len(rows)
+    print(f"serving_70b: {checked} rows, max|out-ref| {worst_o:.3g} max|lse-ref| {worst_l:.3g}")
+    assert checked == w.B * w.Hkv * 6
+    assert worst_o <= BF16_OUT_TOL and worst_l <= BF16_LSE_TOL
 
 
 # ---------------------------------------------------------------------------
@@ -314,9 +331,8 @@ def test_accept_workloads(sv, idx):
     gpu = _accept_gpu(sv, arrs)
     orc = oracle.spec_accept(**arrs)
     stats = compare_accept(gpu, arrs, orc)
-    rerr = compare_ratio(gpu["ratio"], orc)
-    print(f"{w.name}: {stats} max ratio err {rerr:.3g} accept_len {gpu['accept_len'][:8]}")
-    assert rerr < 1e-3
+    print(f"{w.name}: {stats} accept_len {gpu['accept_len'][:8]}")
+    assert stats["ratio_rel_err_first_tests"] <= 1e-5
 
 
 def _synthetic_accept(seed, B, N, V, parent, sigma=3.0, noise=1.0, iid_children=True):
@@ -450,7 +466,7 @@ def test_accept_chi_square_on_gpu(sv):
     _, pval = chisquare(counts, pp * B)
     assert pval > 1e-4, pval
     orc = oracle.spec_accept(**arrs)
-    compare_accept(gpu, arrs, orc, max_flag_frac=1e-3)
+    compare_accept(gpu, arrs, orc, max_tie_frac=1e-3)
 
 
 # ---------------------------------------------------------------------------
