@@ -204,8 +204,13 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
  *     (svf_spec_accept_workspace_size(B, N, V)) exceeds 4 MiB returns
  *     SVF_ERR_SCRATCH_LIMIT without launching anything.
  *   - The first call on a device looks up that array's device address (once
- *     per device, with the device current). Make that first call before any
- *     stream capture begins.
+ *     per device and context, with the device current), and a new context
+ *     on the device (after cudaDeviceReset, say) gets a new lookup. With
+ *     lazy module loading that first call may be where the library's device
+ *     code, and with it the 4 MiB array, is loaded: it can reserve that
+ *     memory and synchronise. The guarantee of no allocation and no
+ *     implicit synchronisation holds from the second call on a device. Make
+ *     that first call before any stream capture begins.
  *   - Every call shares the one array. Calls that overlap on the GPU (on
  *     different streams, or from different host threads without ordering)
  *     race on it and corrupt each other's results; order them. Nothing in

@@ -11,6 +11,7 @@
 // per-row, per-chunk softmax statistics) lives in a fixed array that the
 // library itself defines in device memory. Every GPU that loads the library
 // holds that array until the process exits.
+#include <cuda.h>
 #include <mutex>
 
 #include "common.cuh"
@@ -19,30 +20,62 @@
 namespace svf {
 namespace {
 
-// 4 MiB: room for (rows x chunks) statistics of up to 262,112 (B*N*chunks)
-// entries, far beyond the workloads (a 64 x 31-node batch with a 128K
-// vocabulary needs 32 KB).
+// 4 MiB: room for (4 MiB - 256) / 16 = 262128 (row, chunk) statistics
+// entries of the streaming kernels. None of the five workloads needs any
+// (their vocabularies are at most 151936, which the on-chip walk holds); a
+// batch of 64 sequences x 31 nodes at the largest streamed vocabulary,
+// 786432, needs 32000 bytes.
 constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
 static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+    void *ctx;   // the context the address was looked up in
+    void *addr;  // device address of g_accept_scratch there
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+// The current context (the runtime's primary context of the current device
+// once it is initialised), or nullptr when the driver entry point is missing.
+void *current_context() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    });
+    CUcontext c = nullptr;
+    if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
 
 // Device address of the array on the current device. In host code the
 // array's name only stands in for the symbol, so the address is asked of the
-// runtime once per device and kept.
+// runtime once per device and context and kept; a new context on the device
+// (after cudaDeviceReset, for instance) reloads the module, and the address
+// is looked up again.
 int scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SVF_ERR_LAUNCH;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchAddr &e = g_scratch[dev];
+    void *ctx = current_context();
+    if (e.addr == nullptr || ctx == nullptr || e.ctx != ctx) {
+        // the lookup also initialises the device's primary context if needed
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_accept_scratch) != cudaSuccess || ptr == nullptr)
             return SVF_ERR_LAUNCH;
-        g_scratch_addr[dev] = ptr;
+        e.ctx = current_context();
+        e.addr = ptr;
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return SVF_OK;
 }
 

@@ -1,4 +1,5 @@
-"""The allocation-free acceptance entry point, checked against the usual one.
+"""The allocation-free acceptance entry point, checked against the usual one
+and against the oracle.
 
 svf_spec_accept_noalloc is for callers that have no way to give this library
 device scratch memory: an inference runtime that hands a plugin only its
@@ -7,7 +8,10 @@ at start-up and may not allocate afterwards. It runs the same kernels as
 svf_spec_accept with their scratch in an array the library owns, so it must
 return exactly what svf_spec_accept returns on the same inputs -- and keep
 doing so on the next call, although that call reuses the same array with
-whatever the previous call left in it.
+whatever the previous call left in it. Vocabularies above 262144 take the
+streaming kernels, which are the ones that use the array; the calls below
+run two of those in a row, with different shapes and chunk counts, between
+two on-chip calls.
 """
 
 import ctypes
@@ -15,6 +19,9 @@ import ctypes
 import numpy as np
 import pytest
 import torch
+
+import oracle
+from gpu_common import compare_accept
 
 pytestmark = pytest.mark.gpu
 
@@ -44,9 +51,15 @@ def test_noalloc_accept_matches_workspace_accept_on_two_calls():
     lib = sv.load_library()
     dev = torch.device("cuda")
     stream = torch.cuda.current_stream()
-    # two calls in a row with different shapes: the second must not see the first's scratch
-    for seed, B, N, V in ((5, 8, 15, 32000), (6, 3, 31, 128256)):
-        a = {k: torch.from_numpy(v).to(dev) for k, v in _case(seed, B, N, V).items()}
+    # calls in a row with different shapes: each must not see what the one
+    # before it left in the array (the two streamed ones use it)
+    used = []
+    for seed, B, N, V in ((5, 8, 15, 32000), (7, 2, 7, 300000), (8, 3, 15, 524288),
+                          (6, 3, 31, 128256)):
+        need = sv.spec_accept_workspace_size(B, N, V)
+        used.append(need)
+        arrs = _case(seed, B, N, V)
+        a = {k: torch.from_numpy(v).to(dev) for k, v in arrs.items()}
         ref = sv.spec_accept(a["target"], a["draft"], a["tokens"], a["parent"], a["u_accept"],
                              a["u_bonus"])
         acc_len = torch.full((B,), -7, dtype=torch.int32, device=dev)
@@ -65,8 +78,12 @@ def test_noalloc_accept_matches_workspace_accept_on_two_calls():
         assert torch.equal(acc_len, ref["accept_len"])
         assert torch.equal(path, ref["path"])
         assert torch.equal(out_tok, ref["out_tokens"])
-        np.testing.assert_allclose(ratio.cpu().numpy(), ref["ratio"].cpu().numpy(), rtol=1e-5,
-                                   equal_nan=True)
+        np.testing.assert_array_equal(ratio.cpu().numpy(), ref["ratio"].cpu().numpy())
+        gpu = {"accept_len": acc_len.cpu().numpy(), "path": path.cpu().numpy(),
+               "out_tokens": out_tok.cpu().numpy(), "ratio": ratio.cpu().numpy(),
+               "status": status.cpu().numpy()}
+        compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
+    assert used[1] > 0 and used[2] > 0 and used[1] != used[2], used
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
