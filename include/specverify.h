@@ -431,6 +431,52 @@ int svf_kv_commit(void *k_cache, void *v_cache, int num_layers, long long layer_
  * ---------------------------------------------------------------------- */
 int svf_selftest_wait_timeout(int32_t *result, long long deadline_ns, svf_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * svf_lm_head -- target logits of every tree node from its hidden state.
+ *
+ * "The EAGLE Family", § Why predict features instead of tokens?: the target
+ * distribution at a node is softmax(W_LM h), h the node's last hidden
+ * state; "EAGLE 演化史", § Tree Verification 详解, D.2 places the verify
+ * pass's bandwidth cost in this LM head and the softmax over N·|V|.
+ *   logits[r][v] = sum_k hidden[r][k] * weight[v][k]
+ * bf16 operands, products accumulated in fp32 on the tensor cores, fp32
+ * results; the weight is read from memory once per call.
+ *   hidden  [R, H] bf16 (raw bits), row-major, 16-byte aligned   in
+ *   weight  [V, H] bf16, row-major, 16-byte aligned              in
+ *   logits  [R, V] fp32, row-major                               out
+ *   status  [1] int32, nullable: SVF_DEV_TIMEOUT is OR-ed in if an
+ *           internal wait gave up (logits are then undefined)
+ * Limits: 1 <= R, V <= 2^24; H a multiple of 64, 64 <= H <= 65536.
+ * Returns SVF_ERR_ARG for null or misaligned pointers, SVF_ERR_UNSUPPORTED
+ * outside the limits. All memory is the caller's; nothing is allocated.
+ * ---------------------------------------------------------------------- */
+int svf_lm_head(const void *hidden, const void *weight, int R, int H, int V, float *logits,
+                int32_t *status, svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * svf_spec_accept_lmhead -- the LM head and the acceptance walk in one call.
+ *
+ * The target rows of svf_spec_accept are produced here from the nodes'
+ * hidden states ("The EAGLE Family", § Why predict features instead of
+ * tokens?: p = softmax(W_LM h)): svf_lm_head writes every node's fp32
+ * logits into target_logits, then the walk of svf_spec_accept ("Eagle vs
+ * DFlash", § Target-model decoding is serial; "EAGLE 演化史", § C) reads the
+ * rows of the nodes it visits. The two kernels are chained on the stream.
+ *   hidden        [B, N, H] bf16 in      weight [V, H] bf16 in
+ *   draft_logits  [B, N, V] fp32 in      target_logits [B, N, V] fp32 out
+ *   tokens, parent, u_accept, u_bonus, accept_len, path, out_tokens,
+ *   ratio, status: as svf_spec_accept.
+ *   lm_status     [1] int32, nullable: the LM head's SVF_DEV_TIMEOUT bit.
+ * Limits: those of svf_lm_head with R = B*N, and of svf_spec_accept with a
+ * vocabulary the walk holds on chip (V <= 262144), so no workspace.
+ * ---------------------------------------------------------------------- */
+int svf_spec_accept_lmhead(const void *hidden, const void *weight, const float *draft_logits,
+                           const int32_t *tokens, const int32_t *parent, const float *u_accept,
+                           const float *u_bonus, int B, int N, int H, int V,
+                           float *target_logits, int32_t *accept_len, int32_t *path,
+                           int32_t *out_tokens, float *ratio, int32_t *lm_status,
+                           int32_t *status, svf_stream_t stream);
+
 /* Human-readable name of a host return code or of one device status bit. */
 const char *svf_status_string(int code);
 

@@ -37,6 +37,8 @@ EXPORTED = [
     "svf_spec_accept_workspace_size",
     "svf_spec_accept",
     "svf_spec_accept_noalloc",
+    "svf_lm_head",
+    "svf_spec_accept_lmhead",
     "svf_kv_commit",
     "svf_selftest_wait_timeout",
     "svf_spec_accept_bf16",
@@ -102,6 +104,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_kv_commit.argtypes = [P, P, I, ctypes.c_longlong, I, I, P, I, P, P, P, I, I, I, I,
                                   I, P, P, I, P, P, P]
     lib.svf_kv_commit.restype = I
+    lib.svf_lm_head.argtypes = [P, P, I, I, I, P, P, P]
+    lib.svf_lm_head.restype = I
+    lib.svf_spec_accept_lmhead.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, P, P,
+                                           P]
+    lib.svf_spec_accept_lmhead.restype = I
     lib.svf_status_string.argtypes = [I]
     lib.svf_status_string.restype = ctypes.c_char_p
     lib.svf_version.argtypes = []
@@ -349,6 +356,73 @@ def spec_accept_onehot(target_logits: torch.Tensor, tokens: torch.Tensor, parent
             N, V, _ptr(o["accept_len"]), _ptr(o["path"]), _ptr(o["out_tokens"]),
             _ptr(o.get("ratio")), _ptr(o["status"]), _stream(stream))
     _check(rc, "svf_spec_accept_onehot" + ("_bf16" if bf else ""))
+    return o
+
+
+# ---------------------------------------------------------------------------
+# LM head (target logits from hidden states) and the walk fed by it
+# ---------------------------------------------------------------------------
+
+def lm_head(hidden: torch.Tensor, weight: torch.Tensor, logits: Optional[torch.Tensor] = None,
+            status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """logits[..., v] = hidden[..., :] . weight[v, :] for bf16 hidden [..., H]
+    and weight [V, H], as fp32 [..., V]."""
+    lib = load_library()
+    _dev(hidden, "hidden", torch.bfloat16)
+    H = hidden.shape[-1]
+    _dev(weight, "weight", torch.bfloat16)
+    if weight.dim() != 2 or weight.shape[1] != H:
+        raise SpecVerifyError("weight must be [V, H] with H = hidden.shape[-1]")
+    V = weight.shape[0]
+    R = hidden.numel() // H if H > 0 else 0
+    shape = tuple(hidden.shape[:-1]) + (V,)
+    if logits is None:
+        logits = torch.empty(shape, dtype=torch.float32, device=hidden.device)
+    _dev(logits, "logits", torch.float32, shape)
+    if status is not None:
+        _dev(status, "status", torch.int32)
+    rc = lib.svf_lm_head(_ptr(hidden), _ptr(weight), R, H, V, _ptr(logits), _ptr(status),
+                         _stream(stream))
+    _check(rc, "svf_lm_head")
+    return logits
+
+
+def spec_accept_lmhead(hidden: torch.Tensor, weight: torch.Tensor, draft_logits: torch.Tensor,
+                       tokens: torch.Tensor, parent: torch.Tensor, u_accept: torch.Tensor,
+                       u_bonus: torch.Tensor, want_ratio: bool = True,
+                       outputs: Optional[dict] = None, stream=None) -> dict:
+    """The acceptance walk with target rows from the LM head: hidden [B, N, H]
+    bf16, weight [V, H] bf16, draft logits [B, N, V] fp32. Returns
+    spec_accept's outputs plus "target_logits" [B, N, V] fp32 and
+    "lm_status" [1]."""
+    lib = load_library()
+    _dev(hidden, "hidden", torch.bfloat16)
+    B, N, H = hidden.shape
+    _dev(weight, "weight", torch.bfloat16)
+    V = weight.shape[0]
+    if weight.dim() != 2 or weight.shape[1] != H:
+        raise SpecVerifyError("weight must be [V, H] with H = hidden.shape[-1]")
+    _dev(draft_logits, "draft_logits", torch.float32, (B, N, V))
+    _dev(tokens, "tokens", torch.int32, (B, N))
+    _dev(parent, "parent", torch.int32, (B, N))
+    _dev(u_accept, "u_accept", torch.float32, (B, N))
+    _dev(u_bonus, "u_bonus", torch.float32, (B,))
+    dev = hidden.device
+    o = outputs if outputs is not None else {}
+    if "accept_len" not in o:
+        o["accept_len"] = torch.empty((B,), dtype=torch.int32, device=dev)
+        o["path"] = torch.empty((B, N), dtype=torch.int32, device=dev)
+        o["out_tokens"] = torch.empty((B, N), dtype=torch.int32, device=dev)
+        o["ratio"] = torch.empty((B, N), dtype=torch.float32, device=dev) if want_ratio else None
+        o["status"] = torch.empty((B,), dtype=torch.int32, device=dev)
+        o["target_logits"] = torch.empty((B, N, V), dtype=torch.float32, device=dev)
+        o["lm_status"] = torch.zeros((1,), dtype=torch.int32, device=dev)
+    rc = lib.svf_spec_accept_lmhead(
+        _ptr(hidden), _ptr(weight), _ptr(draft_logits), _ptr(tokens), _ptr(parent),
+        _ptr(u_accept), _ptr(u_bonus), B, N, H, V, _ptr(o["target_logits"]),
+        _ptr(o["accept_len"]), _ptr(o["path"]), _ptr(o["out_tokens"]), _ptr(o.get("ratio")),
+        _ptr(o["lm_status"]), _ptr(o["status"]), _stream(stream))
+    _check(rc, "svf_spec_accept_lmhead")
     return o
 
 

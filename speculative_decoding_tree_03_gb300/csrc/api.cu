@@ -138,6 +138,43 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 
+int svf_lm_head(const void *hidden, const void *weight, int R, int H, int V, float *logits,
+                int32_t *status, svf_stream_t stream) {
+    if (R < 0 || H < 0 || V < 0) return SVF_ERR_ARG;
+    if (R == 0) return SVF_OK;
+    if (!hidden || !weight || !logits) return SVF_ERR_ARG;
+    if (!lm_head_supported(R, H, V)) return SVF_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(weight)) return SVF_ERR_ARG;
+    return launch_lm_head(hidden, weight, R, H, V, logits, status,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int svf_spec_accept_lmhead(const void *hidden, const void *weight, const float *draft_logits,
+                           const int32_t *tokens, const int32_t *parent, const float *u_accept,
+                           const float *u_bonus, int B, int N, int H, int V,
+                           float *target_logits, int32_t *accept_len, int32_t *path,
+                           int32_t *out_tokens, float *ratio, int32_t *lm_status,
+                           int32_t *status, svf_stream_t stream) {
+    if (B < 0 || N < 0 || H < 0 || V < 0) return SVF_ERR_ARG;
+    if (B == 0) return SVF_OK;
+    if (!hidden || !weight || !draft_logits || !tokens || !parent || !u_accept || !u_bonus ||
+        !target_logits || !accept_len || !path || !out_tokens || !status)
+        return SVF_ERR_ARG;
+    if (N < 1 || N > 1024 || V < 1 || !accept_on_chip(V) ||
+        !lm_head_supported(B * N, H, V) || (long long)B * N > (1 << 24))
+        return SVF_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(weight)) return SVF_ERR_ARG;
+    if ((V & 3) == 0 && (!aligned16(target_logits) || !aligned16(draft_logits)))
+        return SVF_ERR_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int rc = launch_lm_head(hidden, weight, B * N, H, V, target_logits, lm_status, s);
+    if (rc != SVF_OK) return rc;
+    cudaError_t e = launch_accept(target_logits, draft_logits, tokens, parent, u_accept, u_bonus,
+                                  B, N, V, accept_len, path, out_tokens, ratio, nullptr, status,
+                                  s);
+    return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
+}
+
 int svf_spec_accept_bf16(const void *target_logits, const void *draft_logits,
                          const int32_t *tokens, const int32_t *parent, const float *u_accept,
                          const float *u_bonus, int B, int N, int V, int32_t *accept_len,

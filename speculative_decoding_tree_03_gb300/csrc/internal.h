@@ -124,6 +124,12 @@ cudaError_t launch_accept_stream(const float *target, const float *draft, const 
                                  int32_t *path, int32_t *out_tokens, float *ratio, void *workspace,
                                  int32_t *status, cudaStream_t stream);
 
+// Target logits from the LM head (lm_head.cu): logits[r][v] = h[r] . W[v],
+// bf16 operands, fp32 accumulation on the tensor cores. Returns an svf_status.
+bool lm_head_supported(int R, int H, int V);
+int launch_lm_head(const void *hidden, const void *weight, int R, int H, int V, float *logits,
+                   int32_t *status, cudaStream_t stream);
+
 int num_sms();
 
 // Launch with programmatic stream serialization (and a cluster size when

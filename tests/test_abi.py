@@ -213,3 +213,19 @@ def test_package_checks_before_any_launch():
         sv.spec_accept(t, t, i, i, u, ub)
     with pytest.raises(sv.SpecVerifyError):
         sv.eagle2_pool(torch.zeros((2,), dtype=torch.int32), 16)
+
+
+def test_lm_head_argument_checks(lib):
+    import speculative_decoding_tree_03_gb300 as sv
+    P = ctypes.c_void_p(256)
+    Q = ctypes.c_void_p(257)  # not 16-byte aligned
+    assert lib.svf_lm_head(None, P, 4, 64, 10, P, None, None) == sv.SVF_ERR_ARG
+    assert lib.svf_lm_head(P, P, 4, 100, 10, P, None, None) == sv.SVF_ERR_UNSUPPORTED
+    assert lib.svf_lm_head(P, P, 4, 64, 0, P, None, None) == sv.SVF_ERR_UNSUPPORTED
+    assert lib.svf_lm_head(Q, P, 4, 64, 10, P, None, None) == sv.SVF_ERR_ARG
+    assert lib.svf_lm_head(P, P, 0, 64, 10, P, None, None) == sv.SVF_OK
+    assert lib.svf_lm_head(P, P, -1, 64, 10, P, None, None) == sv.SVF_ERR_ARG
+    args = [P] * 7 + [2, 3, 64, 300000] + [P] * 4 + [None, None, P, None]
+    assert lib.svf_spec_accept_lmhead(*args) == sv.SVF_ERR_UNSUPPORTED   # V beyond on-chip
+    args = [P] * 7 + [2, 3, 64, 1000] + [P] * 4 + [None, None, None, None]
+    assert lib.svf_spec_accept_lmhead(*args) == sv.SVF_ERR_ARG           # no status
