@@ -118,7 +118,10 @@ int svf_tree_mask_build(const int32_t *parent, int B, int N, uint64_t *anc, int3
  *   out        [B, N, Hq, D] dtype                out
  *   lse        [B, N, Hq] float32                 out, may be NULL (natural log)
  *   workspace  device scratch of at least
- *              svf_tree_verify_attn_workspace_size(...) bytes (NULL if that is 0)
+ *              svf_tree_verify_attn_workspace_size(...) bytes (NULL if that is 0;
+ *              it is 0 for every size: the KV chunks of one (sequence, KV
+ *              head) merge on chip; the argument is kept for callers that
+ *              size it)
  *   status     [B] int32                          out; SVF_DEV_BAD_LENGTH,
  *                                                  SVF_DEV_BAD_PAGE. A bad
  *                                                  sequence's out and lse are 0.
@@ -476,6 +479,30 @@ int svf_spec_accept_lmhead(const void *hidden, const void *weight, const float *
                            float *target_logits, int32_t *accept_len, int32_t *path,
                            int32_t *out_tokens, float *ratio, int32_t *lm_status,
                            int32_t *status, svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * svf_debug_set_attn_wait_ns -- test hook: the deadline of every internal
+ * wait of the bf16 (tensor-core) attention kernel, for later calls in this
+ * process. The pages have no counterpart; it exists so that a test can make
+ * a wait of the product kernel run out without any fault: the kernel then
+ * leaves its loops, waits (with the default deadline) for its copies and
+ * tensor-core operations in flight, releases its tensor memory and sets
+ * SVF_DEV_TIMEOUT in status[b]; outputs of such a sequence are undefined
+ * (zeros when its chunks merge in a cluster). ns <= 0 restores the default
+ * of 2 s. Deadlines under 1 ms poll without blocking. Returns SVF_OK.
+ * ---------------------------------------------------------------------- */
+int svf_debug_set_attn_wait_ns(long long ns);
+
+/* ------------------------------------------------------------------------
+ * svf_debug_set_attn_splits -- test hook: the number of KV chunks per
+ * (sequence, KV head, row block) of later bf16 attention calls in this
+ * process, 1..8 (the CTAs of one cluster, merged on chip); 0 restores the
+ * library's own choice. It changes how the work is divided, not the result
+ * (which stays within the stated tolerance). The pages have no counterpart;
+ * it lets tests run every cluster size on the same inputs. Returns SVF_OK,
+ * or SVF_ERR_ARG outside 0..8.
+ * ---------------------------------------------------------------------- */
+int svf_debug_set_attn_splits(int splits);
 
 /* Human-readable name of a host return code or of one device status bit. */
 const char *svf_status_string(int code);

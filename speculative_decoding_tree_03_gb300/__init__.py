@@ -38,6 +38,8 @@ EXPORTED = [
     "svf_spec_accept",
     "svf_spec_accept_noalloc",
     "svf_lm_head",
+    "svf_debug_set_attn_wait_ns",
+    "svf_debug_set_attn_splits",
     "svf_spec_accept_lmhead",
     "svf_kv_commit",
     "svf_selftest_wait_timeout",
@@ -109,6 +111,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_spec_accept_lmhead.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, P, P,
                                            P]
     lib.svf_spec_accept_lmhead.restype = I
+    lib.svf_debug_set_attn_wait_ns.argtypes = [ctypes.c_longlong]
+    lib.svf_debug_set_attn_wait_ns.restype = I
+    lib.svf_debug_set_attn_splits.argtypes = [I]
+    lib.svf_debug_set_attn_splits.restype = I
     lib.svf_status_string.argtypes = [I]
     lib.svf_status_string.restype = ctypes.c_char_p
     lib.svf_version.argtypes = []

@@ -138,6 +138,17 @@ int svf_spec_accept(const float *target_logits, const float *draft_logits, const
     return e == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
 }
 
+int svf_debug_set_attn_wait_ns(long long ns) {
+    attn_tc_set_wait_ns(ns);
+    return SVF_OK;
+}
+
+int svf_debug_set_attn_splits(int splits) {
+    if (splits < 0 || splits > 8) return SVF_ERR_ARG;
+    attn_tc_force_splits(splits);
+    return SVF_OK;
+}
+
 int svf_lm_head(const void *hidden, const void *weight, int R, int H, int V, float *logits,
                 int32_t *status, svf_stream_t stream) {
     if (R < 0 || H < 0 || V < 0) return SVF_ERR_ARG;

@@ -31,12 +31,20 @@
 //                 2^8), writes P as bf16 over the first 32 S columns, and
 //                 finally reads O.
 //
-// Chunks of the KV range (splits) write normalised partial outputs and their
-// log-sum-exp to the workspace; attn_combine_kernel merges them.
+// Chunks of the KV range: the S CTAs of one (sequence, KV head, row block)
+// form a thread-block cluster; each takes an equal share of that sequence's
+// own tiles (from seq_lens, not from the page-table capacity). At the end
+// they merge through distributed shared memory: every CTA publishes its
+// rows' log-sum-exp, scales its O rows by their merge weights into shared
+// memory, and each CTA sums a share of the rows over the cluster and writes
+// the final bf16 output. Nothing goes through global memory and no second
+// kernel runs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <string.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -63,10 +71,8 @@ __host__ __device__ constexpr int vstages_for(int NH) { return NH == 1 ? 6 : 5; 
 // 512 TMEM columns with two halves; one half has room for four.
 __host__ __device__ constexpr int sbuffers_for(int NH) { return NH == 1 ? 4 : 2; }
 constexpr int kFixedTiles = 3;              // prologue + epilogue cost, in tiles
-// The combine reads a row's partials eight chunks at a time; each group of
-// eight costs about this many tiles of the call's time (measured: 8 chunks
-// beat 17 on a 33-tile, 8-unit batch, 14.4 against 16.4 us).
-constexpr float kCombineGroupTiles = 3.5f;
+constexpr float kMergeTiles = 1.5f;         // the in-cluster merge, in tiles
+constexpr int kMaxSplits = 8;               // cluster size (portable limit)
 // Warps: a K and a V producer, a QK issuer and a PV issuer per half, four
 // softmax warps per half. One thread issuing tcgen05.mma (or TMA copies)
 // sustains about one instruction per 100 cycles; several issuing warps
@@ -82,13 +88,12 @@ struct TcParams {
     const uint64_t *anc;
     int B, N, Hq, Hkv, G, M;
     int num_pages, page_size, max_pages;
-    int splits, chunk, row_blocks;
+    int splits, row_blocks;  // splits: CTAs per cluster, one chunk each
     int q_tma;        // 1: Q arrives by TMA (G a power of two <= 128)
     float scale_log2;
+    unsigned long long wait_ns;  // deadline of every wait but the final drains
     __nv_bfloat16 *out;
     float *lse;
-    float *part_o;    // [splits, B, N, Hq, HD]
-    float *part_lse;  // [splits, B, N, Hq]
     int32_t *status;
 };
 
@@ -101,15 +106,22 @@ struct TcSmem {
     static constexpr int kV = kK + kKS * tc::TILE_BYTES;
     static constexpr int kCrd = kV + kVS * tc::TILE_BYTES;
     static constexpr int kBar = kCrd + tc::MAX_BOXES * 4;
-    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 4 * NH * tc::sbuffers_for(NH) + 2;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 4 * NH * tc::sbuffers_for(NH) + 2 + 2 * NH;
     static constexpr int kMisc = kBar + kNumBars * 8;
-    static constexpr int kBytes = kMisc + 64;
+    // merge: per-row log2-sum-exp of this CTA, merged value, contributing CTAs
+    static constexpr int kLse = kMisc + 64;
+    static constexpr int kFin = kLse + 128 * NH * 4;
+    static constexpr int kMask = kFin + 128 * NH * 4;
+    static constexpr int kBytes = kMask + 128 * NH * 4;
+    // weighted O rows of the merge reuse the K/V rings (free by then)
+    static_assert(kCrd - kK >= 128 * NH * tc::HD * 4, "merge rows fit in the rings");
     static constexpr int kDynamic = kBytes + 1024;  // slack to align the base to 1 KB
     static_assert(kDynamic <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          unsigned long long ns) {
+    const bool ok = mbar_wait_for(bar, parity, abort, ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -157,9 +169,13 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     uint64_t *p_half = o_done + NH * SB;  // [NH][SB]: first half of that P written
     uint64_t *q_full = p_half + NH * SB;
     uint64_t *v_tail = q_full + 1;       // last V tile with its rows past the end zeroed
+    uint64_t *mma_drain = v_tail + 1;    // [2 NH]: an issuer's MMAs done, after an abort
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
-    int *err_flag = reinterpret_cast<int *>(smem + S::kMisc + 8);
+    int *m_flag = reinterpret_cast<int *>(smem + S::kMisc + 16);  // merge: [ok, bad, zero]
+    float *s_lse = reinterpret_cast<float *>(smem + S::kLse);   // [128 NH] log2-sum-exp
+    float *s_fin = reinterpret_cast<float *>(smem + S::kFin);   // [128 NH] merged
+    uint32_t *s_mask = reinterpret_cast<uint32_t *>(smem + S::kMask);  // contributing CTAs
 
     // tensor memory: S buffer (h, b) at columns [64 (SB h + b), +64); O of
     // half h at [256 + 128 h, +128); P goes over the first 32 columns of its S
@@ -193,6 +209,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         }
         mbar_init(q_full, 1);
         mbar_init(v_tail, 1);
+        for (int k = 0; k < 2 * NH; ++k) mbar_init(&mma_drain[k], 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -212,10 +229,12 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     const long long T = (long long)L + p.N;
     const bool len_ok = L >= 0 && T <= (long long)p.max_pages * p.page_size;
     const int ntiles = len_ok ? (int)((T + BN - 1) / BN) : 0;
-    const int j0 = split * p.chunk;
-    const int j1 = min(j0 + p.chunk, ntiles);
+    // this sequence's tiles in equal shares over the cluster's CTAs
+    const int chunk = (ntiles + p.splits - 1) / p.splits;
+    const int j0 = split * chunk;
+    const int j1 = min(j0 + chunk, ntiles);
     const int n = j1 - j0;
-    if (n <= 0) {
+    if (n <= 0 && p.splits == 1) {
         // No tile here. The first chunk reports a bad length; with a single
         // chunk this CTA owns final outputs, which are zeros then.
         tc_fence_before();
@@ -238,6 +257,16 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         return;
     }
 
+    int bad = 0;
+    const uint32_t tmem = *tmem_slot;
+    if (n <= 0) {
+        // an empty chunk of a cluster: it only takes part in the merge; the
+        // first chunk is never empty unless the length is bad
+        if (designated && threadIdx.x == 0) p.status[b] = SVF_DEV_BAD_LENGTH;
+        if (warp >= SW0) s_lse[threadIdx.x - 32 * SW0] = -INFINITY;
+        tc_fence_before();
+        __syncthreads();
+    } else {
     // ---- set-up: barriers, Q, tensor memory, box coordinates
     const int ps = p.page_size;
     const int box_rows = ps < MAX_BOX_ROWS ? ps : MAX_BOX_ROWS;
@@ -285,7 +314,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     // TMA fills with zeros) for boxes past the sequence or with a page id
     // outside the cache. Every index fits in 32 bits (num_pages * page_size
     // <= INT_MAX).
-    int bad = 0, bad_seq = 0;
+    int bad_seq = 0;
     {
         const int oob = p.num_pages * ps;
         const int32_t *__restrict__ pt = p.page_table + (size_t)b * p.max_pages;
@@ -314,7 +343,6 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     tc_fence_before();
     bad = __syncthreads_or(bad);
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     if (warp <= 1) {
         // ------------------------------------------------------------ producers
@@ -329,7 +357,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         int j = 0;  // tiles issued
         for (; j < n; ++j) {
             const int st = j % stages, use = j / stages;
-            if (use > 0 && !warp_wait(&empty[st], (uint32_t)((use - 1) & 1), abort_flag)) break;
+            if (use > 0 && !warp_wait(&empty[st], (uint32_t)((use - 1) & 1), abort_flag, p.wait_ns)) break;
             if (lane == 0) mbar_arrive_expect_tx(&full[st], TILE_BYTES);
             if (lane < bpt) {
                 const int c = crd[j * bpt + lane];
@@ -347,7 +375,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         const long long tbl = (long long)(j0 + n - 1) * BN;
         if (!is_k && tbl + BN > T && vj == n) {
             const int jl = n - 1;
-            if (warp_wait(&v_full[jl % VS], (uint32_t)((jl / VS) & 1), abort_flag)) {
+            if (warp_wait(&v_full[jl % VS], (uint32_t)((jl / VS) & 1), abort_flag, p.wait_ns)) {
                 const int r0 = (int)(T - tbl);
                 uint8_t *vs = sV + (jl % VS) * TILE_BYTES;
                 for (int idx = lane; idx < (BN - r0) * 16; idx += 32) {
@@ -365,10 +393,10 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
             // abort flag) for the last fill of every stage that was loaded.
             volatile int never = 0;
             for (int st = 0; st < KS && st < kj; ++st)
-                mbar_wait(&k_full[st], ((kj - 1 - st) / KS) & 1, &never);
+                mbar_wait_for(&k_full[st], ((kj - 1 - st) / KS) & 1, &never, kWaitDeadlineNs);
             for (int st = 0; st < VS && st < vj; ++st)
-                mbar_wait(&v_full[st], ((vj - 1 - st) / VS) & 1, &never);
-            if (is_k && p.q_tma) mbar_wait(q_full, 0, &never);
+                mbar_wait_for(&v_full[st], ((vj - 1 - st) / VS) & 1, &never, kWaitDeadlineNs);
+            if (is_k && p.q_tma) mbar_wait_for(q_full, 0, &never, kWaitDeadlineNs);
         }
     } else if (warp <= 1 + NH) {
         // ------------------------------------------------------------ QK issuer, half h
@@ -376,14 +404,14 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         const int h = warp - 2;
         constexpr uint32_t idesc_qk = idesc_bf16_f32(128, BN, false, false);
         const uint32_t aQ = smem_u32(sQ) + h * HALF_BYTES, aK = smem_u32(sK);
-        bool ok = !p.q_tma || warp_wait(q_full, 0, abort_flag);
+        bool ok = !p.q_tma || warp_wait(q_full, 0, abort_flag, p.wait_ns);
         for (int t = 0; ok && t < n; ++t) {
             const int bb = t % SB;
-            if (!(ok = warp_wait(&k_full[t % KS], (uint32_t)((t / KS) & 1), abort_flag))) break;
+            if (!(ok = warp_wait(&k_full[t % KS], (uint32_t)((t / KS) & 1), abort_flag, p.wait_ns))) break;
             if (t >= SB) {
                 // PV(t - SB) of this half read P from this S buffer
                 const int pj = t - SB;
-                if (!(ok = warp_wait(&o_done[h * SB + bb], (uint32_t)((pj / SB) & 1), abort_flag)))
+                if (!(ok = warp_wait(&o_done[h * SB + bb], (uint32_t)((pj / SB) & 1), abort_flag, p.wait_ns)))
                     break;
             }
             tc_fence_after();
@@ -412,8 +440,8 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         for (int j = 0; ok && j < n; ++j) {
             const int bb = j % SB;
             const bool tail = (long long)(j0 + j) * BN + BN > T;  // the sequence's last tile
-            ok = tail ? warp_wait(v_tail, 0, abort_flag)
-                      : warp_wait(&v_full[j % VS], (uint32_t)((j / VS) & 1), abort_flag);
+            ok = tail ? warp_wait(v_tail, 0, abort_flag, p.wait_ns)
+                      : warp_wait(&v_full[j % VS], (uint32_t)((j / VS) & 1), abort_flag, p.wait_ns);
             if (!ok) break;
             // P arrives in two halves of 32 tokens; the first half's K-steps
             // go in while the softmax still computes the second
@@ -423,7 +451,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 uint64_t *pb = part == 0 ? &p_half[h * SB + bb] : &p_full[h * SB + bb];
-                if (!(ok = warp_wait(pb, (uint32_t)((j / SB) & 1), abort_flag))) break;
+                if (!(ok = warp_wait(pb, (uint32_t)((j / SB) & 1), abort_flag, p.wait_ns))) break;
                 tc_fence_after();
                 if (lane == 0) {
 #pragma unroll
@@ -461,7 +489,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
             const int bb = j % SB;
             const uint32_t bph = (uint32_t)((j / SB) & 1);
             const uint32_t tS = tmem + lane_off + (uint32_t)((h * SB + bb) * BN);
-            if (!(ok = warp_wait(&s_full[h * SB + bb], bph, abort_flag))) break;
+            if (!(ok = warp_wait(&s_full[h * SB + bb], bph, abort_flag, p.wait_ns))) break;
             tc_fence_after();
             uint32_t v[BN];
             tmem_ld32(tS, v);
@@ -499,7 +527,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
                     // O is final up to PV(j - 1) of this half
                     const int pj = j - 1;
                     if (!(ok = warp_wait(&o_done[h * SB + pj % SB], (uint32_t)((pj / SB) & 1),
-                                         abort_flag)))
+                                         abort_flag, p.wait_ns)))
                         break;
                     tc_fence_after();
 #pragma unroll 1
@@ -544,13 +572,19 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         }
         // epilogue: O of this half after its last PV
         if (ok) ok = warp_wait(&o_done[h * SB + (n - 1) % SB], (uint32_t)(((n - 1) / SB) & 1),
-                               abort_flag);
+                               abort_flag, p.wait_ns);
         tc_fence_after();
+        if (p.splits > 1) {
+            // the merge reads O from tensor memory later; publish this row's
+            // log2-sum-exp and the reference max O is scaled by
+            s_lse[h * 128 + r] = (ok && l > 0.0f) ? m_ref + __log2f(l) : -INFINITY;
+            s_fin[h * 128 + r] = m_ref;
+        }
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const float lse_v = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         const size_t row = ((size_t)b * p.N + node) * p.Hq + hq;
 #pragma unroll 1
-        for (int c64 = 0; c64 < 2; ++c64) {
+        for (int c64 = 0; c64 < 2 && p.splits == 1; ++c64) {
             uint32_t o[64];
             if (ok) {
                 tmem_ld32(tO + c64 * 64, o);
@@ -561,7 +595,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
                 for (int c = 0; c < 64; ++c) o[c] = 0;
             }
             if (row_valid) {
-                if (p.splits == 1) {
+                {
                     uint4 *op = reinterpret_cast<uint4 *>(p.out + row * HD + c64 * 64);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -572,27 +606,134 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
                         w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
                         op[k] = w;
                     }
-                } else {
-                    float4 *op = reinterpret_cast<float4 *>(
-                        p.part_o + ((size_t)split * p.B * p.N * p.Hq + row) * HD + c64 * 64);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        op[k] = make_float4(__uint_as_float(o[4 * k + 0]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                            __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
                 }
             }
         }
-        if (row_valid) {
-            if (p.splits == 1) {
-                if (p.lse) p.lse[row] = lse_v;
-            } else {
-                p.part_lse[(size_t)split * p.B * p.N * p.Hq + row] = lse_v;
-            }
-        }
+        if (row_valid && p.splits == 1 && p.lse) p.lse[row] = lse_v;
     }
 
     tc_fence_before();
     __syncthreads();
+    }  // n > 0
+
+    if (*abort_flag) {
+        // a wait gave up: let every MMA an issuer started finish before the
+        // rings are reused or tensor memory is released
+        if (warp >= 2 && warp < SW0 && lane == 0) {
+            volatile int never = 0;
+            umma_commit(&mma_drain[warp - 2]);
+            mbar_wait_for(&mma_drain[warp - 2], 0, &never, kWaitDeadlineNs);
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+
+    if (p.splits > 1) {
+        // ---- merge of the cluster's chunks through distributed shared memory
+        const uint32_t rank = cluster_ctarank();
+        const int S2 = p.splits;
+        constexpr int RB = 128 * NH;
+        float4 *sO = reinterpret_cast<float4 *>(sK);  // [RB][32] weighted O rows, swizzled
+        if (threadIdx.x == 0) {
+            m_flag[0] = *abort_flag ? 0 : 1;
+            m_flag[1] = bad;
+        }
+        cluster_arrive();
+        cluster_wait();
+        if (threadIdx.x == 0) {
+            int zero = len_ok ? 0 : 1;
+            for (int s2 = 0; s2 < S2; ++s2) {
+                zero |= ld_dsmem_s32(cluster_map(&m_flag[0], (uint32_t)s2)) == 0;
+                zero |= ld_dsmem_s32(cluster_map(&m_flag[1], (uint32_t)s2)) != 0;
+            }
+            m_flag[2] = zero;
+        }
+        if (warp >= SW0) {
+            // the softmax role's row: half h, TMEM lane quarter (warp & 3)
+            const int lr = ((warp - SW0) >> 2) * 128 + (warp & 3) * 32 + lane;
+            float lv[kMaxSplits];
+            float lmax = -INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                lv[s2] = s2 < S2 ? ld_dsmem_f32(cluster_map(&s_lse[lr], (uint32_t)s2)) : -INFINITY;
+                lmax = fmaxf(lmax, lv[s2]);
+            }
+            float W = 0.0f;
+            uint32_t mask = 0;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxSplits; ++s2)
+                if (lv[s2] != -INFINITY) {
+                    W += ex2_approx(lv[s2] - lmax);
+                    mask |= 1u << s2;
+                }
+            const float m_mine = s_fin[lr];
+            s_fin[lr] = mask ? lmax + __log2f(W) : -INFINITY;
+            s_mask[lr] = mask;
+            // a row may see no column of this chunk (its rank bit is then
+            // clear); the tensor-memory loads are warp-wide, so a warp loads
+            // when any of its rows contributes and only those rows store
+            const bool contrib = (mask >> rank) & 1u;
+            tc_fence_after();
+            if (__any_sync(FULL, contrib)) {
+                // O_mine * 2^(m_mine - lmax) / W: this chunk's share of the row
+                const float sc = contrib ? ex2_approx(m_mine - lmax) / W : 0.0f;
+                const uint32_t tO = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256 +
+                                    (uint32_t)((lr >> 7) * 128);
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c4 * 32, o);
+                    tmem_wait_ld();
+                    if (contrib) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            sO[lr * 32 + ((c4 * 8 + k) ^ (lr & 31))] =
+                                make_float4(__uint_as_float(o[4 * k]) * sc,
+                                            __uint_as_float(o[4 * k + 1]) * sc,
+                                            __uint_as_float(o[4 * k + 2]) * sc,
+                                            __uint_as_float(o[4 * k + 3]) * sc);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        cluster_arrive();
+        cluster_wait();
+        // rows lr = rank, rank + S, ... of this row block: sum the cluster's
+        // shares, 16 bytes of a row per thread
+        const bool zero = m_flag[2] != 0;
+        const int nrows = (RB - (int)rank + S2 - 1) / S2;
+        for (int it = threadIdx.x; it < nrows * 32; it += NTHREADS) {
+            const int lr = (int)rank + (it >> 5) * S2;
+            const int c = it & 31;
+            const int Rg = rb * RB + lr;
+            if (Rg >= p.M) continue;
+            const uint32_t mask = s_mask[lr];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!zero) {
+                for (int s2 = 0; s2 < S2; ++s2)
+                    if ((mask >> s2) & 1u) {
+                        const float4 v = ld_dsmem_v4(
+                            cluster_map(&sO[lr * 32 + (c ^ (lr & 31))], (uint32_t)s2));
+                        acc.x += v.x;
+                        acc.y += v.y;
+                        acc.z += v.z;
+                        acc.w += v.w;
+                    }
+            }
+            const size_t row = ((size_t)b * p.N + Rg / p.G) * p.Hq + g * p.G + Rg % p.G;
+            uint2 w2;
+            w2.x = pack_bf16x2(acc.x, acc.y);
+            w2.y = pack_bf16x2(acc.z, acc.w);
+            *reinterpret_cast<uint2 *>(p.out + row * HD + c * 4) = w2;
+            if (c == 0 && p.lse)
+                p.lse[row] = zero ? 0.0f : s_fin[lr] * 0.69314718055994531f;
+        }
+        // no CTA leaves while a peer may still read its shared memory
+        cluster_arrive();
+        cluster_wait();
+    }
+
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -611,71 +752,6 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
             if (p.lse) p.lse[row] = 0.0f;
         }
     }
-    (void)err_flag;
-}
-
-// Merge chunk partials: lse = log sum_s e^{lse_s}, out = sum_s e^{lse_s - lse} o_s,
-// over the chunks that hold tiles of the sequence (ceil(tiles / chunk) of
-// them). One warp per (sequence, node, head) row; lane s holds chunk s's lse
-// (and s + 32's), and the partial rows are loaded eight chunks at a time so
-// their latencies overlap. A sequence with any status bit set gets zeros.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restrict__ part_o,
-                                                           const float *__restrict__ part_lse,
-                                                           long long rows, int per_b, int N,
-                                                           int chunk,
-                                                           const int32_t *__restrict__ seq_lens,
-                                                           const int32_t *__restrict__ status,
-                                                           __nv_bfloat16 *__restrict__ out,
-                                                           float *__restrict__ lse) {
-    pdl_wait();
-    pdl_launch_dependents();
-    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const int b = (int)(row / per_b);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse_out = 0.0f;
-    if (status[b] == 0) {
-        const long long T = (long long)seq_lens[b] + N;
-        const int tiles = (int)((T + tc::BN - 1) / tc::BN);
-        const int splits = (tiles + chunk - 1) / chunk;
-        const float l0 = lane < splits ? part_lse[(size_t)lane * rows + row] : -INFINITY;
-        const float l1 = lane + 32 < splits ? part_lse[(size_t)(lane + 32) * rows + row] : -INFINITY;
-        const float mx = warp_max(fmaxf(l0, l1));
-        if (mx != -INFINITY) {
-            const float w0 = l0 == -INFINITY ? 0.0f : expf(l0 - mx);
-            const float w1 = l1 == -INFINITY ? 0.0f : expf(l1 - mx);
-            const float wsum = warp_sum(w0 + w1);
-            for (int s0 = 0; s0 < splits; s0 += 8) {
-                float4 o[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    o[k] = s0 + k < splits
-                               ? *reinterpret_cast<const float4 *>(
-                                     part_o + ((size_t)(s0 + k) * rows + row) * 128 + lane * 4)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int sidx = s0 + k;
-                    const float wa = __shfl_sync(0xffffffffu, w0, sidx & 31);
-                    const float wb = __shfl_sync(0xffffffffu, w1, sidx & 31);
-                    const float w = sidx < 32 ? wa : wb;
-                    acc.x = fmaf(w, o[k].x, acc.x);
-                    acc.y = fmaf(w, o[k].y, acc.y);
-                    acc.z = fmaf(w, o[k].z, acc.z);
-                    acc.w = fmaf(w, o[k].w, acc.w);
-                }
-            }
-            const float inv = 1.0f / wsum;
-            acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-            lse_out = mx + logf(wsum);
-        }
-    }
-    uint2 w;
-    w.x = pack_bf16x2(acc.x, acc.y);
-    w.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2 *>(out + (size_t)row * 128 + lane * 4) = w;
-    if (lse && lane == 0) lse[row] = lse_out;
 }
 
 // ---------------------------------------------------------------- host side
@@ -727,11 +803,60 @@ static bool make_q_map(CUtensorMap *map, const void *q, int B, int N, int Hq, in
 // tile twice, from L2 or by multicast) on this part.
 static int row_halves(int M) { return M > 128 ? 2 : 1; }
 
-// Chunk count of the KV range per (sequence, KV head, row block): minimises
-// max(waves x (tiles per chunk + fixed cost), total bytes / bandwidth) plus
-// the combine's latency (one term per group of eight chunks), where the
-// bytes count the partial outputs written and read back, with at most
-// CMAX_TILES tiles per chunk.
+// Largest number of clusters of `splits` CTAs of the kernel for NH halves
+// that can be resident at once (one CTA per SM; a cluster's CTAs share a
+// GPC, so not every SM takes part for every cluster size).
+static int resident_ctas(int NH, int splits) {
+    static int cache[3][tc::kMaxSplits + 1] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    static int cached_dev = -1;
+    if (cached_dev != dev) {
+        for (auto &row : cache)
+            for (int &v : row) v = 0;
+        cached_dev = dev;
+    }
+    int &slot = cache[NH][splits];
+    if (slot > 0) return slot;
+    const int C = num_sms();
+    int n = C;
+    if (splits > 1) {
+        const int smem = NH == 1 ? TcSmem<1>::kDynamic : TcSmem<2>::kDynamic;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, (unsigned)splits, (unsigned)C);
+        cfg.blockDim = dim3(tc::threads_for(NH));
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 1;
+        attr.val.clusterDim.y = (unsigned)splits;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        cudaError_t e;
+        if (NH == 1) {
+            cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            e = cudaOccupancyMaxActiveClusters(&clusters, attn_tc_kernel<1>, &cfg);
+        } else {
+            cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            e = cudaOccupancyMaxActiveClusters(&clusters, attn_tc_kernel<2>, &cfg);
+        }
+        n = (e == cudaSuccess && clusters > 0) ? clusters * splits : (C / splits) * splits;
+    }
+    slot = n;
+    return n;
+}
+
+// Chunks per (sequence, KV head, row block) = the cluster size S. A wave is
+// as many CTAs as can be resident for that cluster size, and each CTA costs
+// its tiles plus a fixed cost (plus the merge when S > 1), with at most
+// CMAX_TILES tiles per chunk. The lengths are on the device, so the host
+// rates each S on two length profiles and averages them: every sequence at
+// the page table's capacity (waves x the longest chunk), and lengths spread
+// evenly below it (the longest chunk, or the total work spread over the
+// resident CTAs, whichever is larger). Each cluster then splits its own
+// sequence's tiles evenly, so shorter sequences simply finish sooner.
 int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) {
     const int G = Hq / Hkv;
     const int M = N * G;
@@ -740,20 +865,19 @@ int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) 
     const long long units = (long long)B * Hkv * row_blocks;
     const long long kv_max = (long long)max_pages * page_size;
     const int tiles = (int)((kv_max + tc::BN - 1) / tc::BN);
-    const int C = num_sms();
-    // partial output write + read per chunk and unit, in units of one K+V tile
-    const double part_tiles = (double)(128 * NH) * (tc::HD + 1) * 4 * 2 / (2.0 * tc::TILE_BYTES);
     double best = 1e300;
     int best_s = 1;
-    const int smax = tiles < 64 ? tiles : 64;
-    for (int s = 1; s <= smax; ++s) {
+    for (int s = 1; s <= tc::kMaxSplits; ++s) {
         const int per_cta = (tiles + s - 1) / s;
         if (per_cta > tc::CMAX_TILES) continue;
-        const long long waves = (units * s + C - 1) / C;
-        const double t_chain = (double)waves * (per_cta + tc::kFixedTiles);
-        const double t_bytes = (double)units * (tiles + (s > 1 ? s * part_tiles : 0.0)) / C;
-        const double t = (t_chain > t_bytes ? t_chain : t_bytes) +
-                         (s > 1 ? tc::kCombineGroupTiles * ((s + 7) / 8) : 0.0);
+        const int cap = resident_ctas(NH, s);
+        const double fixed = tc::kFixedTiles + (s > 1 ? tc::kMergeTiles : 0.0);
+        const long long waves = (units * s + cap - 1) / cap;
+        const double t_full = (double)waves * (per_cta + fixed);
+        const double longest = per_cta + fixed;
+        const double spread = (double)units * s * (0.5 * per_cta + fixed) / cap;
+        const double t_spread = longest > spread ? longest : spread;
+        const double t = 0.5 * (t_full + t_spread);
         if (t < best - 1e-9) {
             best = t;
             best_s = s;
@@ -762,35 +886,37 @@ int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) 
     return best_s;
 }
 
-static int attn_tc_chunk(int splits, int max_pages, int page_size) {
-    const long long kv_max = (long long)max_pages * page_size;
-    const int tiles = (int)((kv_max + tc::BN - 1) / tc::BN);
-    return (tiles + splits - 1) / splits;
-}
-
 bool attn_tc_supported(int max_pages, int page_size) {
     const long long kv_max = (long long)max_pages * page_size;
     const int tiles = (int)((kv_max + tc::BN - 1) / tc::BN);
-    return tiles <= 64 * tc::CMAX_TILES;
+    return tiles <= tc::kMaxSplits * tc::CMAX_TILES;
 }
 
-size_t attn_tc_workspace_bytes(int B, int N, int Hq, int Hkv, int max_pages, int page_size) {
-    const int s = attn_tc_splits(B, N, Hq, Hkv, max_pages, page_size);
-    if (s <= 1) return 0;
-    const size_t rows = (size_t)B * N * Hq;
-    return (size_t)s * rows * (tc::HD + 1) * sizeof(float) + 256;
+// No workspace: chunks merge on chip.
+size_t attn_tc_workspace_bytes(int, int, int, int, int, int) { return 0; }
+
+static std::atomic<long long> g_attn_wait_ns{0};
+static std::atomic<int> g_attn_force_splits{0};
+
+void attn_tc_set_wait_ns(long long ns) { g_attn_wait_ns.store(ns > 0 ? ns : 0); }
+void attn_tc_force_splits(int s) {
+    g_attn_force_splits.store(s > 0 && s <= tc::kMaxSplits ? s : 0);
 }
 
-int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+int launch_attn_tc(const AttnArgs &a, void *, size_t, cudaStream_t stream) {
     const int G = a.Hq / a.Hkv;
     const int M = a.N * G;
     const int NH = row_halves(M);
     const int row_blocks = (M + 128 * NH - 1) / (128 * NH);
     if (!attn_tc_supported(a.max_pages, a.page_size)) return SVF_ERR_UNSUPPORTED;
-    const int splits = attn_tc_splits(a.B, a.N, a.Hq, a.Hkv, a.max_pages, a.page_size);
-    const int chunk = attn_tc_chunk(splits, a.max_pages, a.page_size);
-    const size_t need = attn_tc_workspace_bytes(a.B, a.N, a.Hq, a.Hkv, a.max_pages, a.page_size);
-    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return SVF_ERR_WORKSPACE;
+    int splits = attn_tc_splits(a.B, a.N, a.Hq, a.Hkv, a.max_pages, a.page_size);
+    const int forced = g_attn_force_splits.load();
+    if (forced > 0) {
+        const long long kv_max = (long long)a.max_pages * a.page_size;
+        const int tiles = (int)((kv_max + tc::BN - 1) / tc::BN);
+        splits = forced;
+        while ((tiles + splits - 1) / splits > tc::CMAX_TILES) ++splits;
+    }
 
     CUtensorMap tmk, tmv, tmq;
     if (!make_kv_map(&tmk, a.k_cache, a.num_pages, a.page_size, a.Hkv) ||
@@ -812,48 +938,32 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
     p.B = a.B; p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.M = M;
     p.num_pages = a.num_pages; p.page_size = a.page_size; p.max_pages = a.max_pages;
     p.splits = splits;
-    p.chunk = chunk;
     p.row_blocks = row_blocks;
     p.q_tma = q_tma ? 1 : 0;
     const float scale = a.sm_scale > 0.0f ? a.sm_scale : 1.0f / sqrtf((float)a.D);
     p.scale_log2 = scale * 1.4426950408889634f;
+    const long long wns = g_attn_wait_ns.load();
+    p.wait_ns = wns > 0 ? (unsigned long long)wns : kWaitDeadlineNs;
     p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
     p.lse = a.lse;
-    const size_t rows = (size_t)a.B * a.N * a.Hq;
-    if (splits > 1) {
-        uintptr_t base = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~(uintptr_t)255;
-        p.part_o = reinterpret_cast<float *>(base);
-        p.part_lse = p.part_o + (size_t)splits * rows * tc::HD;
-    } else {
-        p.part_o = nullptr;
-        p.part_lse = nullptr;
-    }
     p.status = a.status;
 
     dim3 grid(a.Hkv * row_blocks, splits, a.B);
+    const unsigned cl = splits > 1 ? (unsigned)splits : 0u;
     if (NH == 1) {
         const int smem = TcSmem<1>::kDynamic;
         cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (launch_pdl(attn_tc_kernel<1>, grid, dim3(tc::threads_for(1)), smem, stream, 0u, tmk,
-                       tmv, tmq, p) != cudaSuccess)
+        if (launch_pdl_cluster_y(attn_tc_kernel<1>, grid, dim3(tc::threads_for(1)), smem, stream,
+                                 cl, tmk, tmv, tmq, p) != cudaSuccess)
             return SVF_ERR_LAUNCH;
     } else {
         const int smem = TcSmem<2>::kDynamic;
         cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (launch_pdl(attn_tc_kernel<2>, grid, dim3(tc::threads_for(2)), smem, stream, 0u, tmk,
-                       tmv, tmq, p) != cudaSuccess)
+        if (launch_pdl_cluster_y(attn_tc_kernel<2>, grid, dim3(tc::threads_for(2)), smem, stream,
+                                 cl, tmk, tmv, tmq, p) != cudaSuccess)
             return SVF_ERR_LAUNCH;
     }
     if (cudaGetLastError() != cudaSuccess) return SVF_ERR_LAUNCH;
-    if (splits > 1) {
-        const long long threads = (long long)rows * 32;
-        const int blocks = (int)((threads + 255) / 256);
-        if (launch_pdl(attn_combine_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, 0u,
-                       (const float *)p.part_o, (const float *)p.part_lse, (long long)rows,
-                       a.N * a.Hq, a.N, chunk, a.seq_lens, (const int32_t *)a.status, p.out,
-                       a.lse) != cudaSuccess)
-            return SVF_ERR_LAUNCH;
-    }
     return SVF_OK;
 }
 

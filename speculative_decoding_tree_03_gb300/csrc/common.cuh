@@ -74,13 +74,17 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete. Gives up after the
 // deadline or as soon as another thread of the CTA raised *abort; returns
 // false then (and raises *abort itself on a timeout).
+// Deadlines under 1 ms (set only to make a wait run out in a test) poll
+// without blocking and check the clock on every iteration.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, volatile int *abort,
                                               unsigned long long deadline_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const bool quick = deadline_ns < 1000000ull;
+    if (quick ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
+    const uint32_t every = quick ? 0u : 63u;
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if (quick ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if ((it & every) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > deadline_ns) {
                 *abort = 1;
@@ -137,6 +141,26 @@ __device__ __forceinline__ bool mbar_wait_cluster_for(uint64_t *bar, uint32_t pa
 }
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
     return mbar_wait_cluster_for(bar, parity, kWaitDeadlineNs);
+}
+
+// Loads from another CTA's shared memory (an address from cluster_map).
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void cluster_arrive() {

@@ -104,6 +104,12 @@ size_t attn_tc_workspace_bytes(int B, int N, int Hq, int Hkv, int max_pages, int
 int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size);
 bool attn_tc_supported(int max_pages, int page_size);
 int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream);
+// Test hook: the deadline of the tensor-core attention kernel's waits (ns;
+// 0 or less restores the default of 2 s).
+void attn_tc_set_wait_ns(long long ns);
+// Test hook: the chunk count (cluster size) of later calls, 1..8; 0 restores
+// the host model's choice.
+void attn_tc_force_splits(int s);
 
 // Acceptance walk (accept.cu): rows of the visited nodes held in the registers
 // of one CTA cluster up to kMaxOnChipVocab, streamed from memory beyond that
@@ -152,6 +158,32 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = cluster_x;
         attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
+// The same with the cluster along y (cluster_y CTAs of consecutive blockIdx.y).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster_y(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, unsigned cluster_y, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster_y > 0) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = cluster_y;
         attr[na].val.clusterDim.z = 1;
         ++na;
     }

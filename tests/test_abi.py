@@ -180,9 +180,9 @@ def test_selftest_argument_checks(lib):
 
 
 def test_workspace_sizes_without_gpu(lib):
-    # bf16 attention with many KV tiles per (sequence, head) splits the KV range
-    n = lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 1, 1, 2176)
-    assert n >= 0
+    # bf16 attention merges its KV chunks on chip: no workspace at any size
+    assert lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 1, 1, 2176) == 0
+    assert lib.svf_tree_verify_attn_workspace_size(64, 31, 64, 8, 128, 1, 2051, 16) == 0
     assert lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 0, 1, 2176) == 0
 
 
@@ -229,3 +229,11 @@ def test_lm_head_argument_checks(lib):
     assert lib.svf_spec_accept_lmhead(*args) == sv.SVF_ERR_UNSUPPORTED   # V beyond on-chip
     args = [P] * 7 + [2, 3, 64, 1000] + [P] * 4 + [None, None, None, None]
     assert lib.svf_spec_accept_lmhead(*args) == sv.SVF_ERR_ARG           # no status
+
+
+def test_debug_hooks(lib):
+    import speculative_decoding_tree_03_gb300 as sv
+    assert lib.svf_debug_set_attn_splits(9) == sv.SVF_ERR_ARG
+    assert lib.svf_debug_set_attn_splits(-1) == sv.SVF_ERR_ARG
+    assert lib.svf_debug_set_attn_splits(0) == sv.SVF_OK
+    assert lib.svf_debug_set_attn_wait_ns(0) == sv.SVF_OK

@@ -35,3 +35,35 @@ def test_wait_runs_out_and_reports(sv, deadline_s):
     o_anc, o_depth, _ = oracle.tree_mask(parent)
     assert (anc.cpu().numpy().view(np.uint64) == o_anc).all()
     assert (depth.cpu().numpy() == o_depth).all() and int(status.sum()) == 0
+
+
+def test_attention_wait_runs_out_and_the_next_call_is_exact(sv):
+    """The tensor-core attention kernel with a 1 ns wait deadline: its first
+    wait that is not already complete gives up, the CTA drains its copies and
+    tensor-core operations in flight, releases its tensor memory, and every
+    sequence reports SVF_DEV_TIMEOUT -- with one chunk per unit and with
+    chunks merged in a cluster. With the default deadline restored, the next
+    call on the same inputs matches the oracle (so tensor memory was freed:
+    a leaked allocation would stall every later CTA's allocation)."""
+    from test_gpu_parity import _attn_case, _run_attn, BF16_OUT_TOL, BF16_LSE_TOL
+    from synth import binary_tree_parent
+    lib = sv.load_library()
+    B = 3
+    parent = np.broadcast_to(binary_tree_parent(4), (B, 31)).copy()
+    c = _attn_case(41, B, 31, parent, [2500, 800, 1700], 32, 8, 128, "bf16", 16)
+    try:
+        for splits in (1, 3):
+            assert lib.svf_debug_set_attn_splits(splits) == 0
+            assert lib.svf_debug_set_attn_wait_ns(1) == 0
+            _, _, status = _run_attn(sv, c, "bf16")
+            assert ((status & 16) != 0).all(), status
+            assert ((status & ~16) == 0).all(), status
+            assert lib.svf_debug_set_attn_wait_ns(0) == 0
+            out, lse, status = _run_attn(sv, c, "bf16")
+            assert (status == 0).all()
+            o_ref, l_ref = oracle.tree_attn(c["q"], c["K"], c["V"], c["lens"], c["parent"])
+            assert np.abs(out - o_ref.reshape(out.shape)).max() <= BF16_OUT_TOL
+            assert np.abs(lse - l_ref.reshape(lse.shape)).max() <= BF16_LSE_TOL
+    finally:
+        lib.svf_debug_set_attn_wait_ns(0)
+        lib.svf_debug_set_attn_splits(0)

@@ -486,3 +486,65 @@ def test_verify_step_tiny_chain(sv):
     arrs = _arrays(inp)
     compare_accept({k: (_np(v) if v is not None else None) for k, v in res.items()}, arrs,
                    oracle.spec_accept(**arrs))
+
+
+# ---------------------------------------------------------------------------
+# every chunk count (cluster size) on the same inputs
+# ---------------------------------------------------------------------------
+
+SPLIT_CASES = [
+    # mixed lengths: short sequences leave some of a cluster's chunks empty
+    ("bf16_mixed_lengths", 13, 10, "chain16",
+     [40, 900, 120, 2000, 333, 64, 1500, 7, 250, 1100], 32, 8, 128, "bf16", 16),
+    # one tile per sequence: every chunk but the first is empty
+    ("single_node_no_prefix", 4, 2, "single", [0, 5], 4, 4, 128, "bf16", 128),
+    # two row blocks of two halves, the tree inside the last tile
+    ("random60_paged32_rowblocks", 3, 2, "random60", [700, 250], 8, 1, 128, "bf16", 32),
+    ("binary31_g8_two_halves", 21, 3, "binary4", [3000, 65, 1200], 64, 8, 128, "bf16", 16),
+]
+
+
+@pytest.fixture
+def force_splits(sv):
+    lib = sv.load_library()
+    yield lambda s: lib.svf_debug_set_attn_splits(s)
+    lib.svf_debug_set_attn_splits(0)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+def test_attention_every_cluster_size(sv, force_splits, splits, case):
+    name, seed, B, pk, lens, Hq, Hkv, D, dtype, ps = case
+    assert force_splits(splits) == 0
+    parent = _parent_of(pk, B, np.random.default_rng(seed + 100))
+    N = parent.shape[1]
+    c = _attn_case(seed, B, N, parent, lens, Hq, Hkv, D, dtype, ps)
+    out, lse, status = _run_attn(sv, c, dtype)
+    assert (status == 0).all()
+    o_ref, l_ref = oracle.tree_attn(c["q"], c["K"], c["V"], c["lens"], c["parent"])
+    err_o = np.abs(out - o_ref.reshape(out.shape)).max()
+    err_l = np.abs(lse - l_ref.reshape(lse.shape)).max()
+    print(f"{name} splits={splits}: max|out-ref| {err_o:.3g} max|lse-ref| {err_l:.3g}")
+    assert err_o <= BF16_OUT_TOL and err_l <= BF16_LSE_TOL
+
+
+@pytest.mark.parametrize("splits", [1, 2, 4, 8])
+def test_attention_bad_inputs_every_cluster_size(sv, force_splits, splits):
+    """A bad page id or a bad length zeroes that sequence's outputs (and sets
+    its status) whatever the chunk count; the other sequences stay exact."""
+    assert force_splits(splits) == 0
+    B = 4
+    parent = np.broadcast_to(binary_tree_parent(3), (B, 15)).copy()
+    c = _attn_case(31, B, 15, parent, [900, 700, 1300, 400], 16, 4, 128, "bf16", 16)
+    c["table"][1, 20] = c["P"] + 5          # a page id outside the cache
+    lens = c["lens"].copy()
+    lens[2] = 10 ** 6                        # longer than the page table
+    c2 = dict(c, lens=lens)
+    out, lse, status = _run_attn(sv, c2, "bf16")
+    assert status.tolist() == [0, 4, 8, 0]
+    for b in (1, 2):
+        assert (out[b] == 0).all() and (lse[b] == 0).all()
+    good = [0, 3]
+    o_ref, _ = oracle.tree_attn(c["q"][good], c["K"][good], c["V"][good], c["lens"][good],
+                                c["parent"][good])
+    assert np.abs(out[good] - o_ref.reshape(out[good].shape)).max() <= BF16_OUT_TOL
