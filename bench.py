@@ -472,6 +472,62 @@ def time_step(r: StepRunner, steps, warmup, barrier, stream, clk=None):
     return res
 
 
+def time_lm_head(sv, torch, w, dev, steps, peak, fused_inputs=None):
+    """The LM head of the workload's target layer: R = B*N hidden rows of size
+    H = Hq*D (the model's hidden size) against a [V, H] bf16 weight, fp32
+    logits out; each call timed alone with CUDA events, the L2 flushed
+    between calls. With ``fused_inputs`` (draft logits, tokens, parent,
+    uniforms on the device) the fused LM head + walk call is timed too."""
+    R, H, V = w.B * w.N, w.Hq * w.D, w.V
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4321)
+    hidden = torch.randn((w.B, w.N, H), generator=gen, device=dev).to(torch.bfloat16)
+    weight = (torch.randn((V, H), generator=gen, device=dev) * (3.0 / math.sqrt(H))).to(
+        torch.bfloat16)
+    logits = torch.empty((w.B, w.N, V), dtype=torch.float32, device=dev)
+    status = torch.zeros((1,), dtype=torch.int32, device=dev)
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(b) for a, b in ts) / steps
+
+    ms = timed(lambda: sv.lm_head(hidden, weight, logits=logits, status=status))
+    assert int(status.item()) == 0 and bool(torch.isfinite(logits).all())
+    burst, sustained, kind = measured_tensor_peak()
+    flops = 2.0 * R * H * V
+    nbytes = V * H * 2 + R * H * 2 + R * V * 4
+    out = {"ms": ms, "R": R, "H": H, "V": V, "flops": flops, "tflops": flops / ms / 1e9,
+           "frac_of_bf16_sustained": flops / ms / 1e9 / sustained,
+           "frac_of_bf16_burst": flops / ms / 1e9 / burst, "peak_kind": kind,
+           "bytes": nbytes, "gbs": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / peak,
+           "bytes_note": "weight read once, hidden states read, fp32 logits written",
+           "inputs": "seeded random bf16 hidden states N(0,1) and weight N(0, 9/H)"}
+    if fused_inputs is not None:
+        fo = {}
+        f = fused_inputs
+        ms_f = timed(lambda: sv.spec_accept_lmhead(hidden, weight, f["draft"], f["tokens"],
+                                                   f["parent"], f["u_accept"], f["u_bonus"],
+                                                   outputs=fo))
+        assert int(fo["status"].abs().sum()) == 0 and int(fo["lm_status"].item()) == 0
+        out["fused_with_walk_ms"] = ms_f
+    del hidden, weight, logits, flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def workload_summary(r: StepRunner, t: dict, peak, clocks):
     """Attention and acceptance times of one workload with their roofline shares."""
     w, inp = r.w, r.inp
@@ -547,6 +603,9 @@ def run_ours(args, w, idx):
                     torch.cuda.synchronize(dev)
             r2.check()
             per_workload[w2.name] = workload_summary(r2, t2, peak, clk2.summary())
+            if w2.dtype == "bf16":
+                per_workload[w2.name]["lm_head"] = time_lm_head(sv, torch, w2, dev,
+                                                                args.steps, peak)
             r2.free()
             del r2, inp2
 
@@ -661,6 +720,9 @@ def run_ours(args, w, idx):
     def onehot_bf16_call(s):
         sv.spec_accept_onehot(bf_logits["target"], s["tokens"], s["parent"], s["u_accept"],
                               s["u_bonus"], outputs=var_out["onehot_bf16"])
+
+    lm = time_lm_head(sv, torch, w, dev, args.steps, peak, fused_inputs=r.base) \
+        if bf else None
 
     var_ms = {}
     for name, fn in (("greedy", greedy_call), ("onehot", onehot_call), ("eagle2", eagle2_call),
@@ -847,6 +909,7 @@ def run_ours(args, w, idx):
                           "bytes_note": "K and V rows of accepted nodes not yet in place, "
                                         "read and written, one layer"},
             **var_kernels,
+            **({"lm_head": lm} if lm is not None else {}),
         },
         "roofline": {
             "bound": "hbm",
