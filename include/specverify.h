@@ -67,7 +67,10 @@ enum svf_device_status {
     SVF_DEV_BAD_PAGE = 4,   /* a needed page id outside [0, num_pages) */
     SVF_DEV_BAD_LENGTH = 8, /* seq_lens[b] < 0 or the sequence overflows its page table */
     SVF_DEV_TIMEOUT = 16,   /* an internal wait gave up (the outputs of b are undefined) */
-    SVF_DEV_BAD_PATH = 32   /* accept_len or path[b] is not a root path in BFS order */
+    SVF_DEV_BAD_PATH = 32,  /* accept_len or path[b] is not a root path in BFS order */
+    SVF_DEV_BAD_CLUSTER = 64 /* a kernel ran without the thread-block cluster it was
+                                launched for (e.g. re-launched by a tool that drops the
+                                cluster attribute); it did no work, outputs undefined */
 };
 
 /* ------------------------------------------------------------------------

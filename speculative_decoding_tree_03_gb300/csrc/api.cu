@@ -51,6 +51,7 @@ const char *svf_status_string(int code) {
         case SVF_DEV_BAD_LENGTH: return "device: sequence length outside its page table";
         case SVF_DEV_TIMEOUT: return "device: an internal wait timed out";
         case SVF_DEV_BAD_PATH: return "device: accepted path is not a root path in BFS order";
+        case SVF_DEV_BAD_CLUSTER: return "device: kernel ran without its thread-block cluster";
         default: return "unknown status";
     }
 }

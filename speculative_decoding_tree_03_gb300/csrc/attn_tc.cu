@@ -73,6 +73,7 @@ __host__ __device__ constexpr int sbuffers_for(int NH) { return NH == 1 ? 4 : 2;
 constexpr int kFixedTiles = 3;              // prologue + epilogue cost, in tiles
 constexpr float kMergeTiles = 1.5f;         // the in-cluster merge, in tiles
 constexpr int kMaxSplits = 8;               // cluster size (portable limit)
+constexpr int kMinChunkTiles = 4;           // smallest chunk worth a cluster
 // Warps: a K and a V producer, a QK issuer and a PV issuer per half, four
 // softmax warps per half. One thread issuing tcgen05.mma (or TMA copies)
 // sustains about one instruction per 100 cycles; several issuing warps
@@ -191,6 +192,13 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     // One CTA per sequence owns its status word and stores it whole; other
     // CTAs only add SVF_DEV_TIMEOUT, which takes seconds to arise.
     const bool designated = g == 0 && rb == 0 && split == 0;
+    if (!cluster_shape_is(1u, p.splits > 1 ? (uint32_t)p.splits : 1u, 1u)) {
+        // not the cluster the merge addresses (the chunks of one unit along
+        // y): the whole cluster leaves at once, touching no peer
+        pdl_wait();
+        if (threadIdx.x == 0) atomicOr(&p.status[b], SVF_DEV_BAD_CLUSTER);
+        return;
+    }
     // On-chip set-up first: it overlaps the previous kernel's tail.
     if (threadIdx.x == 0) {
         for (int s2 = 0; s2 < KS; ++s2) {
@@ -870,6 +878,9 @@ int attn_tc_splits(int B, int N, int Hq, int Hkv, int max_pages, int page_size) 
     for (int s = 1; s <= tc::kMaxSplits; ++s) {
         const int per_cta = (tiles + s - 1) / s;
         if (per_cta > tc::CMAX_TILES) continue;
+        // chunks of a few tiles cost more in merge and co-scheduling than
+        // they save
+        if (s > 1 && per_cta < tc::kMinChunkTiles) break;
         const int cap = resident_ctas(NH, s);
         const double fixed = tc::kFixedTiles + (s > 1 ? tc::kMergeTiles : 0.0);
         const long long waves = (units * s + cap - 1) / cap;

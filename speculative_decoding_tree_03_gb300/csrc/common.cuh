@@ -221,6 +221,17 @@ __device__ __forceinline__ void tma_load_2d_multicast(void *dst, const void *tma
         : "memory");
 }
 
+// True when this CTA's cluster is exactly x by y by z CTAs (a non-cluster
+// launch is a cluster of 1 x 1 x 1). Every CTA of one cluster gets the same
+// answer.
+__device__ __forceinline__ bool cluster_shape_is(uint32_t x, uint32_t y, uint32_t z) {
+    uint32_t a, b, c;
+    asm volatile("mov.u32 %0, %%cluster_nctaid.x;" : "=r"(a));
+    asm volatile("mov.u32 %0, %%cluster_nctaid.y;" : "=r"(b));
+    asm volatile("mov.u32 %0, %%cluster_nctaid.z;" : "=r"(c));
+    return a == x && b == y && c == z;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -88,6 +88,13 @@ __global__ void __launch_bounds__(lmh::THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (!cluster_shape_is((uint32_t)p.C, 1u, 1u)) {
+        // not the cluster the multicasts address: the whole cluster leaves
+        // at once, touching no peer
+        pdl_wait();
+        if (threadIdx.x == 0 && p.status) atomicOr(p.status, SVF_DEV_BAD_CLUSTER);
+        return;
+    }
     const uint32_t rank = p.C > 1 ? cluster_ctarank() : 0u;
     const uint16_t mask = (uint16_t)((1u << p.C) - 1u);
     const int cluster_id = blockIdx.x / p.C;
