@@ -34,10 +34,11 @@
 // Chunks of the KV range: the S CTAs of one (sequence, KV head, row block)
 // form a thread-block cluster; each takes an equal share of that sequence's
 // own tiles (from seq_lens, not from the page-table capacity). At the end
-// they merge through distributed shared memory: every CTA publishes its
-// rows' log-sum-exp, scales its O rows by their merge weights into shared
-// memory, and each CTA sums a share of the rows over the cluster and writes
-// the final bf16 output. Nothing goes through global memory and no second
+// they merge through distributed shared memory: every CTA writes its rows'
+// log-sum-exp and normalised partial O rows into its own shared memory, one
+// cluster barrier publishes them, and each CTA merges a share of the rows
+// from the whole cluster (remote loads issued together) and writes the
+// final bf16 output. Nothing goes through global memory and no second
 // kernel runs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -584,9 +585,9 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         tc_fence_after();
         if (p.splits > 1) {
             // the merge reads O from tensor memory later; publish this row's
-            // log2-sum-exp and the reference max O is scaled by
+            // log2-sum-exp and the normalisation 1/l
             s_lse[h * 128 + r] = (ok && l > 0.0f) ? m_ref + __log2f(l) : -INFINITY;
-            s_fin[h * 128 + r] = m_ref;
+            s_fin[h * 128 + r] = l > 0.0f ? 1.0f / l : 0.0f;
         }
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const float lse_v = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -641,50 +642,20 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         const uint32_t rank = cluster_ctarank();
         const int S2 = p.splits;
         constexpr int RB = 128 * NH;
-        float4 *sO = reinterpret_cast<float4 *>(sK);  // [RB][32] weighted O rows, swizzled
+        float4 *sO = reinterpret_cast<float4 *>(sK);  // [RB][32] normalised O rows, swizzled
         if (threadIdx.x == 0) {
             m_flag[0] = *abort_flag ? 0 : 1;
             m_flag[1] = bad;
         }
-        cluster_arrive();
-        cluster_wait();
-        if (threadIdx.x == 0) {
-            int zero = len_ok ? 0 : 1;
-            for (int s2 = 0; s2 < S2; ++s2) {
-                zero |= ld_dsmem_s32(cluster_map(&m_flag[0], (uint32_t)s2)) == 0;
-                zero |= ld_dsmem_s32(cluster_map(&m_flag[1], (uint32_t)s2)) != 0;
-            }
-            m_flag[2] = zero;
-        }
         if (warp >= SW0) {
-            // the softmax role's row: half h, TMEM lane quarter (warp & 3)
+            // the softmax role's row: half h, TMEM lane quarter (warp & 3);
+            // s_lse holds its log2-sum-exp (-inf: no column here) and s_fin
+            // 1 / l from the epilogue. Tensor-memory loads are warp-wide.
             const int lr = ((warp - SW0) >> 2) * 128 + (warp & 3) * 32 + lane;
-            float lv[kMaxSplits];
-            float lmax = -INFINITY;
-#pragma unroll
-            for (int s2 = 0; s2 < kMaxSplits; ++s2) {
-                lv[s2] = s2 < S2 ? ld_dsmem_f32(cluster_map(&s_lse[lr], (uint32_t)s2)) : -INFINITY;
-                lmax = fmaxf(lmax, lv[s2]);
-            }
-            float W = 0.0f;
-            uint32_t mask = 0;
-#pragma unroll
-            for (int s2 = 0; s2 < kMaxSplits; ++s2)
-                if (lv[s2] != -INFINITY) {
-                    W += ex2_approx(lv[s2] - lmax);
-                    mask |= 1u << s2;
-                }
-            const float m_mine = s_fin[lr];
-            s_fin[lr] = mask ? lmax + __log2f(W) : -INFINITY;
-            s_mask[lr] = mask;
-            // a row may see no column of this chunk (its rank bit is then
-            // clear); the tensor-memory loads are warp-wide, so a warp loads
-            // when any of its rows contributes and only those rows store
-            const bool contrib = (mask >> rank) & 1u;
+            const bool contrib = n > 0 && s_lse[lr] != -INFINITY;
             tc_fence_after();
             if (__any_sync(FULL, contrib)) {
-                // O_mine * 2^(m_mine - lmax) / W: this chunk's share of the row
-                const float sc = contrib ? ex2_approx(m_mine - lmax) / W : 0.0f;
+                const float inv = contrib ? s_fin[lr] : 0.0f;
                 const uint32_t tO = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256 +
                                     (uint32_t)((lr >> 7) * 128);
 #pragma unroll 1
@@ -696,10 +667,10 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             sO[lr * 32 + ((c4 * 8 + k) ^ (lr & 31))] =
-                                make_float4(__uint_as_float(o[4 * k]) * sc,
-                                            __uint_as_float(o[4 * k + 1]) * sc,
-                                            __uint_as_float(o[4 * k + 2]) * sc,
-                                            __uint_as_float(o[4 * k + 3]) * sc);
+                                make_float4(__uint_as_float(o[4 * k]) * inv,
+                                            __uint_as_float(o[4 * k + 1]) * inv,
+                                            __uint_as_float(o[4 * k + 2]) * inv,
+                                            __uint_as_float(o[4 * k + 3]) * inv);
                     }
                 }
             }
@@ -707,27 +678,70 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         tc_fence_before();
         cluster_arrive();
         cluster_wait();
-        // rows lr = rank, rank + S, ... of this row block: sum the cluster's
-        // shares, 16 bytes of a row per thread
-        const bool zero = m_flag[2] != 0;
+        // rows lr = rank + o S of this row block. First the merge weights of
+        // each row, from the cluster's log-sum-exps (into the free Q area)
+        float *wgt = reinterpret_cast<float *>(sQ);  // [nrows][kMaxSplits]
         const int nrows = (RB - (int)rank + S2 - 1) / S2;
+        if (threadIdx.x == 0) {
+            int fl[2 * kMaxSplits];
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                fl[2 * s2] = s2 < S2 ? ld_dsmem_s32(cluster_map(&m_flag[0], (uint32_t)s2)) : 1;
+                fl[2 * s2 + 1] = s2 < S2 ? ld_dsmem_s32(cluster_map(&m_flag[1], (uint32_t)s2)) : 0;
+            }
+            int zero = len_ok ? 0 : 1;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxSplits; ++s2) zero |= (fl[2 * s2] == 0) | (fl[2 * s2 + 1] != 0);
+            m_flag[2] = zero;
+        }
+        for (int o = threadIdx.x; o < nrows; o += NTHREADS) {
+            const int lr = (int)rank + o * S2;
+            float lv[kMaxSplits];
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxSplits; ++s2)
+                lv[s2] = s2 < S2 ? ld_dsmem_f32(cluster_map(&s_lse[lr], (uint32_t)s2)) : -INFINITY;
+            float lmax = -INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxSplits; ++s2) lmax = fmaxf(lmax, lv[s2]);
+            float W = 0.0f;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                lv[s2] = lv[s2] == -INFINITY ? 0.0f : ex2_approx(lv[s2] - lmax);
+                W += lv[s2];
+            }
+            const float winv = W > 0.0f ? 1.0f / W : 0.0f;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxSplits; ++s2) wgt[o * kMaxSplits + s2] = lv[s2] * winv;
+            s_mask[o] = __float_as_uint(W > 0.0f ? lmax + __log2f(W) : -INFINITY);
+        }
+        __syncthreads();
+        // then 16 bytes of a row per thread: the row's chunk from every CTA
+        // that saw the row, loaded together
+        const bool zero = m_flag[2] != 0;
         for (int it = threadIdx.x; it < nrows * 32; it += NTHREADS) {
-            const int lr = (int)rank + (it >> 5) * S2;
+            const int o = it >> 5;
+            const int lr = (int)rank + o * S2;
             const int c = it & 31;
             const int Rg = rb * RB + lr;
             if (Rg >= p.M) continue;
-            const uint32_t mask = s_mask[lr];
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (!zero) {
-                for (int s2 = 0; s2 < S2; ++s2)
-                    if ((mask >> s2) & 1u) {
-                        const float4 v = ld_dsmem_v4(
-                            cluster_map(&sO[lr * 32 + (c ^ (lr & 31))], (uint32_t)s2));
-                        acc.x += v.x;
-                        acc.y += v.y;
-                        acc.z += v.z;
-                        acc.w += v.w;
-                    }
+                const uint32_t src = smem_u32(&sO[lr * 32 + (c ^ (lr & 31))]);
+                float4 v[kMaxSplits];
+                float w[kMaxSplits];
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                    w[s2] = s2 < S2 ? wgt[o * kMaxSplits + s2] : 0.0f;
+                    v[s2] = w[s2] > 0.0f ? ld_dsmem_v4(cluster_map_addr(src, (uint32_t)s2))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+                    acc.x = fmaf(w[s2], v[s2].x, acc.x);
+                    acc.y = fmaf(w[s2], v[s2].y, acc.y);
+                    acc.z = fmaf(w[s2], v[s2].z, acc.z);
+                    acc.w = fmaf(w[s2], v[s2].w, acc.w);
+                }
             }
             const size_t row = ((size_t)b * p.N + Rg / p.G) * p.Hq + g * p.G + Rg % p.G;
             uint2 w2;
@@ -735,7 +749,7 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
             w2.y = pack_bf16x2(acc.z, acc.w);
             *reinterpret_cast<uint2 *>(p.out + row * HD + c * 4) = w2;
             if (c == 0 && p.lse)
-                p.lse[row] = zero ? 0.0f : s_fin[lr] * 0.69314718055994531f;
+                p.lse[row] = zero ? 0.0f : __uint_as_float(s_mask[o]) * 0.69314718055994531f;
         }
         // no CTA leaves while a peer may still read its shared memory
         cluster_arrive();

@@ -143,6 +143,14 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     return mbar_wait_cluster_for(bar, parity, kWaitDeadlineNs);
 }
 
+// The same shared-memory address (as a 32-bit shared::cta address) in CTA
+// `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_map_addr(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
 // Loads from another CTA's shared memory (an address from cluster_map).
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     float v;
