@@ -342,21 +342,24 @@ class StepRunner:
         self.sv.tree_mask_build(s["parent"], self.anc, self.depth, self.mstat)
 
     def attn_call(self, s):
-        self.sv.tree_verify_attn(s["q"], s["k"], s["v"], s["page_table"], s["seq_lens"],
-                                 self.anc, out=self.out, lse=self.lse, workspace=self.attn_ws,
-                                 status=self.astat)
+        # ancestor masks and attention in one call (one kernel for bf16)
+        self.sv.tree_mask_attn(s["parent"], s["q"], s["k"], s["v"], s["page_table"],
+                               s["seq_lens"], anc=self.anc, depth=self.depth,
+                               mask_status=self.mstat, out=self.out, lse=self.lse,
+                               workspace=self.attn_ws, status=self.astat)
 
     def accept_call(self, s):
         self.sv.spec_accept(s["target"], s["draft"], s["tokens"], s["parent"], s["u_accept"],
                             s["u_bonus"], workspace=self.acc_ws, outputs=self.acc_out)
 
     def step(self, s):
-        self.mask_call(s)
         self.attn_call(s)
         self.accept_call(s)
 
     def launches_per_step(self):
-        return 1 + 1 + (1 if self.attn_ws_need > 0 else 0) + (2 if self.acc_ws_need > 0 else 1)
+        # fused masks + attention: one kernel for bf16, mask + attention for fp32
+        attn = 1 if self.w.dtype == "bf16" else 2
+        return attn + (2 if self.acc_ws_need > 0 else 1)
 
     def capture(self, fn, s):
         g = self.torch.cuda.CUDAGraph()
@@ -365,23 +368,21 @@ class StepRunner:
         return g
 
     def capture_instrumented(self, s):
-        """The step graph with a timing event before, between and after its three
+        """The step graph with a timing event before, between and after its two
         calls (events of external kind, so that replays can be timed), or None
         where this PyTorch cannot record such events in a graph."""
         torch = self.torch
         try:
-            evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+            evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
         except TypeError:
             return None
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=self.cap):
             evs[0].record()
-            self.mask_call(s)
-            evs[1].record()
             self.attn_call(s)
-            evs[2].record()
+            evs[1].record()
             self.accept_call(s)
-            evs[3].record()
+            evs[2].record()
         return g, evs
 
     def check(self):
@@ -400,11 +401,12 @@ def time_step(r: StepRunner, steps, warmup, barrier, stream, clk=None):
     """Step time from replays of one CUDA graph per input set, and per-kernel
     times inside the step from the instrumented capture.
 
-    Returns a dict: ``ms`` per step (plain graphs), ``in_step`` ms of the mask,
-    attention (with its split merge) and acceptance calls and their total
-    inside one instrumented step (its events sit between the kernels, so the
-    dependent-launch overlap of the plain graph is lost there), and
-    ``single_call`` ms of each call captured and replayed alone."""
+    Returns a dict: ``ms`` per step (plain graphs), ``in_step`` ms of the
+    fused masks + attention call (with its split merge) and of the acceptance
+    call, and their total inside one instrumented step (its events sit
+    between the kernels, so the dependent-launch overlap of the plain graph
+    is lost there), and ``single_call`` ms of each call captured and
+    replayed alone (the stand-alone mask build included)."""
     torch = r.torch
     for i in range(warmup):
         r.step(r.sets[i % r.nsets])
@@ -437,16 +439,15 @@ def time_step(r: StepRunner, steps, warmup, barrier, stream, clk=None):
     # per-kernel times inside the step
     inst = [r.capture_instrumented(s) for s in r.sets]
     if inst[0] is not None:
-        acc = np.zeros(4)
+        acc = np.zeros(3)
         for i in range(steps):
             g, evs = inst[i % r.nsets]
             g.replay()
             torch.cuda.synchronize(r.dev)
             acc += [evs[0].elapsed_time(evs[1]), evs[1].elapsed_time(evs[2]),
-                    evs[2].elapsed_time(evs[3]), evs[0].elapsed_time(evs[3])]
+                    evs[0].elapsed_time(evs[2])]
         acc /= steps
-        res["in_step"] = {"mask_ms": acc[0], "attn_ms": acc[1], "accept_ms": acc[2],
-                          "total_ms": acc[3],
+        res["in_step"] = {"attn_ms": acc[0], "accept_ms": acc[1], "total_ms": acc[2],
                           "method": "timing events captured between the calls of the step "
                                     "graph; replayed per input set"}
     # each call captured alone, replayed back to back with events around it
@@ -463,9 +464,8 @@ def time_step(r: StepRunner, steps, warmup, barrier, stream, clk=None):
         single[name + "_ms"] = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
     res["single_call"] = single
     if "in_step" not in res:
-        res["in_step"] = {"mask_ms": single["mask_ms"], "attn_ms": single["attn_ms"],
-                          "accept_ms": single["accept_ms"],
-                          "total_ms": single["mask_ms"] + single["attn_ms"] + single["accept_ms"],
+        res["in_step"] = {"attn_ms": single["attn_ms"], "accept_ms": single["accept_ms"],
+                          "total_ms": single["attn_ms"] + single["accept_ms"],
                           "method": "single-call graphs (this PyTorch records no timing "
                                     "events inside a graph)"}
     g_step.clear()
@@ -553,7 +553,7 @@ def workload_summary(r: StepRunner, t: dict, peak, clocks):
         "accept_visited_nodes": nodes,
         "accept_us_per_visited_node": ins["accept_ms"] * 1e3 / nodes,
         "accept_us_per_visited_node_per_sequence": ins["accept_ms"] * 1e3 * w.B / nodes,
-        "mask_us": ins["mask_ms"] * 1e3,
+        "mask_alone_us": t["single_call"]["mask_ms"] * 1e3,
         "in_step_total_us": ins["total_ms"] * 1e3,
         "single_call_us": {k.replace("_ms", ""): v * 1e3 for k, v in t["single_call"].items()},
         "clocks": clocks,
@@ -875,14 +875,14 @@ def run_ours(args, w, idx):
             "l2": f"inputs rotate over {r.nsets} copies ({r.nsets * r.step_bytes / 1e6:.0f} MB "
                   f"> L2 {r.l2 / 1e6:.0f} MB)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "launch": "one CUDA graph per step (masks, attention, acceptance)",
+            "launch": "one CUDA graph per step: masks + attention (one fused call), acceptance",
             "e2e_copies": "one packed pinned host-to-device copy per step, issued one step "
                           "ahead on a side stream; outputs read back every step",
         },
         "accept_steps_per_s": rsum(B) / (ms / 1e3),
         "graph_100_steps": {"ms_per_step": ms100, "value": rsum(B * N) / (ms100 / 1e3),
                             "note": "100 steps captured as one CUDA graph"},
-        "in_step": {"mask_us": ins["mask_ms"] * 1e3, "attn_us": attn_ms * 1e3,
+        "in_step": {"attn_us": attn_ms * 1e3,
                     "accept_us": acc_ms * 1e3, "total_us": ins["total_ms"] * 1e3,
                     "step_us": ms * 1e3, "method": ins["method"],
                     "note": "the plain step graph launches its kernels with programmatic "
@@ -902,8 +902,9 @@ def run_ours(args, w, idx):
                             "bytes_all_rows": nb["accept_bytes"],
                             "bytes_note": "rows of the visited nodes; bytes_all_rows counts "
                                           "every row a walk could test"},
-            "tree_mask_build": {"ms": ins["mask_ms"],
-                                "single_call_ms": t["single_call"]["mask_ms"]},
+            "tree_mask_build": {"in_step": "built inside the fused attention call",
+                                "single_call_ms": t["single_call"]["mask_ms"],
+                                "note": "svf_tree_mask_build alone, captured and replayed"},
             "kv_commit": {"ms": commit_ms, "bytes": commit_bytes, "gbs": commit_gbs,
                           "frac_of_hbm": commit_gbs / peak, "rows_moved": rows_moved,
                           "bytes_note": "K and V rows of accepted nodes not yet in place, "

@@ -144,6 +144,30 @@ int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache
                          svf_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * svf_tree_mask_attn -- svf_tree_mask_build and svf_tree_verify_attn in one
+ * call: the ancestor masks are built from parent[] where the attention needs
+ * them ("EAGLE 演化史", § Tree Verification 详解, B: a node sees its
+ * ancestors and itself; A: one pass verifies the whole tree).
+ *
+ * Arguments are those of the two calls: parent [B, N] int32 in; anc
+ * [B, N, 1] uint64, depth [B, N] int32 and mask_status [B] int32 get exactly
+ * what svf_tree_mask_build writes (for SVF_BF16 each may be NULL; for
+ * SVF_F32 anc and mask_status are required, since that path reads the masks
+ * from memory); the attention arguments and outputs are svf_tree_verify_attn's
+ * (its anc argument is replaced by parent; workspace sizes are the same).
+ * For SVF_BF16 one kernel does both: its prologue checks the tree and walks
+ * every node's parent links in shared memory. Limits: those of
+ * svf_tree_verify_attn (N <= 64).
+ * ---------------------------------------------------------------------- */
+int svf_tree_mask_attn(const int32_t *parent, uint64_t *anc, int32_t *depth,
+                       int32_t *mask_status, const void *q, const void *k_cache,
+                       const void *v_cache, int num_pages, int page_size,
+                       const int32_t *page_table, int max_pages, const int32_t *seq_lens, int B,
+                       int N, int Hq, int Hkv, int D, int dtype, float sm_scale, void *out,
+                       float *lse, void *workspace, size_t workspace_bytes, int32_t *status,
+                       svf_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * svf_spec_accept -- lossless acceptance walk over the verified tree.
  *
  * Follows "Eagle vs DFlash" (accept x with probability min(1, p(x)/q(x));

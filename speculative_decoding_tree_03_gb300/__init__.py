@@ -34,6 +34,7 @@ EXPORTED = [
     "svf_tree_mask_build",
     "svf_tree_verify_attn_workspace_size",
     "svf_tree_verify_attn",
+    "svf_tree_mask_attn",
     "svf_spec_accept_workspace_size",
     "svf_spec_accept",
     "svf_spec_accept_noalloc",
@@ -79,6 +80,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_tree_verify_attn.argtypes = [P, P, P, I, I, P, I, P, P, I, I, I, I, I, I, F, P, P, P,
                                          Z, P, P]
     lib.svf_tree_verify_attn.restype = I
+    lib.svf_tree_mask_attn.argtypes = [P, P, P, P, P, P, P, I, I, P, I, P, I, I, I, I, I, I, F,
+                                       P, P, P, Z, P, P]
+    lib.svf_tree_mask_attn.restype = I
     lib.svf_spec_accept_workspace_size.argtypes = [I, I, I]
     lib.svf_spec_accept_workspace_size.restype = Z
     lib.svf_spec_accept.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P, Z, P, P]
@@ -253,6 +257,65 @@ def tree_verify_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
     _check(rc, "svf_tree_verify_attn")
     return out, lse, status
+
+
+def tree_mask_attn(parent: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                   sm_scale: float = 0.0, anc: Optional[torch.Tensor] = None,
+                   depth: Optional[torch.Tensor] = None,
+                   mask_status: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None, want_lse: bool = True, stream=None):
+    """tree_mask_build and tree_verify_attn in one call (one kernel for
+    bfloat16). Returns (out, lse, status, anc, depth, mask_status)."""
+    lib = load_library()
+    _dev(q, "q")
+    B, N, Hq, D = q.shape
+    dt = q.dtype
+    _dev(parent, "parent", torch.int32, (B, N))
+    _dev(k_cache, "k_cache", dt)
+    num_pages, page_size, Hkv, Dk = k_cache.shape
+    if Dk != D:
+        raise SpecVerifyError("k_cache head_dim differs from q")
+    _dev(v_cache, "v_cache", dt, k_cache.shape)
+    _dev(page_table, "page_table", torch.int32)
+    if page_table.dim() != 2 or page_table.shape[0] != B:
+        raise SpecVerifyError("page_table must be [B, max_pages]")
+    max_pages = page_table.shape[1]
+    _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    dev = q.device
+    if anc is None:
+        anc = torch.empty((B, N, 1), dtype=torch.int64, device=dev)
+    _dev(anc, "anc", torch.int64, (B, N, 1))
+    if depth is None:
+        depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    _dev(depth, "depth", torch.int32, (B, N))
+    if mask_status is None:
+        mask_status = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev(mask_status, "mask_status", torch.int32, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", dt, q.shape)
+    if lse is None and want_lse:
+        lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _dev(lse, "lse", torch.float32, (B, N, Hq))
+    if status is None:
+        status = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev(status, "status", torch.int32, (B,))
+    code = _dtype_code(dt)
+    need = int(lib.svf_tree_verify_attn_workspace_size(B, N, Hq, Hkv, D, code, max_pages,
+                                                       page_size))
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.svf_tree_mask_attn(
+        _ptr(parent), _ptr(anc), _ptr(depth), _ptr(mask_status), _ptr(q), _ptr(k_cache),
+        _ptr(v_cache), num_pages, page_size, _ptr(page_table), max_pages, _ptr(seq_lens), B, N,
+        Hq, Hkv, D, code, float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+        _ptr(status), _stream(stream))
+    _check(rc, "svf_tree_mask_attn")
+    return out, lse, status, anc, depth, mask_status
 
 
 # ---------------------------------------------------------------------------
@@ -581,23 +644,23 @@ def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Te
 
 def verify_step(parent, tokens, q, k_cache, v_cache, page_table, seq_lens, target_logits,
                 draft_logits, u_accept, u_bonus, stream=None, buffers: Optional[dict] = None):
-    """The whole hot path on device tensors: ancestor masks, tree attention of
-    one layer, acceptance walk. ``buffers`` (optional) holds preallocated
-    outputs and workspaces and is filled on the first call."""
+    """The whole hot path on device tensors: ancestor masks and tree attention
+    of one layer (one fused call), then the acceptance walk. ``buffers``
+    (optional) holds preallocated outputs and workspaces and is filled on the
+    first call."""
     bufs = buffers if buffers is not None else {}
-    anc, depth, mstatus = tree_mask_build(parent, bufs.get("anc"), bufs.get("depth"),
-                                          bufs.get("mask_status"), stream)
-    bufs["anc"], bufs["depth"], bufs["mask_status"] = anc, depth, mstatus
-    out, lse, astatus = tree_verify_attn(q, k_cache, v_cache, page_table, seq_lens, anc,
-                                         out=bufs.get("attn_out"), lse=bufs.get("lse"),
-                                         workspace=bufs.get("attn_ws"),
-                                         status=bufs.get("attn_status"), stream=stream)
-    bufs["attn_out"], bufs["lse"], bufs["attn_status"] = out, lse, astatus
     if "attn_ws" not in bufs:
         B, N, Hq, D = q.shape
         need = tree_verify_attn_workspace_size(B, N, Hq, k_cache.shape[2], D, q.dtype,
                                                page_table.shape[1], k_cache.shape[1])
         bufs["attn_ws"] = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+    out, lse, astatus, anc, depth, mstatus = tree_mask_attn(
+        parent, q, k_cache, v_cache, page_table, seq_lens, anc=bufs.get("anc"),
+        depth=bufs.get("depth"), mask_status=bufs.get("mask_status"), out=bufs.get("attn_out"),
+        lse=bufs.get("lse"), workspace=bufs["attn_ws"], status=bufs.get("attn_status"),
+        stream=stream)
+    bufs["anc"], bufs["depth"], bufs["mask_status"] = anc, depth, mstatus
+    bufs["attn_out"], bufs["lse"], bufs["attn_status"] = out, lse, astatus
     if "acc_ws" not in bufs:
         B, N, V = target_logits.shape
         bufs["acc_ws"] = torch.empty((spec_accept_workspace_size(B, N, V),), dtype=torch.uint8,

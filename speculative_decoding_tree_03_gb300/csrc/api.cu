@@ -76,17 +76,19 @@ size_t svf_tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int D,
     return attn_tc_workspace_bytes(B, N, Hq, Hkv, max_pages, page_size);
 }
 
-int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache, int num_pages,
-                         int page_size, const int32_t *page_table, int max_pages,
-                         const int32_t *seq_lens, const uint64_t *anc, int B, int N, int Hq,
-                         int Hkv, int D, int dtype, float sm_scale, void *out, float *lse,
-                         void *workspace, size_t workspace_bytes, int32_t *status,
-                         svf_stream_t stream) {
+static int tree_attn_common(const void *q, const void *k_cache, const void *v_cache,
+                            int num_pages, int page_size, const int32_t *page_table,
+                            int max_pages, const int32_t *seq_lens, const uint64_t *anc,
+                            const int32_t *parent, uint64_t *anc_out, int32_t *depth_out,
+                            int32_t *mask_status, int B, int N, int Hq, int Hkv, int D, int dtype,
+                            float sm_scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, int32_t *status, svf_stream_t stream) {
     if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 ||
         max_pages <= 0)
         return SVF_ERR_ARG;
     if (B == 0) return SVF_OK;
-    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !anc || !out || !status)
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || (!anc && !parent) || !out ||
+        !status)
         return SVF_ERR_ARG;
     if (N < 1 || N > 64 || Hq % Hkv != 0) return SVF_ERR_UNSUPPORTED;
     if ((long long)num_pages * page_size > INT_MAX) return SVF_ERR_UNSUPPORTED;
@@ -101,6 +103,13 @@ int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache
     a.sm_scale = sm_scale; a.out = out; a.lse = lse; a.status = status;
     if (dtype == SVF_F32) {
         if (D != 64 && D != 128) return SVF_ERR_UNSUPPORTED;
+        if (parent) {
+            // the CUDA-core path reads the masks from memory: build them first
+            if (!anc_out || !mask_status) return SVF_ERR_ARG;
+            if (launch_tree_mask(parent, B, N, anc_out, depth_out, mask_status, s) != cudaSuccess)
+                return SVF_ERR_LAUNCH;
+            a.anc = anc_out;
+        }
         if (cudaMemsetAsync(status, 0, sizeof(int32_t) * (size_t)B, s) != cudaSuccess)
             return SVF_ERR_LAUNCH;
         return launch_attn_simt(a, s) == cudaSuccess ? SVF_OK : SVF_ERR_LAUNCH;
@@ -109,8 +118,37 @@ int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache
     if (D != 128 || !tc_page_size_ok(page_size)) return SVF_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return SVF_ERR_ARG;
+    a.parent = parent;
+    a.anc_out = anc_out;
+    a.depth_out = depth_out;
+    a.mask_status = mask_status;
     // the kernel stores every sequence's status word itself
     return launch_attn_tc(a, workspace, workspace_bytes, s);
+}
+
+int svf_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache, int num_pages,
+                         int page_size, const int32_t *page_table, int max_pages,
+                         const int32_t *seq_lens, const uint64_t *anc, int B, int N, int Hq,
+                         int Hkv, int D, int dtype, float sm_scale, void *out, float *lse,
+                         void *workspace, size_t workspace_bytes, int32_t *status,
+                         svf_stream_t stream) {
+    if (B > 0 && !anc) return SVF_ERR_ARG;
+    return tree_attn_common(q, k_cache, v_cache, num_pages, page_size, page_table, max_pages,
+                            seq_lens, anc, nullptr, nullptr, nullptr, nullptr, B, N, Hq, Hkv, D,
+                            dtype, sm_scale, out, lse, workspace, workspace_bytes, status, stream);
+}
+
+int svf_tree_mask_attn(const int32_t *parent, uint64_t *anc, int32_t *depth,
+                       int32_t *mask_status, const void *q, const void *k_cache,
+                       const void *v_cache, int num_pages, int page_size,
+                       const int32_t *page_table, int max_pages, const int32_t *seq_lens, int B,
+                       int N, int Hq, int Hkv, int D, int dtype, float sm_scale, void *out,
+                       float *lse, void *workspace, size_t workspace_bytes, int32_t *status,
+                       svf_stream_t stream) {
+    if (B > 0 && !parent) return SVF_ERR_ARG;
+    return tree_attn_common(q, k_cache, v_cache, num_pages, page_size, page_table, max_pages,
+                            seq_lens, nullptr, parent, anc, depth, mask_status, B, N, Hq, Hkv, D,
+                            dtype, sm_scale, out, lse, workspace, workspace_bytes, status, stream);
 }
 
 size_t svf_spec_accept_workspace_size(int B, int N, int V) {

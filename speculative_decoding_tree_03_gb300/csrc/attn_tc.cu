@@ -97,6 +97,10 @@ struct TcParams {
     __nv_bfloat16 *out;
     float *lse;
     int32_t *status;
+    const int32_t *parent;  // non-null: build the ancestor masks here (N <= 64)
+    uint64_t *anc_out;      // with parent: the masks written out (nullable)
+    int32_t *depth_out;     // nullable
+    int32_t *mask_status;   // nullable
 };
 
 template <int NH>
@@ -114,7 +118,9 @@ struct TcSmem {
     static constexpr int kLse = kMisc + 64;
     static constexpr int kFin = kLse + 128 * NH * 4;
     static constexpr int kMask = kFin + 128 * NH * 4;
-    static constexpr int kBytes = kMask + 128 * NH * 4;
+    // ancestor masks and parent[] of the sequence when built here (N <= 64)
+    static constexpr int kAnc = kMask + 128 * NH * 4;
+    static constexpr int kBytes = kAnc + 64 * 8 + 64 * 4;
     // weighted O rows of the merge reuse the K/V rings (free by then)
     static_assert(kCrd - kK >= 128 * NH * tc::HD * 4, "merge rows fit in the rings");
     static constexpr int kDynamic = kBytes + 1024;  // slack to align the base to 1 KB
@@ -233,6 +239,45 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
     }
     pdl_wait();
     pdl_launch_dependents();
+
+    uint64_t *s_anc = reinterpret_cast<uint64_t *>(smem + S::kAnc);
+    if (p.parent) {
+        // "EAGLE 演化史", § Tree Verification 详解, B: node i sees its
+        // ancestors and itself. parent[] of the sequence into shared memory
+        // with the tree check, then each thread walks one node's parent links
+        // to the root (parent[i] < i bounds the walk). An invalid tree gives
+        // every node only its own bit, as svf_tree_mask_build does. One CTA
+        // per sequence writes the masks, depths and mask status out.
+        int32_t *s_par = reinterpret_cast<int32_t *>(s_anc + 64);
+        const int i = threadIdx.x;
+        int badt = 0;
+        if (i < p.N) {
+            const int pp = p.parent[(size_t)b * p.N + i];
+            s_par[i] = pp;
+            badt = i == 0 ? pp != -1 : (pp < 0 || pp >= i);
+        }
+        badt = __syncthreads_or(badt);
+        if (i < p.N) {
+            uint64_t word = 1ull << i;
+            int d = 0;
+            if (!badt) {
+                d = -1;
+                word = 0;
+                for (int a = i; a != -1; a = s_par[a]) {
+                    word |= 1ull << a;
+                    ++d;
+                }
+            }
+            s_anc[i] = word;
+            if (designated) {
+                if (p.anc_out) p.anc_out[(size_t)b * p.N + i] = word;
+                if (p.depth_out) p.depth_out[(size_t)b * p.N + i] = d;
+            }
+        }
+        if (designated && i == 0 && p.mask_status)
+            p.mask_status[b] = badt ? SVF_DEV_BAD_PARENT : 0;
+        __syncthreads();
+    }
 
     const int L = p.seq_lens[b];
     const long long T = (long long)L + p.N;
@@ -488,7 +533,8 @@ __global__ void __launch_bounds__(tc::threads_for(NH), 1)
         const bool row_valid = R < p.M;
         const int node = row_valid ? R / p.G : 0;
         const int hq = g * p.G + (row_valid ? R % p.G : 0);
-        const uint64_t anc = row_valid ? p.anc[(size_t)b * p.N + node] : 0ull;
+        const uint64_t anc =
+            row_valid ? (p.parent ? s_anc[node] : p.anc[(size_t)b * p.N + node]) : 0ull;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tO = tmem + lane_off + 256 + h * 128;
         const float sl2 = p.scale_log2;
@@ -972,6 +1018,10 @@ int launch_attn_tc(const AttnArgs &a, void *, size_t, cudaStream_t stream) {
     p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
     p.lse = a.lse;
     p.status = a.status;
+    p.parent = a.parent;
+    p.anc_out = a.anc_out;
+    p.depth_out = a.depth_out;
+    p.mask_status = a.mask_status;
 
     dim3 grid(a.Hkv * row_blocks, splits, a.B);
     const unsigned cl = splits > 1 ? (unsigned)splits : 0u;

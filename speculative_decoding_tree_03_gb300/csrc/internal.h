@@ -94,6 +94,13 @@ struct AttnArgs {
     void *out;
     float *lse;
     int32_t *status;
+    // non-null: the ancestor masks are built from parent[] inside the
+    // tensor-core kernel (anc above is then ignored) and written out as
+    // svf_tree_mask_build writes them (each output nullable)
+    const int32_t *parent = nullptr;
+    uint64_t *anc_out = nullptr;
+    int32_t *depth_out = nullptr;
+    int32_t *mask_status = nullptr;
 };
 
 // CUDA-core path for fp32 (and any dtype): one warp per (sequence, node, head) (attn_simt.cu).

@@ -237,3 +237,20 @@ def test_debug_hooks(lib):
     assert lib.svf_debug_set_attn_splits(-1) == sv.SVF_ERR_ARG
     assert lib.svf_debug_set_attn_splits(0) == sv.SVF_OK
     assert lib.svf_debug_set_attn_wait_ns(0) == sv.SVF_OK
+
+
+def test_fused_mask_attention_argument_checks(lib):
+    import speculative_decoding_tree_03_gb300 as sv
+    P = ctypes.c_void_p(256)
+    # parent missing
+    args = [None, P, P, P, P, P, P, 10, 16, P, 4, P, 2, 7, 8, 2, 128, 1, 0.0, P, P, None, 0, P,
+            None]
+    assert lib.svf_tree_mask_attn(*args) == sv.SVF_ERR_ARG
+    # N above the attention limit
+    args = [P, P, P, P, P, P, P, 10, 16, P, 4, P, 2, 65, 8, 2, 128, 1, 0.0, P, P, None, 0, P,
+            None]
+    assert lib.svf_tree_mask_attn(*args) == sv.SVF_ERR_UNSUPPORTED
+    # fp32 needs the mask outputs (that path reads the masks from memory)
+    args = [P, None, None, None, P, P, P, 10, 16, P, 4, P, 2, 7, 8, 2, 128, 0, 0.0, P, P, None,
+            0, P, None]
+    assert lib.svf_tree_mask_attn(*args) == sv.SVF_ERR_ARG

@@ -548,3 +548,44 @@ def test_attention_bad_inputs_every_cluster_size(sv, force_splits, splits):
     o_ref, _ = oracle.tree_attn(c["q"][good], c["K"][good], c["V"][good], c["lens"][good],
                                 c["parent"][good])
     assert np.abs(out[good] - o_ref.reshape(out[good].shape)).max() <= BF16_OUT_TOL
+
+
+# ---------------------------------------------------------------------------
+# the fused call: masks built inside the attention kernel
+# ---------------------------------------------------------------------------
+
+FUSED_CASES = [c for c in CASES if c[0] in ("worked_tree_contig", "binary31_paged16_g8",
+                                            "random60_paged32_rowblocks", "single_node_no_prefix",
+                                            "tree_crosses_tile", "fp32_d64", "bf16_mixed_lengths")]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=[c[0] for c in FUSED_CASES])
+def test_fused_mask_attention_matches_the_two_calls(sv, case):
+    """svf_tree_mask_attn gives the masks of svf_tree_mask_build (checked
+    against the oracle) and, bit for bit, the attention of
+    svf_tree_verify_attn on those masks; one tree in the batch is invalid."""
+    name, seed, B, pk, lens, Hq, Hkv, D, dtype, ps = case
+    parent = _parent_of(pk, B, np.random.default_rng(seed + 100))
+    N = parent.shape[1]
+    if B > 1 and N > 1:
+        parent[B - 1, N - 1] = N - 1          # not BFS: parent must precede the node
+    c = _attn_case(seed, B, N, parent, lens, Hq, Hkv, D, dtype, ps)
+    dev = "cuda"
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    q = torch.from_numpy(c["q"]).to(dev).to(tdt)
+    kc = torch.from_numpy(c["kc"]).to(dev).to(tdt)
+    vc = torch.from_numpy(c["vc"]).to(dev).to(tdt)
+    table = torch.from_numpy(c["table"]).to(dev)
+    sl = torch.from_numpy(c["lens"]).to(dev)
+    par = torch.from_numpy(parent).to(dev)
+    out_f, lse_f, st_f, anc_f, dep_f, mst_f = sv.tree_mask_attn(par, q, kc, vc, table, sl)
+    anc, dep, mst = sv.tree_mask_build(par)
+    out_s, lse_s, st_s = sv.tree_verify_attn(q, kc, vc, table, sl, anc)
+    torch.cuda.synchronize()
+    oa, od, os_ = oracle.tree_mask(parent)
+    assert (_np(anc_f).view(np.uint64) == oa).all()
+    assert (_np(dep_f) == od).all() and (_np(mst_f) == os_).all()
+    assert torch.equal(st_f, st_s)
+    assert torch.equal(out_f.view(torch.int16) if dtype == "bf16" else out_f,
+                       out_s.view(torch.int16) if dtype == "bf16" else out_s)
+    assert torch.equal(lse_f, lse_s)
