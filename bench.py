@@ -82,14 +82,15 @@ def source_hash(rel):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def committed_traffic(workload, kernel_src):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source
-    has not changed since it was taken (else None)."""
+def committed_traffic(workload, kernel_src, chunks=0):
+    """DRAM bytes per launch from a committed ncu summary of the same workload
+    and chunk setting (0: the library's choice), if the kernel source has not
+    changed since it was taken (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d[workload]
+        e = d[f"{workload}@{chunks}" if chunks else workload]
         if e.get("source_hash") == source_hash(kernel_src):
             return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -573,6 +574,8 @@ def run_ours(args, w, idx):
     from speculative_decoding_tree_03_gb300 import build as _build
     _build.build()
     import speculative_decoding_tree_03_gb300 as sv
+    if args.attn_chunks:
+        assert sv.load_library().svf_debug_set_attn_splits(args.attn_chunks) == 0
 
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
@@ -876,6 +879,7 @@ def run_ours(args, w, idx):
                   f"> L2 {r.l2 / 1e6:.0f} MB)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "launch": "one CUDA graph per step: masks + attention (one fused call), acceptance",
+            "attn_chunks": args.attn_chunks or "library's choice",
             "e2e_copies": "one packed pinned host-to-device copy per step, issued one step "
                           "ahead on a side stream; outputs read back every step",
         },
@@ -920,7 +924,8 @@ def run_ours(args, w, idx):
             "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
             "unit": "GB/s",
             "frac": attn_gbs / peak,
-            "traffic": committed_traffic(w.name, "speculative_decoding_tree_03_gb300/csrc/attn_tc.cu"),
+            "traffic": committed_traffic(w.name, "speculative_decoding_tree_03_gb300/csrc/attn_tc.cu",
+                                         args.attn_chunks),
             "duration_from": "CUDA events around the attention call inside the step graph",
         },
         "per_workload": per_workload,
@@ -947,6 +952,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--attn-chunks", type=int, default=0,
+                    help="KV chunks per (sequence, KV head) of the bf16 attention, 1..8 "
+                         "(0: the library's choice); 1 launches no thread-block cluster")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
