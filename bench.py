@@ -333,7 +333,8 @@ class StepRunner:
         self.astat = torch.empty((B,), dtype=torch.int32, device=dev)
         self.attn_ws_need = sv.tree_verify_attn_workspace_size(
             B, N, Hq, w.Hkv, D, self.base["q"].dtype, inp.page_table.shape[1], inp.page_size)
-        self.attn_ws = torch.empty((max(self.attn_ws_need, 1),), dtype=torch.uint8, device=dev)
+        # zero-filled once; every call leaves it so
+        self.attn_ws = torch.zeros((max(self.attn_ws_need, 1),), dtype=torch.uint8, device=dev)
         self.acc_ws_need = sv.spec_accept_workspace_size(B, N, w.V)
         self.acc_ws = torch.empty((self.acc_ws_need,), dtype=torch.uint8, device=dev)
         self.acc_out = {}
@@ -576,6 +577,8 @@ def run_ours(args, w, idx):
     import speculative_decoding_tree_03_gb300 as sv
     if args.attn_chunks:
         assert sv.load_library().svf_debug_set_attn_splits(args.attn_chunks) == 0
+    if args.attn_kernel:
+        assert sv.load_library().svf_debug_set_attn_kernel(args.attn_kernel) == 0
 
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
@@ -880,6 +883,8 @@ def run_ours(args, w, idx):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "launch": "one CUDA graph per step: masks + attention (one fused call), acceptance",
             "attn_chunks": args.attn_chunks or "library's choice",
+            "attn_kernel": {0: "library's choice", 1: "chunks merged in clusters",
+                            2: "persistent, one CTA per SM"}[args.attn_kernel],
             "e2e_copies": "one packed pinned host-to-device copy per step, issued one step "
                           "ahead on a side stream; outputs read back every step",
         },
@@ -952,6 +957,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--attn-kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="bf16 attention kernel: 0 the library's choice, 1 KV chunks merged in "
+                         "thread-block clusters, 2 persistent (one CTA per SM)")
     ap.add_argument("--attn-chunks", type=int, default=0,
                     help="KV chunks per (sequence, KV head) of the bf16 attention, 1..8 "
                          "(0: the library's choice); 1 launches no thread-block cluster")

@@ -120,11 +120,17 @@ int svf_tree_mask_build(const int32_t *parent, int B, int N, uint64_t *anc, int3
  *   sm_scale   <= 0 selects 1/sqrt(D)
  *   out        [B, N, Hq, D] dtype                out
  *   lse        [B, N, Hq] float32                 out, may be NULL (natural log)
- *   workspace  device scratch of at least
- *              svf_tree_verify_attn_workspace_size(...) bytes (NULL if that is 0;
- *              it is 0 for every size: the KV chunks of one (sequence, KV
- *              head) merge on chip; the argument is kept for callers that
- *              size it)
+ *   workspace  device scratch of svf_tree_verify_attn_workspace_size(...)
+ *              bytes, ZERO-FILLED once before its first use. For SVF_BF16
+ *              with Hq / Hkv a power of two it holds the pieces of the units
+ *              that the persistent kernel splits between SMs (two slots per
+ *              SM) and a pair of counters per unit, which every call leaves
+ *              at zero again; a workspace that is large enough for one shape
+ *              is reused as is by any call whose size fits in it. Calls that
+ *              may overlap on the GPU need workspaces of their own. NULL (or
+ *              fewer bytes) selects the kernel that merges a unit's KV chunks
+ *              on chip, inside a thread-block cluster, which needs none;
+ *              SVF_F32 needs none.
  *   status     [B] int32                          out; SVF_DEV_BAD_LENGTH,
  *                                                  SVF_DEV_BAD_PAGE. A bad
  *                                                  sequence's out and lse are 0.
@@ -530,6 +536,19 @@ int svf_debug_set_attn_wait_ns(long long ns);
  * or SVF_ERR_ARG outside 0..8.
  * ---------------------------------------------------------------------- */
 int svf_debug_set_attn_splits(int splits);
+
+/* ------------------------------------------------------------------------
+ * svf_debug_set_attn_kernel -- test hook: which bf16 attention kernel later
+ * calls in this process run. 0: the library's choice; 1: one CTA per (unit,
+ * KV chunk), the chunks of a unit merged inside a thread-block cluster (no
+ * workspace); 2: one persistent CTA per SM over an equal share of all units'
+ * tiles, split units merged through the workspace (SVF_ERR_WORKSPACE without
+ * one). A chunk count set with svf_debug_set_attn_splits selects kernel 1.
+ * The result is the same within the stated tolerance. The pages have no
+ * counterpart; it lets tests run both kernels on the same inputs. Returns
+ * SVF_OK, or SVF_ERR_ARG outside 0..2.
+ * ---------------------------------------------------------------------- */
+int svf_debug_set_attn_kernel(int which);
 
 /* Human-readable name of a host return code or of one device status bit. */
 const char *svf_status_string(int code);

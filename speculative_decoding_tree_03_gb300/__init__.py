@@ -41,6 +41,7 @@ EXPORTED = [
     "svf_lm_head",
     "svf_debug_set_attn_wait_ns",
     "svf_debug_set_attn_splits",
+    "svf_debug_set_attn_kernel",
     "svf_spec_accept_lmhead",
     "svf_kv_commit",
     "svf_selftest_wait_timeout",
@@ -119,6 +120,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.svf_debug_set_attn_wait_ns.restype = I
     lib.svf_debug_set_attn_splits.argtypes = [I]
     lib.svf_debug_set_attn_splits.restype = I
+    lib.svf_debug_set_attn_kernel.argtypes = [I]
+    lib.svf_debug_set_attn_kernel.restype = I
     lib.svf_status_string.argtypes = [I]
     lib.svf_status_string.restype = ctypes.c_char_p
     lib.svf_version.argtypes = []
@@ -150,6 +153,21 @@ def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> torch.Tensor:
     if not t.is_contiguous():
         raise SpecVerifyError(f"{name} must be contiguous")
     return t
+
+
+_ZEROED_WS = {}
+
+
+def _zeroed_workspace(need: int, dev: torch.device) -> torch.Tensor:
+    """The attention workspace used when the caller passes none: zero-filled
+    once and kept per device (every call leaves it zero-filled). Calls that
+    may overlap on the GPU should pass workspaces of their own."""
+    key = (dev.type, dev.index if dev.index is not None else torch.cuda.current_device())
+    ws = _ZEROED_WS.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros((need,), dtype=torch.uint8, device=dev)
+        _ZEROED_WS[key] = ws
+    return ws
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -249,7 +267,7 @@ def tree_verify_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     need = int(lib.svf_tree_verify_attn_workspace_size(B, N, Hq, Hkv, D, code, max_pages,
                                                        page_size))
     if workspace is None and need > 0:
-        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+        workspace = _zeroed_workspace(need, dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.svf_tree_verify_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages, page_size, _ptr(page_table), max_pages,
@@ -307,7 +325,7 @@ def tree_mask_attn(parent: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
     need = int(lib.svf_tree_verify_attn_workspace_size(B, N, Hq, Hkv, D, code, max_pages,
                                                        page_size))
     if workspace is None and need > 0:
-        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+        workspace = _zeroed_workspace(need, dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.svf_tree_mask_attn(
         _ptr(parent), _ptr(anc), _ptr(depth), _ptr(mask_status), _ptr(q), _ptr(k_cache),

@@ -73,7 +73,9 @@ size_t svf_tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int D,
         page_size <= 0)
         return 0;
     if (dtype != SVF_BF16 || D != 128) return 0;
-    return attn_tc_workspace_bytes(B, N, Hq, Hkv, max_pages, page_size);
+    const size_t tc_bytes = attn_tc_workspace_bytes(B, N, Hq, Hkv, max_pages, page_size);
+    const size_t sk_bytes = attn_sk_workspace_bytes(B, N, Hq, Hkv);
+    return tc_bytes > sk_bytes ? tc_bytes : sk_bytes;
 }
 
 static int tree_attn_common(const void *q, const void *k_cache, const void *v_cache,
@@ -122,7 +124,10 @@ static int tree_attn_common(const void *q, const void *k_cache, const void *v_ca
     a.anc_out = anc_out;
     a.depth_out = depth_out;
     a.mask_status = mask_status;
-    // the kernel stores every sequence's status word itself
+    // the kernels store every sequence's status word themselves
+    const int which = attn_choose_kernel(a, workspace, workspace_bytes);
+    if (which < 0) return SVF_ERR_WORKSPACE;
+    if (which == 2) return launch_attn_sk(a, workspace, workspace_bytes, s);
     return launch_attn_tc(a, workspace, workspace_bytes, s);
 }
 
@@ -185,6 +190,12 @@ int svf_debug_set_attn_wait_ns(long long ns) {
 int svf_debug_set_attn_splits(int splits) {
     if (splits < 0 || splits > 8) return SVF_ERR_ARG;
     attn_tc_force_splits(splits);
+    return SVF_OK;
+}
+
+int svf_debug_set_attn_kernel(int which) {
+    if (which < 0 || which > 2) return SVF_ERR_ARG;
+    attn_set_kernel(which);
     return SVF_OK;
 }
 

@@ -115,8 +115,21 @@ int launch_attn_tc(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStre
 // 0 or less restores the default of 2 s).
 void attn_tc_set_wait_ns(long long ns);
 // Test hook: the chunk count (cluster size) of later calls, 1..8; 0 restores
-// the host model's choice.
+// the host model's choice. A forced count selects the cluster kernel.
 void attn_tc_force_splits(int s);
+int attn_tc_forced_splits();
+long long attn_tc_wait_ns();
+
+// Persistent tensor-core path for bf16 (attn_sk.cu): one CTA per SM over an
+// equal share of all units' tiles; split units merge through the workspace,
+// which must be zero-filled before its first use (every call leaves it so).
+bool attn_sk_supported(int Hq, int Hkv);
+size_t attn_sk_workspace_bytes(int B, int N, int Hq, int Hkv);
+int launch_attn_sk(const AttnArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream);
+// Which bf16 kernel runs: 0 the library's choice, 1 the cluster kernel, 2 the
+// persistent kernel (test hook).
+void attn_set_kernel(int which);
+int attn_choose_kernel(const AttnArgs &a, const void *workspace, size_t ws_bytes);
 
 // Acceptance walk (accept.cu): rows of the visited nodes held in the registers
 // of one CTA cluster up to kMaxOnChipVocab, streamed from memory beyond that

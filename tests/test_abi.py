@@ -180,10 +180,29 @@ def test_selftest_argument_checks(lib):
 
 
 def test_workspace_sizes_without_gpu(lib):
-    # bf16 attention merges its KV chunks on chip: no workspace at any size
-    assert lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 1, 1, 2176) == 0
-    assert lib.svf_tree_verify_attn_workspace_size(64, 31, 64, 8, 128, 1, 2051, 16) == 0
+    # bf16 with Hq / Hkv a power of two: the persistent kernel's pieces (two
+    # slots per SM of 256 fp32 rows of 128, their log-sum-exps and flags)
+    # and then two counters per unit, each part rounded up to 256 bytes
+    up = lambda x: (x + 255) // 256 * 256
+    sms = 148  # the library's stand-in without a device
+    def expect(B, N, Hq, Hkv):
+        M = N * (Hq // Hkv)
+        rows = 256 if M > 128 else 128
+        units = B * Hkv * -(-M // rows)
+        return (up(2 * sms * 32 * 256 * 16) + up(2 * sms * 256 * 4) + up(2 * sms * 4)
+                + up(units * 8))
+    assert lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 1, 1, 2176) == expect(1, 31, 32, 8)
+    assert lib.svf_tree_verify_attn_workspace_size(64, 31, 64, 8, 128, 1, 2051, 16) == \
+        expect(64, 31, 64, 8)
+    assert lib.svf_tree_verify_attn_workspace_size(16, 64, 64, 8, 128, 1, 256, 16) == \
+        expect(16, 64, 64, 8)
+    # fp32 and a non-power-of-two group size need none
     assert lib.svf_tree_verify_attn_workspace_size(1, 31, 32, 8, 128, 0, 1, 2176) == 0
+    assert lib.svf_tree_verify_attn_workspace_size(1, 31, 24, 8, 128, 1, 1, 2176) == 0
+    # the hook that picks the bf16 kernel checks its argument
+    assert lib.svf_debug_set_attn_kernel(3) == -1
+    assert lib.svf_debug_set_attn_kernel(-1) == -1
+    assert lib.svf_debug_set_attn_kernel(0) == 0
 
 
 def test_package_refuses_cpu_tensors():

@@ -38,13 +38,15 @@ def test_wait_runs_out_and_reports(sv, deadline_s):
 
 
 def test_attention_wait_runs_out_and_the_next_call_is_exact(sv):
-    """The tensor-core attention kernel with a 1 ns wait deadline: its first
+    """The tensor-core attention kernels with a 1 ns wait deadline: the first
     wait that is not already complete gives up, the CTA drains its copies and
     tensor-core operations in flight, releases its tensor memory, and every
-    sequence reports SVF_DEV_TIMEOUT -- with one chunk per unit and with
-    chunks merged in a cluster. With the default deadline restored, the next
-    call on the same inputs matches the oracle (so tensor memory was freed:
-    a leaked allocation would stall every later CTA's allocation)."""
+    sequence reports SVF_DEV_TIMEOUT -- with one chunk per unit, with chunks
+    merged in a cluster, and in the persistent kernel (whose pieces are still
+    published and merged, flagged). With the default deadline restored, the
+    next call on the same inputs matches the oracle (so tensor memory was
+    freed: a leaked allocation would stall every later CTA's allocation; and
+    the persistent kernel's per-unit counters were left at zero)."""
     from test_gpu_parity import _attn_case, _run_attn, BF16_OUT_TOL, BF16_LSE_TOL
     from synth import binary_tree_parent
     lib = sv.load_library()
@@ -52,8 +54,9 @@ def test_attention_wait_runs_out_and_the_next_call_is_exact(sv):
     parent = np.broadcast_to(binary_tree_parent(4), (B, 31)).copy()
     c = _attn_case(41, B, 31, parent, [2500, 800, 1700], 32, 8, 128, "bf16", 16)
     try:
-        for splits in (1, 3):
+        for splits, kernel in ((1, 1), (3, 1), (0, 2)):
             assert lib.svf_debug_set_attn_splits(splits) == 0
+            assert lib.svf_debug_set_attn_kernel(kernel) == 0
             assert lib.svf_debug_set_attn_wait_ns(1) == 0
             _, _, status = _run_attn(sv, c, "bf16")
             assert ((status & 16) != 0).all(), status
@@ -67,3 +70,4 @@ def test_attention_wait_runs_out_and_the_next_call_is_exact(sv):
     finally:
         lib.svf_debug_set_attn_wait_ns(0)
         lib.svf_debug_set_attn_splits(0)
+        lib.svf_debug_set_attn_kernel(0)

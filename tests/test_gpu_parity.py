@@ -39,6 +39,20 @@ def _np(t):
     return t.detach().cpu().numpy()
 
 
+# the two bf16 attention kernels: 1 = chunks of a unit merged inside a
+# thread-block cluster, 2 = one persistent CTA per SM over an equal share of
+# all units' tiles, split units merged through the workspace
+KERNELS = [1, 2]
+
+
+@pytest.fixture(params=KERNELS, ids=["cluster", "persistent"])
+def attn_kernel(sv, request):
+    lib = sv.load_library()
+    assert lib.svf_debug_set_attn_kernel(request.param) == 0
+    yield request.param
+    lib.svf_debug_set_attn_kernel(0)
+
+
 # ---------------------------------------------------------------------------
 # tree_mask_build
 # ---------------------------------------------------------------------------
@@ -174,7 +188,7 @@ def _parent_of(kind, B, rng):
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_attention_small_cases(sv, case):
+def test_attention_small_cases(sv, attn_kernel, case):
     name, seed, B, pk, lens, Hq, Hkv, D, dtype, ps = case
     parent = _parent_of(pk, B, np.random.default_rng(seed + 100))
     N = parent.shape[1]
@@ -188,12 +202,12 @@ def test_attention_small_cases(sv, case):
     tol_l = BF16_LSE_TOL if dtype == "bf16" else F32_TOL
     err_o = np.abs(out - o_ref).max()
     err_l = np.abs(lse - l_ref).max()
-    print(f"{name}: max|out-ref| {err_o:.3g} max|lse-ref| {err_l:.3g}")
+    print(f"{name} kernel {attn_kernel}: max|out-ref| {err_o:.3g} max|lse-ref| {err_l:.3g}")
     assert err_l <= tol_l, err_l
     assert err_o <= tol_o, err_o
 
 
-def test_attention_ignores_garbage_past_sequence_end(sv):
+def test_attention_ignores_garbage_past_sequence_end(sv, attn_kernel):
     parent = binary_tree_parent(3)
     B = 2
     parent = np.broadcast_to(parent, (B, parent.size)).copy()
@@ -204,7 +218,7 @@ def test_attention_ignores_garbage_past_sequence_end(sv):
     assert np.abs(out - o_ref.reshape(out.shape)).max() <= BF16_OUT_TOL
 
 
-def test_attention_bad_page_and_length_status(sv):
+def test_attention_bad_page_and_length_status(sv, attn_kernel):
     parent = binary_tree_parent(2)
     B = 3
     parent = np.broadcast_to(parent, (B, parent.size)).copy()
@@ -221,7 +235,7 @@ def test_attention_bad_page_and_length_status(sv):
         assert np.abs(out[0] - o_ref.reshape(out[0].shape)).max() <= tol
 
 
-def test_attention_mixed_lengths_with_bad_sequences(sv):
+def test_attention_mixed_lengths_with_bad_sequences(sv, attn_kernel):
     """80 units of mixed lengths with a bad page and a bad length in the batch:
     those sequences get their status bit and zeros, the rest match."""
     parent = chain_parent(16)
@@ -243,7 +257,7 @@ def test_attention_mixed_lengths_with_bad_sequences(sv):
 
 
 @pytest.mark.parametrize("idx", [0, 1, 2, 3])
-def test_attention_workloads_full(sv, idx):
+def test_attention_workloads_full(sv, attn_kernel, idx):
     w = WORKLOADS[idx]
     inp = make_inputs(w, 1000 + idx, with_kv=True, with_logits=False)
     d = device_inputs(inp)
@@ -551,6 +565,119 @@ def test_attention_bad_inputs_every_cluster_size(sv, force_splits, splits):
 
 
 # ---------------------------------------------------------------------------
+# the persistent kernel: units split into pieces between CTAs
+# ---------------------------------------------------------------------------
+
+@pytest.fixture
+def persistent(sv):
+    lib = sv.load_library()
+    assert lib.svf_debug_set_attn_kernel(2) == 0
+    yield lib
+    lib.svf_debug_set_attn_kernel(0)
+
+
+def _check_attn(c, out, lse, status, skip=()):
+    good = [b for b in range(c["q"].shape[0]) if b not in skip]
+    assert (status[good] == 0).all(), status
+    o_ref, l_ref = oracle.tree_attn(c["q"][good], c["K"][good], c["V"][good], c["lens"][good],
+                                    c["parent"][good])
+    err_o = np.abs(out[good] - o_ref.reshape(out[good].shape)).max()
+    err_l = np.abs(lse[good] - l_ref.reshape(lse[good].shape)).max()
+    assert err_o <= BF16_OUT_TOL and err_l <= BF16_LSE_TOL, (err_o, err_l)
+    return err_o, err_l
+
+
+PERSISTENT_CASES = [
+    # one unit of 160 tiles: 20 CTAs of 8 tiles, every piece merged (F = 20)
+    ("one_unit_twenty_pieces", 51, 1, "binary3", [10200], 4, 1, 128, 16),
+    # four units of ~80 tiles over 40 CTAs: ~10 pieces per unit, both halves
+    ("two_halves_ten_pieces", 52, 2, "binary4", [5000, 5100], 32, 2, 128, 16),
+    # 300 short sequences (more than one CTA per SM): many whole units and
+    # many segments per CTA, each with its own Q, tail tile and epilogue
+    ("three_hundred_short", 53, 300, "chain16", None, 8, 2, 128, 16),
+    # two row blocks of two halves (M = 480) and a contiguous cache
+    ("row_blocks_contig", 54, 3, "random60", [3000, 90, 1500], 8, 1, 128, 0),
+    # one tile per sequence: the tile space is shorter than the SM count
+    ("tiny_units", 55, 5, "single", [0, 3, 10, 1, 40], 4, 4, 128, 16),
+]
+
+
+@pytest.mark.parametrize("case", PERSISTENT_CASES, ids=[c[0] for c in PERSISTENT_CASES])
+def test_persistent_pieces_and_segments(sv, persistent, case):
+    name, seed, B, pk, lens, Hq, Hkv, D, ps = case
+    rng = np.random.default_rng(seed)
+    if lens is None:
+        lens = rng.integers(0, 400, B).tolist()
+    parent = _parent_of(pk, B, np.random.default_rng(seed + 100))
+    c = _attn_case(seed, B, parent.shape[1], parent, lens, Hq, Hkv, D, "bf16", ps)
+    out, lse, status = _run_attn(sv, c, "bf16", poison_tail=True)
+    err_o, err_l = _check_attn(c, out, lse, status)
+    print(f"{name}: max|out-ref| {err_o:.3g} max|lse-ref| {err_l:.3g}")
+
+
+def test_persistent_bad_sequences_among_pieces(sv, persistent):
+    """A bad page in the middle of a sequence whose units are split between
+    CTAs zeroes every piece's merge of that sequence (the piece that saw the
+    page flags it); a bad length has no tile at all. The rest stay exact."""
+    B = 6
+    parent = np.broadcast_to(binary_tree_parent(4), (B, 31)).copy()
+    lens = [4000, 3000, 2500, 100, 3900, 700]
+    c = _attn_case(61, B, 31, parent, lens, 64, 8, 128, "bf16", 16)
+    c["table"][1, 100] = c["P"] + 3          # a page id outside the cache
+    lens2 = c["lens"].copy()
+    lens2[3] = 10 ** 6                        # longer than the page table
+    c2 = dict(c, lens=lens2)
+    out, lse, status = _run_attn(sv, c2, "bf16")
+    assert status.tolist() == [0, 4, 0, 8, 0, 0], status
+    for b in (1, 3):
+        assert (out[b] == 0).all() and (lse[b] == 0).all()
+    _check_attn(c, out, lse, status, skip=(1, 3))
+
+
+def test_persistent_counters_reset_between_shapes(sv, persistent):
+    """Calls of different shapes share one workspace: the per-unit counters
+    each call leaves at zero must give the next call (another split of the
+    tile space, other piece counts) exact results, and the first shape again
+    after it."""
+    ws_need = sv.tree_verify_attn_workspace_size(8, 31, 64, 8, 128, torch.bfloat16, 400, 16)
+    ws = torch.zeros((ws_need,), dtype=torch.uint8, device="cuda")
+    cases = []
+    for seed, B, lens in ((71, 2, [6000, 2500]), (72, 8, [900, 50, 3000, 10, 2000, 700, 6300, 1]),
+                          (71, 2, [6000, 2500])):
+        parent = np.broadcast_to(binary_tree_parent(4), (B, 31)).copy()
+        cases.append(_attn_case(seed, B, 31, parent, lens, 64, 8, 128, "bf16", 16))
+    for c in cases:
+        dev = "cuda"
+        q = torch.from_numpy(c["q"]).to(dev).to(torch.bfloat16)
+        kc = torch.from_numpy(c["kc"]).to(dev).to(torch.bfloat16)
+        vc = torch.from_numpy(c["vc"]).to(dev).to(torch.bfloat16)
+        anc, _, _ = sv.tree_mask_build(torch.from_numpy(c["parent"]).to(dev))
+        for _ in range(2):
+            out, lse, status = sv.tree_verify_attn(q, kc, vc, torch.from_numpy(c["table"]).to(dev),
+                                                   torch.from_numpy(c["lens"]).to(dev), anc,
+                                                   workspace=ws)
+            torch.cuda.synchronize()
+            _check_attn(c, _np(out.float()), _np(lse), _np(status))
+    # every counter is back at zero: they are the workspace's last bytes
+    units = 8 * 8
+    assert (ws[ws_need - units * 8:].view(torch.int32) == 0).all()
+
+
+def test_persistent_needs_a_workspace(sv, persistent):
+    parent = np.broadcast_to(binary_tree_parent(2), (1, 7)).copy()
+    c = _attn_case(81, 1, 7, parent, [100], 8, 2, 128, "bf16", 16)
+    dev = "cuda"
+    q = torch.from_numpy(c["q"]).to(dev).to(torch.bfloat16)
+    kc = torch.from_numpy(c["kc"]).to(dev).to(torch.bfloat16)
+    vc = torch.from_numpy(c["vc"]).to(dev).to(torch.bfloat16)
+    anc, _, _ = sv.tree_mask_build(torch.from_numpy(c["parent"]).to(dev))
+    with pytest.raises(sv.SpecVerifyError):
+        sv.tree_verify_attn(q, kc, vc, torch.from_numpy(c["table"]).to(dev),
+                            torch.from_numpy(c["lens"]).to(dev), anc,
+                            workspace=torch.zeros((256,), dtype=torch.uint8, device=dev))
+
+
+# ---------------------------------------------------------------------------
 # the fused call: masks built inside the attention kernel
 # ---------------------------------------------------------------------------
 
@@ -560,7 +687,7 @@ FUSED_CASES = [c for c in CASES if c[0] in ("worked_tree_contig", "binary31_page
 
 
 @pytest.mark.parametrize("case", FUSED_CASES, ids=[c[0] for c in FUSED_CASES])
-def test_fused_mask_attention_matches_the_two_calls(sv, case):
+def test_fused_mask_attention_matches_the_two_calls(sv, attn_kernel, case):
     """svf_tree_mask_attn gives the masks of svf_tree_mask_build (checked
     against the oracle) and, bit for bit, the attention of
     svf_tree_verify_attn on those masks; one tree in the batch is invalid."""
