@@ -411,10 +411,7 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
             // ask L2 for this CTA's slice of the first child's rows
             const int s0 = rank * NG * 128;
             if (s0 < V) {
-                // (a bulk prefetch wants a multiple of 16 bytes; the tail of
-                // a bf16 row may be left out, it is only a hint)
-                const uint32_t bytes =
-                    ((uint32_t)min(NG * 128, V - s0) * (uint32_t)sizeof(T)) & ~15u;
+                const uint32_t bytes = (uint32_t)min(NG * 128, V - s0) * (uint32_t)sizeof(T);
                 prefetch_l2_bulk(target + (base + c1) * V + s0, bytes);
                 if (sfirst[c1] >= 0) prefetch_l2_bulk(draft + (base + c1) * V + s0, bytes);
             }

@@ -275,8 +275,16 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int c0, int
 }
 
 // Pull `bytes` (a multiple of 16) starting at a 16-byte aligned address into L2.
+// Ask L2 for [p, p + bytes). The bulk prefetch wants a 16-byte aligned start
+// and a multiple of 16 bytes, so the range shrinks to its aligned interior
+// (it is only a hint).
 __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uintptr_t a16 = (a + 15) & ~static_cast<uintptr_t>(15);
+    if ((uintptr_t)bytes <= a16 - a) return;
+    const uint32_t n = (bytes - (uint32_t)(a16 - a)) & ~15u;
+    if (n == 0) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a16), "r"(n) : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {

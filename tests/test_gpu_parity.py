@@ -404,10 +404,12 @@ def _accept_gpu_bf16(sv, arrs):
     return {k: (_np(v) if v is not None else None) for k, v in res.items()}, wide
 
 
-@pytest.mark.parametrize("V", [8, 37, 1000, 5003, 32000, 128256])
+@pytest.mark.parametrize("V", [8, 37, 1000, 1004, 5003, 32000, 128256])
 def test_accept_bf16_logits(sv, V):
     """bf16 logits (vector and scalar loads, warp, block and cluster paths)
-    against the oracle on the widened values."""
+    against the oracle on the widened values. V = 1004: rows start on 8-byte
+    but not 16-byte boundaries, so the walk's L2 prefetches are shrunk to the
+    aligned interior of each slice."""
     arrs = _synthetic_accept(V + 3, 48, 7, V, [-1, 0, 0, 1, 1, 2, 2], sigma=2.0, noise=0.7)
     gpu, wide = _accept_gpu_bf16(sv, arrs)
     compare_accept(gpu, wide, oracle.spec_accept(**wide))
