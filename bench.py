@@ -25,6 +25,7 @@ the workload (weak scaling) and the step time is the maximum over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -82,16 +83,16 @@ def source_hash(rel):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def committed_traffic(workload, kernel_src, chunks=0):
+def committed_traffic(workload, chunks=0):
     """DRAM bytes per launch from a committed ncu summary of the same workload
-    and chunk setting (0: the library's choice), if the kernel source has not
-    changed since it was taken (else None)."""
+    and chunk setting (0: the library's choice), if the source of the kernel
+    it captured has not changed since (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[f"{workload}@{chunks}" if chunks else workload]
-        if e.get("source_hash") == source_hash(kernel_src):
+        if e.get("source_hash") == source_hash(e["source"]):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -929,8 +930,8 @@ def run_ours(args, w, idx):
             "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
             "unit": "GB/s",
             "frac": attn_gbs / peak,
-            "traffic": committed_traffic(w.name, "speculative_decoding_tree_03_gb300/csrc/attn_tc.cu",
-                                         args.attn_chunks),
+            "traffic": (committed_traffic(w.name, args.attn_chunks)
+                        if not args.batch and not args.attn_kernel else None),
             "duration_from": "CUDA events around the attention call inside the step graph",
         },
         "per_workload": per_workload,
@@ -960,6 +961,9 @@ def main():
     ap.add_argument("--attn-kernel", type=int, default=0, choices=[0, 1, 2],
                     help="bf16 attention kernel: 0 the library's choice, 1 KV chunks merged in "
                          "thread-block clusters, 2 persistent (one CTA per SM)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload with this many sequences instead of its own batch "
+                         "(a smaller case of the same shapes, for profiler captures)")
     ap.add_argument("--attn-chunks", type=int, default=0,
                     help="KV chunks per (sequence, KV head) of the bf16 attention, 1..8 "
                          "(0: the library's choice); 1 launches no thread-block cluster")
@@ -967,6 +971,8 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     idx, w = workload_by_name(args.workload)
+    if args.batch > 0:
+        w = dataclasses.replace(w, B=args.batch)
     if args.impl == "reference":
         run_reference(args, w, idx)
     else:
