@@ -38,12 +38,16 @@ def test_committed_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     src.write_text("kernel v1")
     (tmp_path / "profiles").mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    entry = {"dram_bytes_per_launch": 1234, "source_hash": bench.source_hash("k.cu")}
-    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"w": entry}))
-    assert bench.committed_traffic("w", "k.cu") == 1234.0
-    assert bench.committed_traffic("other", "k.cu") is None
+    entry = {"dram_bytes_per_launch": 1234, "source": "k.cu",
+             "source_hash": bench.source_hash("k.cu")}
+    one_chunk = dict(entry, dram_bytes_per_launch=99)
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"w": entry, "w@1": one_chunk}))
+    assert bench.committed_traffic("w") == 1234.0
+    assert bench.committed_traffic("w", 1) == 99.0     # captured with one chunk
+    assert bench.committed_traffic("w", 2) is None     # no capture with two
+    assert bench.committed_traffic("other") is None
     src.write_text("kernel v2")                 # the kernel changed since the capture
-    assert bench.committed_traffic("w", "k.cu") is None
+    assert bench.committed_traffic("w") is None
 
 
 def test_measured_peaks_fallback(tmp_path, monkeypatch):
