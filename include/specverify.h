@@ -289,8 +289,11 @@ int svf_spec_accept_bf16(const void *target_logits, const void *draft_logits,
  *   svf_spec_accept); outputs accept_len [B], path [B, N], out_tokens [B, N]
  *   and status [B] as for svf_spec_accept (same status bits and "no result"
  *   values).
- * Limits: 1 <= N <= 1024, 1 <= V <= 262144; target_logits 16-byte aligned
- * when V % 4 == 0.
+ * Limits: 1 <= N <= 1024, 1 <= V <= 786432 (up to 262144 a cluster holds
+ * the visited node's row in registers; above that each CTA streams its
+ * slice of the row from memory on every pass: one per visited node, and
+ * for the one-hot bonus one more plus the crossing group's); target_logits
+ * 16-byte aligned when V % 4 == 0. No workspace.
  * ---------------------------------------------------------------------- */
 int svf_spec_accept_greedy(const float *target_logits, const int32_t *tokens,
                            const int32_t *parent, int B, int N, int V, int32_t *accept_len,
@@ -315,8 +318,11 @@ int svf_spec_accept_greedy(const float *target_logits, const int32_t *tokens,
  *   Arguments and outputs as for svf_spec_accept without draft_logits and
  *   workspace; ratio [B, N] (may be NULL) gets p~(x) = p~(x)/q(x) for every
  *   tested child, NaN otherwise.
- * Limits: 1 <= N <= 1024, 1 <= V <= 262144; target_logits 16-byte aligned
- * when V % 4 == 0.
+ * Limits: 1 <= N <= 1024, 1 <= V <= 786432 (up to 262144 a cluster holds
+ * the visited node's row in registers; above that each CTA streams its
+ * slice of the row from memory on every pass: one per visited node, and
+ * for the one-hot bonus one more plus the crossing group's); target_logits
+ * 16-byte aligned when V % 4 == 0. No workspace.
  * ---------------------------------------------------------------------- */
 int svf_spec_accept_onehot(const float *target_logits, const int32_t *tokens,
                            const int32_t *parent, const float *u_accept, const float *u_bonus,

@@ -20,6 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libspecverify.so")
 SOURCES = ["mask.cu", "attn_simt.cu", "attn_tc.cu", "attn_sk.cu", "accept.cu", "accept_stream.cu",
+           "accept_target_stream.cu",
            "accept_noalloc.cu", "accept_target.cu", "eagle2.cu",
            "kv_commit.cu", "lm_head.cu", "selftest.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

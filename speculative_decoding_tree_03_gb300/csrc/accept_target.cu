@@ -633,7 +633,11 @@ cudaError_t dispatch_target(const TargetCfg &c, const T *target, const int32_t *
 
 }  // namespace
 
-bool accept_target_supported(int V) {
+// On chip up to kMaxOnChipVocab; the streaming kernels of
+// accept_target_stream.cu above that, up to kMaxStreamVocab.
+bool accept_target_supported(int V) { return V >= 1 && V <= kMaxStreamVocab; }
+
+static bool accept_target_on_chip(int V) {
     TargetCfg c;
     return V >= 1 && target_config(1, V, &c);
 }
@@ -667,6 +671,10 @@ cudaError_t launch_accept_target(bool greedy, const float *target, const int32_t
                                  const float *u_bonus, int B, int N, int V, int32_t *accept_len,
                                  int32_t *path, int32_t *out_tokens, float *ratio,
                                  int32_t *status, cudaStream_t stream) {
+    if (!accept_target_on_chip(V))
+        return launch_accept_target_stream(greedy, target, tokens, parent, u_accept, u_bonus, B,
+                                           N, V, accept_len, path, out_tokens, ratio, status,
+                                           stream);
     return launch_target_walk(greedy, target, tokens, parent, u_accept, u_bonus, B, N, V,
                               accept_len, path, out_tokens, ratio, status, stream);
 }
@@ -677,6 +685,10 @@ cudaError_t launch_accept_target_bf16(bool greedy, const __nv_bfloat16 *target,
                                       int V, int32_t *accept_len, int32_t *path,
                                       int32_t *out_tokens, float *ratio, int32_t *status,
                                       cudaStream_t stream) {
+    if (!accept_target_on_chip(V))
+        return launch_accept_target_stream_bf16(greedy, target, tokens, parent, u_accept,
+                                                u_bonus, B, N, V, accept_len, path, out_tokens,
+                                                ratio, status, stream);
     return launch_target_walk(greedy, target, tokens, parent, u_accept, u_bonus, B, N, V,
                               accept_len, path, out_tokens, ratio, status, stream);
 }

@@ -43,7 +43,9 @@ cudaError_t launch_accept_bf16(const __nv_bfloat16 *target, const __nv_bfloat16 
                                int32_t *accept_len, int32_t *path, int32_t *out_tokens,
                                float *ratio, int32_t *status, cudaStream_t stream);
 
-// Target-only acceptance variants (accept_target.cu): greedy or one-hot q.
+// Target-only acceptance variants (accept_target.cu): greedy or one-hot q;
+// the rows of vocabularies above kMaxOnChipVocab stream from memory
+// (accept_target_stream.cu).
 bool accept_target_supported(int V);
 cudaError_t launch_accept_target(bool greedy, const float *target, const int32_t *tokens,
                                  const int32_t *parent, const float *u_accept,
@@ -56,6 +58,17 @@ cudaError_t launch_accept_target_bf16(bool greedy, const __nv_bfloat16 *target,
                                       int V, int32_t *accept_len, int32_t *path,
                                       int32_t *out_tokens, float *ratio, int32_t *status,
                                       cudaStream_t stream);
+cudaError_t launch_accept_target_stream(bool greedy, const float *target, const int32_t *tokens,
+                                        const int32_t *parent, const float *u_accept,
+                                        const float *u_bonus, int B, int N, int V,
+                                        int32_t *accept_len, int32_t *path, int32_t *out_tokens,
+                                        float *ratio, int32_t *status, cudaStream_t stream);
+cudaError_t launch_accept_target_stream_bf16(bool greedy, const __nv_bfloat16 *target,
+                                             const int32_t *tokens, const int32_t *parent,
+                                             const float *u_accept, const float *u_bonus, int B,
+                                             int N, int V, int32_t *accept_len, int32_t *path,
+                                             int32_t *out_tokens, float *ratio, int32_t *status,
+                                             cudaStream_t stream);
 
 // Arguments of one KV commit call (kv_commit.cu).
 struct KvCommitArgs {

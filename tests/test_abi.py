@@ -139,7 +139,7 @@ def test_accept_variant_argument_checks(lib):
         assert call(B=0, t=None) == 0
         assert call(t=None) == -1
         assert call(N=0) == -2 and call(N=1025) == -2
-        assert call(V=262145) == -2
+        assert call(V=786433) == -2                        # beyond the streamed vocabularies
         assert call(V=128, t=ctypes.c_void_p(260)) == -1   # float4 loads need 16-byte rows
     assert onehot(u=None) == -1
 
@@ -155,7 +155,7 @@ def test_accept_variant_bf16_argument_checks(lib):
         assert call(B=0, t=None) == 0
         assert call(t=None) == -1
         assert call(N=0) == -2 and call(N=1025) == -2
-        assert call(V=262145) == -2
+        assert call(V=786433) == -2                        # beyond the streamed vocabularies
         assert call(V=128, t=ctypes.c_void_p(260)) == -1   # 8-byte loads of four bf16
     assert onehot(u=None) == -1
 

@@ -107,6 +107,65 @@ def test_onehot_matches_oracle(sv, V):
     assert orc["accept_len"].max() >= 1
 
 
+# above 262144 the rows stream from memory (accept_target_stream.cu); 262145
+# and 300001 take the scalar loads (V % 4 != 0), 786432 is the largest
+STREAM_VOCABS = [262145, 300000, 300001, 524288, 786432]
+
+
+@pytest.mark.parametrize("V", STREAM_VOCABS)
+def test_greedy_streaming_vocabularies(sv, V):
+    # the top gaps of 3e5 draws are small: little draft noise, so walks go deep
+    a = _case(V, 6, 15, V, noise=0.05)
+    gpu = _greedy(sv, a)
+    orc = oracle.spec_accept_greedy(a["target"], a["tokens"], a["parent"])
+    for k in ("accept_len", "path", "out_tokens", "status"):
+        np.testing.assert_array_equal(gpu[k], orc[k], err_msg=k)
+    assert orc["accept_len"].max() >= 2
+
+
+@pytest.mark.parametrize("V", STREAM_VOCABS)
+def test_onehot_streaming_vocabularies(sv, V):
+    a = _case(V + 7, 4, 15, V, sigma=8.0, noise=0.7)
+    gpu = _onehot(sv, a)
+    orc = oracle.spec_accept_onehot(a["target"], a["tokens"], a["parent"], a["u_accept"],
+                                    a["u_bonus"])
+    _compare_onehot(gpu, orc, a)
+    assert orc["accept_len"].max() >= 1
+
+
+def test_onehot_streaming_flat_rows_bonus(sv):
+    """Flat rows over 524288 tokens: every child is rejected, so every
+    sequence's bonus token comes from the inverse CDF of the residual over the
+    whole streamed row, with the rejected tokens excluded."""
+    a = _case(77, 6, 7, 524288, sigma=1.0, noise=0.7)
+    gpu = _onehot(sv, a)
+    orc = oracle.spec_accept_onehot(a["target"], a["tokens"], a["parent"], a["u_accept"],
+                                    a["u_bonus"])
+    _compare_onehot(gpu, orc, a)
+
+
+def test_variants_streaming_status_and_duplicates(sv):
+    V = 300000
+    a = _case(55, 4, 7, V)
+    a["tokens"][1, 4] = V          # outside the vocabulary
+    a["parent"][2] = [-1, 0, 1, 2, 3, 4, 5]   # a chain
+    a["tokens"][2, 1:] = 7         # duplicate tokens along it
+    a["parent"][3] = [-1, 0, 0, 0, 0, 0, 0]   # five siblings, two with the same token
+    a["tokens"][3, 2] = a["tokens"][3, 1]
+    for run, ref in ((_greedy, lambda: oracle.spec_accept_greedy(a["target"], a["tokens"],
+                                                                  a["parent"])),
+                     (_onehot, lambda: oracle.spec_accept_onehot(**a))):
+        gpu = run(sv, a)
+        orc = ref()
+        assert gpu["status"].tolist() == orc["status"].tolist() == [0, 2, 0, 0]
+        assert (gpu["path"][1] == -1).all() and gpu["accept_len"][1] == 0
+        if run is _greedy:
+            for k in ("accept_len", "path", "out_tokens"):
+                np.testing.assert_array_equal(gpu[k], orc[k], err_msg=k)
+        else:
+            _compare_onehot(gpu, orc, a)
+
+
 def test_variants_many_sequences(sv):
     """More sequences than SMs at the 70B-serving vocabulary: binary trees."""
     a = _case(99, 64, 31, 128256, noise=1.5, binary=True)
@@ -199,6 +258,22 @@ def test_onehot_bf16_matches_oracle(sv, V):
     gpu = {k: _np(v) for k, v in r.items()}
     orc = oracle.spec_accept_onehot(tf, a["tokens"], a["parent"], a["u_accept"], a["u_bonus"])
     _compare_onehot(gpu, orc, dict(a, target=tf))
+
+
+@pytest.mark.parametrize("V", [300000, 524288])
+def test_variants_bf16_streaming_vocabularies(sv, V):
+    a = _case(V + 17, 4, 15, V, sigma=8.0, noise=0.7)
+    tb, tf = _bf16(a["target"])
+    g = sv.spec_accept_greedy(tb, _dev(a["tokens"]), _dev(a["parent"]))
+    h = sv.spec_accept_onehot(tb, _dev(a["tokens"]), _dev(a["parent"]), _dev(a["u_accept"]),
+                              _dev(a["u_bonus"]))
+    torch.cuda.synchronize()
+    o = oracle.spec_accept_greedy(tf, a["tokens"], a["parent"])
+    for k in ("accept_len", "path", "out_tokens", "status"):
+        np.testing.assert_array_equal(_np(g[k]), o[k], err_msg=k)
+    _compare_onehot({k: _np(v) for k, v in h.items()},
+                    oracle.spec_accept_onehot(tf, a["tokens"], a["parent"], a["u_accept"],
+                                              a["u_bonus"]), dict(a, target=tf))
 
 
 def test_variants_bf16_many_sequences(sv):
