@@ -9,17 +9,17 @@
 //
 // One CTA = (KV head [x row block], KV chunk, sequence); up to 128 rows form
 // one half (NH = 1), up to 256 rows two halves (NH = 2). Roles:
-//   warp 0        producer: K and V tiles of 64 tokens, one TMA box per page
-//                 (16 tokens at most) and 64-dim half, 128-byte swizzle,
-//                 issued by several lanes at once into two rings (K and V).
-//                 Every box's coordinate is computed once, at kernel start,
-//                 into shared memory. It also zeroes V rows past the
-//                 sequence end in the last tile.
-//   warp 1 + h    QK issuer of half h: S_h,b = Q_h K^T (A, B from shared
-//                 memory, M=128, N=64) into S buffer b = tile parity, once
-//                 the PV that read that buffer is done. Warp 1 also owns the
+//   warps 0, 1    producers of K (warp 0) and V (warp 1): tiles of 64
+//                 tokens, one TMA box per page (64 tokens at most) and
+//                 64-dim half, 128-byte swizzle, issued by several lanes at
+//                 once into two rings. Every box's coordinate is computed
+//                 once, at kernel start, into shared memory. The V producer
+//                 also zeroes V rows past the sequence end in the last tile.
+//   warp 2 + h    QK issuer of half h: S_h,b = Q_h K^T (A, B from shared
+//                 memory, M=128, N=64) into S buffer b = tile mod SB, once
+//                 the PV that read that buffer is done. Warp 2 also owns the
 //                 tensor-memory allocation.
-//   warp 1+NH+h   PV issuer of half h: O_h += P_h,b V (A = P from tensor
+//   warp 2+NH+h   PV issuer of half h: O_h += P_h,b V (A = P from tensor
 //                 memory, B = V MN-major) once the softmax wrote P.
 //                 A thread issuing tcgen05.mma sustains about one MMA per 100
 //                 cycles; separate issuing warps overlap, so every chain gets
