@@ -9,9 +9,11 @@ layer (batch 64, context 32768, 31-node trees, 64/8 heads, vocabulary
 128256), the largest configuration. ``value`` is verified tree nodes per
 second (per attention layer) over all ranks, with inputs resident in HBM;
 ``e2e`` repeats the measurement through the public API from pinned host
-buffers with the copies inside the timed region (one packed host-to-device
-copy per step, issued on a side stream one step ahead, and the outputs read
-back). Between timed steps the inputs rotate over enough copies that the
+buffers with the copies inside the timed region: the prefix KV cache is
+device-resident state, and each step's inputs (queries, the tree's own K/V
+rows scattered into their cache slots, tree, uniforms, lengths, page table,
+both logits arrays) travel in one packed host-to-device copy, issued on a
+side stream one step ahead; the outputs are read back every step. Between timed steps the inputs rotate over enough copies that the
 working set exceeds L2. Per-kernel times are taken inside the step: a second
 capture of the step graph carries timing events between its kernels.
 ``per_workload`` repeats the step measurement on the four other workloads.
@@ -759,26 +761,47 @@ def run_ours(args, w, idx):
     ms100 = rmax(ms100_local)
 
     # ---- end to end through the public API from pinned host buffers. The
-    # inputs of a step sit in one pinned host buffer and travel in one copy
-    # into one of two device buffers whose slices the step's tensors view; a
-    # side stream copies step i + 1 while step i runs (double buffering), and
-    # every step's outputs come back to pinned host memory.
+    # KV cache of the prefix is device-resident state (written once, as a
+    # serving loop keeps it); a step's inputs are everything else: the
+    # queries, the K/V rows of the tree's own tokens (scattered into their
+    # cache slots on arrival), the tree, the uniforms, the lengths and page
+    # table, and both logits arrays. They sit in one pinned host buffer and
+    # travel in one copy into one of two device buffers whose slices the
+    # step's tensors view; a side stream copies step i + 1 while step i runs
+    # (double buffering), and every step's outputs come back to pinned host
+    # memory.
     base = r.base
+    kres, vres = base["k"], base["v"]
+    Hkv, D = kres.shape[2], kres.shape[3]
+    ps = int(inp.page_size)
+    slots = np.empty((B * N,), np.int64)
+    for b in range(B):
+        pos = int(inp.seq_lens[b]) + np.arange(N)
+        slots[b * N:(b + 1) * N] = inp.page_table[b, pos // ps].astype(np.int64) * ps + pos % ps
+    kflat_h = kres.view(-1, Hkv, D)
+    slots_d = torch.from_numpy(slots).to(dev)
+    step_in = {k: v for k, v in base.items() if k not in ("k", "v")}
+    step_in["tree_k"] = kflat_h.index_select(0, slots_d)
+    step_in["tree_v"] = vres.view(-1, Hkv, D).index_select(0, slots_d)
+    step_in["slots"] = slots_d
     offs, total = {}, 0
-    for k, v in base.items():
+    for k, v in step_in.items():
         nbytes = v.numel() * v.element_size()
         offs[k] = (total, nbytes, v.shape, v.dtype)
         total += (nbytes + 255) & ~255
     host_in = torch.empty((total,), dtype=torch.uint8).pin_memory()
     for k, (o, nbytes, _, _) in offs.items():
-        host_in[o:o + nbytes].copy_(base[k].reshape(-1).view(torch.uint8).cpu())
-    # the resident input copies are no longer needed: make room for the two
-    # end-to-end device buffers
+        host_in[o:o + nbytes].copy_(step_in[k].reshape(-1).view(torch.uint8).cpu())
+    del step_in
+    # the rotated input copies are no longer needed: make room for the two
+    # end-to-end device buffers (the resident cache stays)
     r.sets = [r.base]
     torch.cuda.empty_cache()
     dbufs = [torch.empty((total,), dtype=torch.uint8, device=dev) for _ in range(2)]
     dsets = [{k: buf[o:o + nbytes].view(dt).view(shape)
               for k, (o, nbytes, shape, dt) in offs.items()} for buf in dbufs]
+    for ds in dsets:
+        ds["k"], ds["v"] = kres, vres
     h2d = sum(nbytes for _, nbytes, _, _ in offs.values())
     out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
     res_h = {k: torch.empty((B, N) if k in ("path", "out_tokens") else (B,),
@@ -805,7 +828,11 @@ def run_ours(args, w, idx):
                 issue_copy(i + 1)
             j = i % len(dbufs)
             stream.wait_event(copied[j])
-            r.step(dsets[j])
+            ds = dsets[j]
+            # the tree's K/V rows into their cache slots, then the step
+            kres.view(-1, Hkv, D).index_copy_(0, ds["slots"], ds["tree_k"])
+            vres.view(-1, Hkv, D).index_copy_(0, ds["slots"], ds["tree_v"])
+            r.step(ds)
             used[j].record(stream)
             out_h.copy_(r.out, non_blocking=True)
             for k in res_h:
@@ -886,8 +913,10 @@ def run_ours(args, w, idx):
             "attn_chunks": args.attn_chunks or "library's choice",
             "attn_kernel": {0: "library's choice", 1: "chunks merged in clusters",
                             2: "persistent, one CTA per SM"}[args.attn_kernel],
-            "e2e_copies": "one packed pinned host-to-device copy per step, issued one step "
-                          "ahead on a side stream; outputs read back every step",
+            "e2e_copies": "the prefix KV cache resident on the device; per step one packed "
+                          "pinned host-to-device copy of the step's inputs (queries, the tree's "
+                          "K/V rows, tree, uniforms, lengths, page table, both logits arrays), "
+                          "issued one step ahead on a side stream; outputs read back every step",
         },
         "accept_steps_per_s": rsum(B) / (ms / 1e3),
         "graph_100_steps": {"ms_per_step": ms100, "value": rsum(B * N) / (ms100 / 1e3),
