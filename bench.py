@@ -771,6 +771,12 @@ def run_ours(args, w, idx):
     # (double buffering), and every step's outputs come back to pinned host
     # memory.
     base = r.base
+    # the outputs of one device-resident step on these inputs: the end-to-end
+    # steps must reproduce them bit for bit
+    r.step(base)
+    torch.cuda.synchronize(dev)
+    ref_out = r.out.clone().cpu()
+    ref_res = {k: acc_out[k].clone().cpu() for k in ("accept_len", "path", "out_tokens", "status")}
     kres, vres = base["k"], base["v"]
     Hkv, D = kres.shape[2], kres.shape[3]
     ps = int(inp.page_size)
@@ -849,6 +855,12 @@ def run_ours(args, w, idx):
     e2e_ms = rmax(e0.elapsed_time(e1) / args.steps)
     e2e_value = rsum(B * N) / (e2e_ms / 1e3)
     r.check()
+    torch.cuda.synchronize(dev)
+    assert torch.equal(out_h.view(torch.int16) if out_h.dtype == torch.bfloat16 else out_h,
+                       ref_out.view(torch.int16) if ref_out.dtype == torch.bfloat16 else ref_out), \
+        "end-to-end attention output differs from the device-resident step"
+    for k, v in ref_res.items():
+        assert torch.equal(res_h[k], v), f"end-to-end {k} differs from the device-resident step"
 
     if rank != 0:
         if world > 1:
