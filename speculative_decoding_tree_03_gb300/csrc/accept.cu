@@ -252,7 +252,17 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
 
     pdl_wait();
     pdl_launch_dependents();
-    // the root's rows go out first: their latency hides behind the set-up
+    // This thread's own tree entry is read first: the set-up waits for it,
+    // and loads issued after the root's rows would return behind them.
+    const int i0 = threadIdx.x;
+    int pp0 = -1, tk0 = 0;
+    float ua0 = 0.0f;
+    if (i0 < N) {
+        pp0 = parent[base + i0];
+        tk0 = tokens[base + i0];
+        ua0 = u_accept[base + i0];
+    }
+    // the root's rows go out next: their latency hides behind the set-up
     float4 P[E4], Q[E4];
     load_slice<E4, VEC>(target + base * V, V, g0, lane, P);
     if (N > 1) {
@@ -260,6 +270,16 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
     } else {
 #pragma unroll
         for (int k = 0; k < E4; ++k) Q[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // then node i0's token logits at its parent's rows (a parent's draft row
+    // is read because it has a child), when both of its indexes are valid; an
+    // invalid tree is reported below and nothing else is read. Node i0 keeps
+    // the pair in registers until the first test, so these loads overlap the
+    // set-up and the root's statistics.
+    float2 lx_mine = make_float2(0.0f, 0.0f);
+    if (i0 > 0 && i0 < N && pp0 >= 0 && pp0 < i0 && tk0 >= 0 && tk0 < V) {
+        const size_t row = (base + pp0) * (size_t)V + tk0;
+        lx_mine = make_float2(ldg_logit(target + row), ldg_logit(draft + row));
     }
 
     // ---- the tree: parents, tokens, uniforms; validity; child lists
@@ -271,11 +291,12 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
     __syncthreads();
     int bad = 0;
     for (int i = threadIdx.x; i < N; i += NT) {
-        const int pp = parent[base + i];
-        const int tk = tokens[base + i];
+        const bool mine = i == i0;
+        const int pp = mine ? pp0 : parent[base + i];
+        const int tk = mine ? tk0 : tokens[base + i];
         sp[i] = pp;
         stok[i] = tk;
-        su[i] = u_accept[base + i];
+        su[i] = mine ? ua0 : u_accept[base + i];
         const bool pok = i == 0 ? pp == -1 : (pp >= 0 && pp < i);
         if (!pok) bad |= SVF_DEV_BAD_PARENT;
         if (i > 0 && (tk < 0 || tk >= V)) bad |= SVF_DEV_BAD_TOKEN;
@@ -304,11 +325,8 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
     // peers may push records once every CTA's barriers are initialised
     if (CLUSTER) cluster_arrive();
 
-    // siblings in ascending index order; every child's token logits at its
-    // parent's rows (a parent's draft row is read because it has a child).
-    // Node threadIdx.x keeps its pair in registers until the first test, so
-    // those loads overlap the root's statistics.
-    float2 lx_mine = make_float2(0.0f, 0.0f);
+    // siblings in ascending index order; the token logits of the nodes past
+    // the first NT at their parents' rows
     for (int i = threadIdx.x; i < N; i += NT) {
         if (sfirst[i] == INT_MAX) sfirst[i] = -1;
         int nx = -1;
@@ -319,10 +337,8 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
                     nx = c;
                     break;
                 }
-            const size_t row = (base + pp) * (size_t)V + stok[i];
-            if (i < NT) {
-                lx_mine = make_float2(ldg_logit(target + row), ldg_logit(draft + row));
-            } else {
+            if (i >= NT) {
+                const size_t row = (base + pp) * (size_t)V + stok[i];
                 slx[i] = make_float2(ldg_logit(target + row), ldg_logit(draft + row));
             }
         }

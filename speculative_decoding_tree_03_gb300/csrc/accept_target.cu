@@ -185,8 +185,23 @@ __global__ void __launch_bounds__(NT, 1) accept_target_kernel(
 
     pdl_wait();
     pdl_launch_dependents();
+    // This thread's own tree entry is read first: the set-up waits for it,
+    // and loads issued after the root's row would return behind them.
+    const int i0 = threadIdx.x;
+    int pp0 = -1, tk0 = 0;
+    float ua0 = 0.0f;
+    if (i0 < N) {
+        pp0 = parent[base + i0];
+        tk0 = tokens[base + i0];
+        if (!GREEDY) ua0 = u_accept[base + i0];
+    }
     float4 P[E4];
     load_row<E4, VEC>(target + base * V, V, g0, lane, P);
+    // one-hot: node i0's token logit at its parent's row, when both of its
+    // indexes are valid (an invalid tree is reported below)
+    float lx0 = 0.0f;
+    if (!GREEDY && i0 > 0 && i0 < N && pp0 >= 0 && pp0 < i0 && tk0 >= 0 && tk0 < V)
+        lx0 = logit_at(target + (base + pp0) * (size_t)V + tk0);
 
     // ---- the tree: parents, tokens, uniforms; validity; child lists
     if (threadIdx.x == 0) {
@@ -197,11 +212,12 @@ __global__ void __launch_bounds__(NT, 1) accept_target_kernel(
     __syncthreads();
     int bad = 0;
     for (int i = threadIdx.x; i < N; i += NT) {
-        const int pp = parent[base + i];
-        const int tk = tokens[base + i];
+        const bool mine = i == i0;
+        const int pp = mine ? pp0 : parent[base + i];
+        const int tk = mine ? tk0 : tokens[base + i];
         sp[i] = pp;
         stok[i] = tk;
-        su[i] = GREEDY ? 0.0f : u_accept[base + i];
+        su[i] = GREEDY ? 0.0f : (mine ? ua0 : u_accept[base + i]);
         const bool pok = i == 0 ? pp == -1 : (pp >= 0 && pp < i);
         if (!pok) bad |= SVF_DEV_BAD_PARENT;
         if (i > 0 && (tk < 0 || tk >= V)) bad |= SVF_DEV_BAD_TOKEN;
@@ -239,7 +255,8 @@ __global__ void __launch_bounds__(NT, 1) accept_target_kernel(
                     nx = c;
                     break;
                 }
-            if (!GREEDY) slx[i] = logit_at(target + (base + pp) * (size_t)V + stok[i]);
+            if (!GREEDY)
+                slx[i] = i == i0 ? lx0 : logit_at(target + (base + pp) * (size_t)V + stok[i]);
         }
         snext[i] = nx;
     }

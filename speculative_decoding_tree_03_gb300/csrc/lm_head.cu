@@ -138,6 +138,11 @@ __global__ void __launch_bounds__(lmh::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Each cluster starts its k loop at its own offset (spread evenly over
+        // H) and wraps around: clusters that start together then read
+        // different columns of their weight rows instead of the same 128-byte
+        // column of every row. The sum over k is the same set of terms.
+        const int rot = (int)((long long)cluster_id * p.kblocks / num_clusters) % p.kblocks;
         bool ok = true;
         for (int i = 0; i < my_groups && ok; ++i) {
             const int g = cluster_id + i * num_clusters;
@@ -146,18 +151,19 @@ __global__ void __launch_bounds__(lmh::THREADS, 1)
             const int n0 = nt * p.BN;
             for (int kb = 0; kb < p.kblocks; ++kb) {
                 const int s = issued % S, use = issued / S;
+                const int kc = (kb + rot < p.kblocks ? kb + rot : kb + rot - p.kblocks) * BK;
                 if (use > 0 &&
                     !(ok = lmh_warp_wait(&empty[s], (uint32_t)((use - 1) & 1), abort_flag,
                                          p.wait_ns)))
                     break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(A_BYTES + b_bytes));
-                    tma_load_2d(sA + s * A_BYTES, &tmw, kb * BK, m0, &full[s]);
+                    tma_load_2d(sA + s * A_BYTES, &tmw, kc, m0, &full[s]);
                     if (p.C == 1)
-                        tma_load_2d(sB + s * b_bytes, &tmh, kb * BK, n0, &full[s]);
+                        tma_load_2d(sB + s * b_bytes, &tmh, kc, n0, &full[s]);
                     else
                         tma_load_2d_multicast(sB + s * b_bytes + (int)rank * slice_rows * 128,
-                                              &tmh, kb * BK, n0 + (int)rank * slice_rows,
+                                              &tmh, kc, n0 + (int)rank * slice_rows,
                                               &full[s], mask);
                 }
                 __syncwarp();
