@@ -344,6 +344,9 @@ __global__ void __launch_bounds__(NT, 1) accept_walk_kernel(
         }
         snext[i] = nx;
     }
+    // every thread reads the child lists from here on (a root without
+    // children is marked -1 just above)
+    __syncthreads();
     if (CLUSTER) cluster_wait();
 
     // One exchange: warp 0 pushes this CTA's record into slot `rank` of every

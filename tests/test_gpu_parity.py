@@ -439,9 +439,31 @@ def test_accept_root_only_and_chain(sv):
     orc = oracle.spec_accept(**arrs)
     compare_accept(gpu, arrs, orc)
     assert (gpu["accept_len"] == 0).all()
+    # a lone root with several warps per CTA (V = 3001), clusters (40000,
+    # 128256 with B = 24, the widest register slices) and the streamed walk
+    # (300000): the root is a leaf, so every thread must see it as one
+    for seed, B, V in ((24, 8, 3001), (25, 8, 40000), (27, 24, 128256), (26, 3, 300000)):
+        arrs = _synthetic_accept(seed, B, 1, V, [-1])
+        gpu = _accept_gpu(sv, arrs)
+        compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
+        assert (gpu["accept_len"] == 0).all() and (gpu["status"] == 0).all()
+        assert (gpu["out_tokens"][:, 0] >= 0).all()
     arrs = _synthetic_accept(22, 32, 12, 3000, chain_parent(12), sigma=1.0, noise=0.3)
     gpu = _accept_gpu(sv, arrs)
     compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
+
+
+@pytest.mark.parametrize("V", [3000, 40000])
+def test_accept_star_tree(sv, V):
+    """One node with 40 children and a second level below two of them: every
+    child's token logits at the root's rows come from the threads that hold
+    them, 40 pairs on one exchange; tokens drawn i.i.d. from q, so siblings
+    repeat tokens."""
+    parent = [-1] + [0] * 40 + [1] * 3 + [2] * 3
+    arrs = _synthetic_accept(40 + V % 7, 16, len(parent), V, parent, sigma=1.0, noise=0.3)
+    gpu = _accept_gpu(sv, arrs)
+    compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
+    assert (gpu["status"] == 0).all()
 
 
 def test_accept_status_errors(sv):
