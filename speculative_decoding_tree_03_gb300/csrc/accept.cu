@@ -36,6 +36,10 @@
 #include <limits.h>
 #include <math.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -47,6 +51,11 @@ namespace acc {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = 16;
 constexpr int kLargeThreads = 512;  // threads per CTA of the clustered variants
+// The wide variant for large batches: 11 warps x 16 slots per lane and row,
+// the largest slices the register file holds, so a sequence needs fewer CTAs
+// and more clusters are resident at once.
+constexpr int kWideThreads = 352;
+constexpr int kWideSlots = 16;
 }  // namespace acc
 
 // 2^(l log2 e - ml2): e^(l - m) for ml2 = m log2 e, in one FFMA and one MUFU op.
@@ -725,6 +734,45 @@ cudaError_t launch_walk(const WalkCfg &c, const T *target, const T *draft,
                       accept_len, path, out_tokens, ratio, status);
 }
 
+// Clusters of `cl` CTAs of `kern` that can be resident at once on the
+// current device, from the occupancy calculator (cached); 0 if unknown.
+template <typename K>
+int resident_clusters(K kern, int nt, size_t smem, int cl) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, int, size_t, int, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const auto key = std::make_tuple(reinterpret_cast<const void *>(kern), nt, smem, cl, dev);
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    bool ok = true;
+    if (cl > 8)
+        ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+             cudaSuccess;
+    if (ok && smem > 48 * 1024)
+        ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+             cudaSuccess;
+    if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)cl);
+        cfg.blockDim = dim3((unsigned)nt);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)cl;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    if (n == 0) (void)cudaGetLastError();  // a failed query leaves no sticky error
+    cache[key] = n;
+    return n;
+}
+
 template <bool VEC, typename T>
 cudaError_t dispatch_walk(const WalkCfg &c, const T *target, const T *draft,
                           const int32_t *tokens, const int32_t *parent, const float *u_accept,
@@ -736,6 +784,21 @@ cudaError_t dispatch_walk(const WalkCfg &c, const T *target, const T *draft,
                                               u_bonus,                                         \
                                            B, N, V, accept_len, path, out_tokens, ratio, status, \
                                            stream)
+    if (c.nt == acc::kLargeThreads && c.e4 == 8 && (long long)B * c.cl > num_sms()) {
+        // More sequences than one wave of the widest 512-thread slices: take
+        // the wide variant when its smaller clusters need fewer waves.
+        constexpr int cap = acc::kWideThreads / 32 * 128 * acc::kWideSlots;
+        WalkCfg w{acc::kWideThreads, acc::kWideSlots, ceil_div(V, (long long)cap)};
+        const int r8 = resident_clusters(accept_walk_kernel<acc::kLargeThreads, 8, VEC, true, T>,
+                                         acc::kLargeThreads, walk_smem(N, c), c.cl);
+        const int rw = resident_clusters(
+            accept_walk_kernel<acc::kWideThreads, acc::kWideSlots, VEC, true, T>,
+            acc::kWideThreads, walk_smem(N, w), w.cl);
+        if (r8 > 0 && rw > 0 && w.cl <= acc::kMaxCluster && ceil_div(B, rw) < ceil_div(B, r8))
+            return launch_walk<acc::kWideThreads, acc::kWideSlots, VEC, true, T>(
+                w, target, draft, tokens, parent, u_accept, u_bonus, B, N, V, accept_len, path,
+                out_tokens, ratio, status, stream);
+    }
     if (c.nt == 32) {
         if (c.e4 == 1) SVF_WALK(32, 1, false);
         SVF_WALK(32, 4, false);

@@ -453,6 +453,22 @@ def test_accept_root_only_and_chain(sv):
     compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
 
 
+@pytest.mark.parametrize("V,bf16", [(128256, False), (128255, False), (100000, True)])
+def test_accept_wide_slices(sv, V, bf16):
+    """Batches of 48 sequences at vocabularies where the widest 512-thread
+    slices need more than one wave of clusters: the library then takes the
+    352-thread, 16-slot slices when their smaller clusters need fewer waves.
+    Vector and scalar loads, fp32 and bf16 rows."""
+    arrs = _synthetic_accept(60 + V % 11, 48, 7, V, [-1, 0, 0, 1, 1, 2, 2], sigma=2.0, noise=0.7)
+    if bf16:
+        gpu, wide = _accept_gpu_bf16(sv, arrs)
+        compare_accept(gpu, wide, oracle.spec_accept(**wide))
+    else:
+        gpu = _accept_gpu(sv, arrs)
+        compare_accept(gpu, arrs, oracle.spec_accept(**arrs))
+    assert (gpu["status"] == 0).all()
+
+
 @pytest.mark.parametrize("V", [3000, 40000])
 def test_accept_star_tree(sv, V):
     """One node with 40 children and a second level below two of them: every
