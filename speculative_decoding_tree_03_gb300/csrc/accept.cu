@@ -36,10 +36,6 @@
 #include <limits.h>
 #include <math.h>
 
-#include <map>
-#include <mutex>
-#include <tuple>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -734,45 +730,6 @@ cudaError_t launch_walk(const WalkCfg &c, const T *target, const T *draft,
                       accept_len, path, out_tokens, ratio, status);
 }
 
-// Clusters of `cl` CTAs of `kern` that can be resident at once on the
-// current device, from the occupancy calculator (cached); 0 if unknown.
-template <typename K>
-int resident_clusters(K kern, int nt, size_t smem, int cl) {
-    static std::mutex mu;
-    static std::map<std::tuple<const void *, int, size_t, int, int>, int> cache;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const auto key = std::make_tuple(reinterpret_cast<const void *>(kern), nt, smem, cl, dev);
-    std::lock_guard<std::mutex> lock(mu);
-    const auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-    int n = 0;
-    bool ok = true;
-    if (cl > 8)
-        ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-             cudaSuccess;
-    if (ok && smem > 48 * 1024)
-        ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
-             cudaSuccess;
-    if (ok) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)cl);
-        cfg.blockDim = dim3((unsigned)nt);
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = (unsigned)cl;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
-    }
-    if (n == 0) (void)cudaGetLastError();  // a failed query leaves no sticky error
-    cache[key] = n;
-    return n;
-}
-
 template <bool VEC, typename T>
 cudaError_t dispatch_walk(const WalkCfg &c, const T *target, const T *draft,
                           const int32_t *tokens, const int32_t *parent, const float *u_accept,
@@ -784,9 +741,12 @@ cudaError_t dispatch_walk(const WalkCfg &c, const T *target, const T *draft,
                                               u_bonus,                                         \
                                            B, N, V, accept_len, path, out_tokens, ratio, status, \
                                            stream)
-    if (c.nt == acc::kLargeThreads && c.e4 == 8 && (long long)B * c.cl > num_sms()) {
+    if (sizeof(T) == 4 && c.nt == acc::kLargeThreads && c.e4 == 8 &&
+        (long long)B * c.cl > num_sms()) {
         // More sequences than one wave of the widest 512-thread slices: take
-        // the wide variant when its smaller clusters need fewer waves.
+        // the wide variant when its smaller clusters need fewer waves (fp32
+        // rows; on bf16 rows it measured slower: 78.6 against 71-74 us on
+        // the 70B batch).
         constexpr int cap = acc::kWideThreads / 32 * 128 * acc::kWideSlots;
         WalkCfg w{acc::kWideThreads, acc::kWideSlots, ceil_div(V, (long long)cap)};
         const int r8 = resident_clusters(accept_walk_kernel<acc::kLargeThreads, 8, VEC, true, T>,

@@ -40,6 +40,7 @@ namespace tgt {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = 16;
 constexpr int kClusterThreads = 512;
+constexpr int kWideSlots = 16;  // slots per lane for large batches (one row in registers)
 constexpr int kSmallThreads = 128;
 
 // Elements past V read as -inf.
@@ -631,6 +632,23 @@ cudaError_t dispatch_target(const TargetCfg &c, const T *target, const int32_t *
     return launch_target<NT_, E4_, VEC, CL_, GREEDY, T>(c, target, tokens, parent, u_accept,    \
                                                      u_bonus, B, N, V, accept_len, path,        \
                                                      out_tokens, ratio, status, stream)
+    if (c.nt == tgt::kClusterThreads && c.e4 == 8 && (long long)B * c.cl > num_sms()) {
+        // More sequences than one wave of 8-slot clusters: 16 slots per lane
+        // halve the cluster, taken when that needs fewer waves.
+        TargetCfg w{tgt::kClusterThreads, tgt::kWideSlots,
+                    cdiv(V, (long long)tgt::kClusterThreads * 4 * tgt::kWideSlots)};
+        const size_t smem = (size_t)N * 6 * sizeof(int32_t);
+        const int r8 = resident_clusters(
+            accept_target_kernel<tgt::kClusterThreads, 8, VEC, true, GREEDY, T>,
+            tgt::kClusterThreads, smem, c.cl);
+        const int rw = resident_clusters(
+            accept_target_kernel<tgt::kClusterThreads, tgt::kWideSlots, VEC, true, GREEDY, T>,
+            tgt::kClusterThreads, smem, w.cl);
+        if (r8 > 0 && rw > 0 && cdiv(B, rw) < cdiv(B, r8))
+            return launch_target<tgt::kClusterThreads, tgt::kWideSlots, VEC, true, GREEDY, T>(
+                w, target, tokens, parent, u_accept, u_bonus, B, N, V, accept_len, path,
+                out_tokens, ratio, status, stream);
+    }
     if (c.nt == tgt::kSmallThreads) {
         switch (c.e4) {
             case 1: SVF_TGT(tgt::kSmallThreads, 1, false);

@@ -5,6 +5,10 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "specverify.h"
 
 namespace svf {
@@ -170,6 +174,46 @@ int launch_lm_head(const void *hidden, const void *weight, int R, int H, int V, 
                    int32_t *status, cudaStream_t stream);
 
 int num_sms();
+
+// Clusters of `cl` CTAs of `kern` that can be resident at once on the
+// current device, from the occupancy calculator (cached); 0 if unknown.
+template <typename K>
+inline int resident_clusters(K kern, int nt, size_t smem, int cl) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, int, size_t, int, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const auto key = std::make_tuple(reinterpret_cast<const void *>(kern), nt, smem, cl, dev);
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    bool ok = true;
+    if (cl > 8)
+        ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+             cudaSuccess;
+    if (ok && smem > 48 * 1024)
+        ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+             cudaSuccess;
+    if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)cl);
+        cfg.blockDim = dim3((unsigned)nt);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)cl;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    if (n == 0) (void)cudaGetLastError();  // a failed query leaves no sticky error
+    cache[key] = n;
+    return n;
+}
+
 
 // Launch with programmatic stream serialization (and a cluster size when
 // cluster_x > 0): the kernel may be scheduled while the previous kernel on the stream

@@ -456,9 +456,10 @@ def test_accept_root_only_and_chain(sv):
 @pytest.mark.parametrize("V,bf16", [(128256, False), (128255, False), (100000, True)])
 def test_accept_wide_slices(sv, V, bf16):
     """Batches of 48 sequences at vocabularies where the widest 512-thread
-    slices need more than one wave of clusters: the library then takes the
-    352-thread, 16-slot slices when their smaller clusters need fewer waves.
-    Vector and scalar loads, fp32 and bf16 rows."""
+    slices need more than one wave of clusters: for fp32 rows the library
+    then takes the 352-thread, 16-slot slices when their smaller clusters
+    need fewer waves (vector and scalar loads); bf16 rows keep the 512-thread
+    slices at the same batch."""
     arrs = _synthetic_accept(60 + V % 11, 48, 7, V, [-1, 0, 0, 1, 1, 2, 2], sigma=2.0, noise=0.7)
     if bf16:
         gpu, wide = _accept_gpu_bf16(sv, arrs)
