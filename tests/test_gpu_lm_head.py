@@ -61,9 +61,13 @@ def _case(seed, R, H, V):
 
 # (R, H, V): a binary tree at batch 1; odd sizes (V not a multiple of 128, R
 # not a multiple of 32); the EAGLE-2 batch at the 128K vocabulary; the
-# multicast path (R >= 512) with an odd tile width; the 70B serving shape
+# multicast path (R >= 512) with an odd tile width; the 70B serving shape;
+# a vocabulary past 2^18 with a ragged last tile, and 313 weight tiles at 200
+# rows (a second wave of 9 tiles).
 LM_CASES = [
     (31, 4096, 32000, None),
+    (7, 128, 300001, None),
+    (200, 192, 40000, None),
     (60, 256, 1000, None),
     (1000, 64, 300, None),
     (240, 4096, 128256, 6),
