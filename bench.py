@@ -533,6 +533,35 @@ def time_lm_head(sv, torch, w, dev, steps, peak, fused_inputs=None):
     return out
 
 
+def time_graph_of_steps(r: StepRunner, stream, barrier, n=100) -> float:
+    """Launch-amortised ms per step: ``n`` consecutive steps (rotating input
+    sets) captured as one CUDA graph, replayed after one warm-up replay."""
+    torch = r.torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=r.cap):
+        for i in range(n):
+            r.step(r.sets[i % r.nsets])
+    g.replay()
+    barrier()
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    g.replay()
+    h1.record(stream)
+    barrier()
+    ms = h0.elapsed_time(h1) / n
+    # a second replay for short steps, whose single replay is only a few ms
+    if ms < 1.0:
+        h0.record(stream)
+        for _ in range(3):
+            g.replay()
+        h1.record(stream)
+        barrier()
+        ms = h0.elapsed_time(h1) / (3 * n)
+    del g
+    return ms
+
+
 def workload_summary(r: StepRunner, t: dict, peak, clocks):
     """Attention and acceptance times of one workload with their roofline shares."""
     w, inp = r.w, r.inp
@@ -612,6 +641,10 @@ def run_ours(args, w, idx):
                     torch.cuda.synchronize(dev)
             r2.check()
             per_workload[w2.name] = workload_summary(r2, t2, peak, clk2.summary())
+            g100_ms = time_graph_of_steps(r2, stream, lambda: torch.cuda.synchronize(dev))
+            per_workload[w2.name]["graph_100_steps"] = {
+                "step_us": g100_ms * 1e3, "nodes_per_s": w2.B * w2.N / (g100_ms / 1e3),
+                "note": "100 steps captured as one CUDA graph"}
             if w2.dtype == "bf16":
                 per_workload[w2.name]["lm_head"] = time_lm_head(sv, torch, w2, dev,
                                                                 args.steps, peak)
@@ -636,24 +669,8 @@ def run_ours(args, w, idx):
     ms_local = t["ms"]
     ins = t["in_step"]
 
-    # launch-amortised: 100 consecutive steps (rotating input sets) captured
-    # as one CUDA graph, replayed after one warm-up replay
-    g100 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g100, stream=r.cap):
-        for i in range(100):
-            r.step(r.sets[i % r.nsets])
-    g100.replay()
-    barrier()
-    h0 = torch.cuda.Event(enable_timing=True)
-    h1 = torch.cuda.Event(enable_timing=True)
-    reps = 3 if ms_local < 1.0 else 1
-    h0.record(stream)
-    for _ in range(reps):
-        g100.replay()
-    h1.record(stream)
-    barrier()
-    ms100_local = h0.elapsed_time(h1) / (100 * reps)
-    del g100
+    # launch-amortised: 100 consecutive steps captured as one CUDA graph
+    ms100_local = time_graph_of_steps(r, stream, barrier)
 
     def timed_calls(fn, name_out=None):
         """ms per call of ``fn`` captured alone per input set, replayed K times."""
