@@ -741,23 +741,26 @@ cudaError_t dispatch_walk(const WalkCfg &c, const T *target, const T *draft,
                                               u_bonus,                                         \
                                            B, N, V, accept_len, path, out_tokens, ratio, status, \
                                            stream)
-    if (sizeof(T) == 4 && c.nt == acc::kLargeThreads && c.e4 == 8 &&
-        (long long)B * c.cl > num_sms()) {
+    if constexpr (sizeof(T) == 4) {
         // More sequences than one wave of the widest 512-thread slices: take
         // the wide variant when its smaller clusters need fewer waves (fp32
         // rows; on bf16 rows it measured slower: 78.6 against 71-74 us on
         // the 70B batch).
-        constexpr int cap = acc::kWideThreads / 32 * 128 * acc::kWideSlots;
-        WalkCfg w{acc::kWideThreads, acc::kWideSlots, ceil_div(V, (long long)cap)};
-        const int r8 = resident_clusters(accept_walk_kernel<acc::kLargeThreads, 8, VEC, true, T>,
-                                         acc::kLargeThreads, walk_smem(N, c), c.cl);
-        const int rw = resident_clusters(
-            accept_walk_kernel<acc::kWideThreads, acc::kWideSlots, VEC, true, T>,
-            acc::kWideThreads, walk_smem(N, w), w.cl);
-        if (r8 > 0 && rw > 0 && w.cl <= acc::kMaxCluster && ceil_div(B, rw) < ceil_div(B, r8))
-            return launch_walk<acc::kWideThreads, acc::kWideSlots, VEC, true, T>(
-                w, target, draft, tokens, parent, u_accept, u_bonus, B, N, V, accept_len, path,
-                out_tokens, ratio, status, stream);
+        if (c.nt == acc::kLargeThreads && c.e4 == 8 && (long long)B * c.cl > num_sms()) {
+            constexpr int cap = acc::kWideThreads / 32 * 128 * acc::kWideSlots;
+            WalkCfg w{acc::kWideThreads, acc::kWideSlots, ceil_div(V, (long long)cap)};
+            const int r8 = resident_clusters(
+                accept_walk_kernel<acc::kLargeThreads, 8, VEC, true, T>, acc::kLargeThreads,
+                walk_smem(N, c), c.cl);
+            const int rw = resident_clusters(
+                accept_walk_kernel<acc::kWideThreads, acc::kWideSlots, VEC, true, T>,
+                acc::kWideThreads, walk_smem(N, w), w.cl);
+            if (r8 > 0 && rw > 0 && w.cl <= acc::kMaxCluster &&
+                ceil_div(B, rw) < ceil_div(B, r8))
+                return launch_walk<acc::kWideThreads, acc::kWideSlots, VEC, true, T>(
+                    w, target, draft, tokens, parent, u_accept, u_bonus, B, N, V, accept_len,
+                    path, out_tokens, ratio, status, stream);
+        }
     }
     if (c.nt == 32) {
         if (c.e4 == 1) SVF_WALK(32, 1, false);

@@ -188,7 +188,7 @@ inline int resident_clusters(K kern, int nt, size_t smem, int cl) {
     const auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
-    bool ok = true;
+    bool ok = true;  // every call below succeeded
     if (cl > 8)
         ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
              cudaSuccess;
@@ -207,9 +207,13 @@ inline int resident_clusters(K kern, int nt, size_t smem, int cl) {
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            n = 0;
+            ok = false;
+        }
     }
-    if (n == 0) (void)cudaGetLastError();  // a failed query leaves no sticky error
+    // a failed query is not the caller's error: clear it (only then)
+    if (!ok) (void)cudaGetLastError();
     cache[key] = n;
     return n;
 }
